@@ -1,0 +1,37 @@
+"""CPU oracle for speculative-decoding verification.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product path (the CUDA library and its Python binding) never imports, calls
+or links anything here, and this package imports nothing from it: the two
+share no code, constants or helpers.  Inputs come from ``workloads`` (data
+only) or from the tests themselves.
+
+What it computes follows the spec-verify model card (sections "Method",
+"Correctness", "Requirements and limits") and the llmstudio.ru explainer
+"Как работает speculative decoding и MTP при инференсе LLM" (sections 13,
+15-17, 38, 47, 48).  Every function is pinned by ``tests/test_oracle_*.py``
+against values the pages print, closed forms, exact enumeration or brute
+force; none is "parity unpinned".
+"""
+
+from .spec_verify import (  # noqa: F401
+    BAD_TOKEN,
+    BAD_VALUE,
+    ZERO_MASS,
+    NEAR_BOUNDARY,
+    BAD_LAYOUT,
+    BOUNDARY_REL_TOL,
+    Result,
+    decode_rows,
+    exact_mass_int,
+    exact_mass,
+    argmax_lowest,
+    accept_decision,
+    inverse_cdf_draw,
+    verify_greedy,
+    accept,
+    accept_from_logits,
+    softmax_fp64,
+    warped_rows_f32,
+)
