@@ -1,0 +1,21 @@
+"""GB300-native verification step of speculative decoding.
+
+Greedy verification and Leviathan/Chen rejection sampling for B sequences in
+one kernel launch (libsv.so, C ABI in include/sv.h); this package is the thin
+PyTorch binding.  See the spec-verify model card, sections "Method" and
+"Correctness", for what is computed.
+"""
+
+from ._lib import (  # noqa: F401
+    FLAG_FORCE_EXACT,
+    SEQ_BAD_LAYOUT,
+    SEQ_BAD_TOKEN,
+    SEQ_BAD_VALUE,
+    SEQ_EXACT_PATH,
+    SEQ_NEAR_BOUNDARY,
+    SEQ_TIMEOUT,
+    SEQ_ZERO_MASS,
+    load as load_library,
+)
+from .api import SVError, VerifyResult, accept, accept_from_logits, verify_greedy  # noqa: F401
+from ._build import build  # noqa: F401

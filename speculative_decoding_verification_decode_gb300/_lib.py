@@ -1,0 +1,56 @@
+"""ctypes declarations of the C ABI in include/sv.h (loads lib/libsv.so)."""
+
+import ctypes
+import os
+import re
+
+from ._build import LIB_PATH, PKG_DIR
+
+HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "sv.h")
+
+SV_F32, SV_BF16, SV_F16 = 0, 1, 2
+SV_OK, SV_ERR_ARG, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3
+SEQ_BAD_TOKEN, SEQ_BAD_VALUE, SEQ_ZERO_MASS, SEQ_NEAR_BOUNDARY = 1, 2, 4, 8
+SEQ_EXACT_PATH, SEQ_TIMEOUT, SEQ_BAD_LAYOUT = 16, 32, 64
+FLAG_FORCE_EXACT = 1
+
+_vp = ctypes.c_void_p
+_i32, _i64, _u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+
+SIGNATURES = {
+    "sv_verify_greedy": (_i32, [_vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
+                                _vp, _vp, _vp, _u32, _vp]),
+    "sv_accept": (_i32, [_vp, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                         _vp, _vp, _vp, _u32, _vp]),
+    "sv_accept_from_logits": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
+                                     _i32, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "sv_status_string": (ctypes.c_char_p, [_i32]),
+    "sv_last_error": (ctypes.c_char_p, []),
+    "sv_version": (_i32, []),
+}
+
+_lib = None
+
+
+def header_symbols():
+    """Function names declared in include/sv.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(sv_[a-z_]+)\s*\(", text)))
+
+
+def load():
+    """Load libsv.so; raise (never fall back) if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

@@ -1,0 +1,172 @@
+"""PyTorch binding of libsv: argument marshalling only.
+
+Every step of verification runs in the CUDA kernel behind the C ABI; these
+functions only check shapes, pick the current CUDA stream and pass device
+pointers.  When the inputs live in host memory the call copies them to the
+GPU (from pinned memory when they are pinned), runs the kernel and copies the
+results back, which is how an end-to-end caller with host buffers uses it.
+"""
+
+from __future__ import annotations
+
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float32: _lib.SV_F32, torch.bfloat16: _lib.SV_BF16, torch.float16: _lib.SV_F16}
+
+
+class VerifyResult(NamedTuple):
+    n_accepted: torch.Tensor  # int32 [B]
+    next_token: torch.Tensor  # int32 [B]; -1 when the sequence's inputs are invalid
+    status: torch.Tensor  # int32 [B]; OR of SV_SEQ_* bits
+
+
+class SVError(RuntimeError):
+    pass
+
+
+def _check(rc: int):
+    if rc != _lib.SV_OK:
+        lib = _lib.load()
+        raise SVError(f"{lib.sv_status_string(rc).decode()}: {lib.sv_last_error().decode()}")
+
+
+def _rows(x: torch.Tensor) -> torch.Tensor:
+    """[rows, V] view of a 2-D or 3-D ([B, rows_per_seq, V]) input with unit
+    stride along V."""
+    if x.dim() == 3:
+        x = x.reshape(-1, x.shape[-1])
+    if x.dim() != 2:
+        raise ValueError("rows must be 2-D [rows, V] or 3-D [B, rows, V]")
+    if x.stride(1) != 1:
+        x = x.contiguous()
+    return x
+
+
+def _layout(n_target_rows: int, tokens: torch.Tensor, cu_k, k):
+    sum_k = int(tokens.numel())
+    if cu_k is None:
+        B = n_target_rows - sum_k
+        if B < 0 or (B and sum_k % B):
+            raise ValueError("target rows must be B*(K+1) for B*K draft tokens")
+        K = sum_k // B if B else 0
+        return B, K, sum_k
+    B = int(cu_k.numel()) - 1
+    if k is None:
+        raise ValueError("k (the largest K_b) is required with cu_k")
+    if n_target_rows < sum_k + B:
+        raise ValueError("target must hold sum(K_b) + B rows")
+    return B, int(k), sum_k
+
+
+class _Marshal:
+    """Moves host inputs to the device (and results back) for one call."""
+
+    def __init__(self, ref: torch.Tensor):
+        self.host = ref.device.type != "cuda"
+        self.device = torch.device("cuda", torch.cuda.current_device()) if self.host else ref.device
+
+    def dev(self, t: Optional[torch.Tensor], dtype=None) -> Optional[torch.Tensor]:
+        if t is None:
+            return None
+        if dtype is not None and t.dtype != dtype:
+            t = t.to(dtype)
+        if t.device != self.device:
+            t = t.to(self.device, non_blocking=True)
+        return t.contiguous() if t.dim() == 1 else t
+
+    def outputs(self, B: int):
+        mk = lambda: torch.empty(B, dtype=torch.int32, device=self.device)
+        return mk(), mk(), mk()
+
+    def finish(self, res: VerifyResult) -> VerifyResult:
+        if not self.host:
+            return res
+        return VerifyResult(*(x.to("cpu") for x in res))
+
+    def stream(self):
+        return ctypes_ptr(torch.cuda.current_stream(self.device).cuda_stream)
+
+
+def ctypes_ptr(v):
+    return None if v is None else int(v)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor,
+                  cu_k: Optional[torch.Tensor] = None, k: Optional[int] = None,
+                  flags: int = 0) -> VerifyResult:
+    """Greedy verification (spec-verify card, "Method"): ``target`` holds the
+    K_b + 1 rows of every sequence (probabilities or logits, f32/bf16/f16)."""
+    m = _Marshal(target)
+    tg = _rows(m.dev(target))
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(tg.shape[0], tok, cu, k)
+    n, nxt, st = m.outputs(B)
+    lib = _lib.load()
+    with torch.cuda.device(m.device):
+        _check(lib.sv_verify_greedy(_p(tg), _DTYPES[tg.dtype], tg.stride(0), _p(tok), _p(cu), B, K,
+                                    sum_k, tg.shape[1], _p(n), _p(nxt), _p(st), flags, m.stream()))
+    return m.finish(VerifyResult(n, nxt, st))
+
+
+def accept(target_probs: torch.Tensor, draft_probs: torch.Tensor, draft_tokens: torch.Tensor,
+           uniforms: torch.Tensor, cu_k: Optional[torch.Tensor] = None, k: Optional[int] = None,
+           flags: int = 0) -> VerifyResult:
+    """Speculative sampling on f32 probability rows with explicit uniforms
+    (``K_b + 1`` per sequence; the last one draws the correction or bonus)."""
+    m = _Marshal(target_probs)
+    tg = _rows(m.dev(target_probs, torch.float32))
+    dr = _rows(m.dev(draft_probs, torch.float32))
+    if dr.stride(0) != tg.stride(0):
+        dr = dr.contiguous()
+        tg = tg.contiguous()
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    u = m.dev(uniforms.reshape(-1), torch.float32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(tg.shape[0], tok, cu, k)
+    n, nxt, st = m.outputs(B)
+    lib = _lib.load()
+    with torch.cuda.device(m.device):
+        _check(lib.sv_accept(_p(tg), _p(dr), tg.stride(0), _p(tok), _p(u), _p(cu), B, K, sum_k,
+                             tg.shape[1], _p(n), _p(nxt), _p(st), flags, m.stream()))
+    return m.finish(VerifyResult(n, nxt, st))
+
+
+def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                       temperature: torch.Tensor, draft_tokens: torch.Tensor,
+                       uniforms: torch.Tensor, cu_k: Optional[torch.Tensor] = None,
+                       k: Optional[int] = None, warped_out: Optional[tuple] = None,
+                       flags: int = 0) -> VerifyResult:
+    """Mixed greedy / sampled verification from logits with a fused
+    per-sequence temperature softmax (``temperature[b] == 0`` is greedy).
+
+    ``warped_out``: optional pair of f32 device tensors ``[target_rows, V]``
+    and ``[draft_rows, V]`` that receive the warped weights of every row the
+    kernel reached (a testing aid)."""
+    m = _Marshal(target_logits)
+    tg = _rows(m.dev(target_logits))
+    dr = _rows(m.dev(draft_logits, tg.dtype))
+    if dr.stride(0) != tg.stride(0):
+        dr = dr.contiguous()
+        tg = tg.contiguous()
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    u = m.dev(uniforms.reshape(-1), torch.float32)
+    T = m.dev(temperature.reshape(-1), torch.float32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(tg.shape[0], tok, cu, k)
+    wt, wd = (None, None) if warped_out is None else warped_out
+    n, nxt, st = m.outputs(B)
+    lib = _lib.load()
+    with torch.cuda.device(m.device):
+        _check(lib.sv_accept_from_logits(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T),
+                                         _p(tok), _p(u), _p(cu), B, K, sum_k, tg.shape[1], _p(n),
+                                         _p(nxt), _p(st), _p(wt), _p(wd), flags, m.stream()))
+    return m.finish(VerifyResult(n, nxt, st))

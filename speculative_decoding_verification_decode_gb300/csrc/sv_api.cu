@@ -1,0 +1,271 @@
+// Host side of libsv.so: argument checks, launch planning, the C ABI.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sv.h"
+#include "sv_verify.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+sv_status fail(sv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+int bit_length(unsigned long long v) {
+  int n = 0;
+  while (v) {
+    ++n;
+    v >>= 1;
+  }
+  return n;
+}
+
+struct Plan {
+  int C, slice, ck_el, nck, S;
+  size_t smem;
+};
+
+// One cluster of C CTAs per sequence.  Greedy rows stream through a 4-slot
+// ring; sampling keeps a row pair (2 * nck slots) resident plus lookahead,
+// so C grows until a slice fits in the ring.
+bool make_plan(bool sampling, int B, int V, int elem, Plan& p) {
+  const int vec = 16 / elem;
+  const int ck_el = svk::kSlotBytes / elem;
+  const long long nvec = (V + vec - 1) / vec;
+  const int sms = sm_count();
+  int C = static_cast<int>((2LL * sms + B - 1) / (B > 0 ? B : 1));
+  if (C < 1) C = 1;
+  if (sampling) {
+    // at least a pair of resident slices of <= 2 slots each
+    const long long c_res = (V + 2LL * ck_el - 1) / (2LL * ck_el);
+    if (c_res > C) C = static_cast<int>(c_res > svk::kMaxCluster ? svk::kMaxCluster : c_res);
+  }
+  if (C > svk::kMaxCluster) C = svk::kMaxCluster;
+  if (C > nvec) C = static_cast<int>(nvec);
+  long long slice = (V + C - 1) / C;
+  slice = (slice + vec - 1) / vec * vec;
+  C = static_cast<int>((V + slice - 1) / slice);
+  const int nck = static_cast<int>((slice + ck_el - 1) / ck_el);
+  int S;
+  if (sampling) {
+    const int look = nck < 2 ? nck : 2;
+    S = 2 * nck + (look > 0 ? look : 1);
+  } else {
+    S = 4;
+  }
+  if (S > svk::kMaxSlots) return false;
+  p.C = C;
+  p.slice = static_cast<int>(slice);
+  p.ck_el = ck_el;
+  p.nck = nck;
+  p.S = S;
+  p.smem = static_cast<size_t>(S) * svk::kSlotBytes + sizeof(svk::SmemTail);
+  return true;
+}
+
+template <int MODE, typename T>
+sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
+  auto kern = svk::sv_verify_kernel<MODE, T>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(smem): %s", cudaGetErrorString(e));
+  if (pl.C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess)
+      return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(cluster): %s", cudaGetErrorString(e));
+  }
+  prm.slice = pl.slice;
+  prm.ck_el = pl.ck_el;
+  prm.S = pl.S;
+  const unsigned gy = static_cast<unsigned>(prm.B < 65535 ? prm.B : 65535);
+  const unsigned gz = static_cast<unsigned>((prm.B + gy - 1) / gy);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.C), gy, gz);
+  cfg.blockDim = dim3(svk::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(pl.C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+  if (clusters < 1)
+    return fail(SV_ERR_UNSUPPORTED, "no cluster of %d CTAs with %zu B shared memory fits", pl.C, pl.smem);
+  e = cudaLaunchKernelEx(&cfg, kern, prm);
+  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return SV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sv_status check_common(const void* target, int64_t row_stride, const int32_t* tokens,
+                       const int32_t* cu_k, int32_t B, int32_t K, int32_t sum_k, int32_t V,
+                       const int32_t* n_out, const int32_t* next_out, const uint32_t* st_out,
+                       uint32_t flags) {
+  g_err[0] = '\0';
+  if (B < 0) return fail(SV_ERR_ARG, "batch must be >= 0 (got %d)", B);
+  if (K < 0) return fail(SV_ERR_ARG, "k must be >= 0 (got %d)", K);
+  if (V < 1) return fail(SV_ERR_ARG, "vocab must be >= 1 (got %d)", V);
+  if (sum_k < 0) return fail(SV_ERR_ARG, "sum_k must be >= 0 (got %d)", sum_k);
+  if (row_stride < V) return fail(SV_ERR_ARG, "row_stride (%lld) < vocab (%d)", (long long)row_stride, V);
+  if (!cu_k && static_cast<long long>(B) * K != sum_k)
+    return fail(SV_ERR_ARG, "without cu_k, sum_k must equal batch * k (%lld), got %d",
+                static_cast<long long>(B) * K, sum_k);
+  if (static_cast<long long>(sum_k) + B > 0x7FFFFFFFLL)
+    return fail(SV_ERR_ARG, "too many rows (sum_k + batch > 2^31 - 1)");
+  if (flags & ~static_cast<uint32_t>(SV_FLAG_FORCE_EXACT)) return fail(SV_ERR_ARG, "unknown flag bits 0x%x", flags);
+  if (B == 0) return SV_OK;
+  if (!target) return fail(SV_ERR_ARG, "target pointer is NULL");
+  if (sum_k > 0 && !tokens) return fail(SV_ERR_ARG, "draft_tokens is NULL");
+  if (!n_out || !next_out || !st_out) return fail(SV_ERR_ARG, "an output pointer is NULL");
+  return SV_OK;
+}
+
+svk::Params base_params(const void* tgt, const void* drf, int64_t stride, const int32_t* tok,
+                        const float* uni, const int32_t* cu_k, const float* temp, int B, int K,
+                        int V, int sum_k, int32_t* n_out, int32_t* next_out, uint32_t* st_out,
+                        uint32_t flags) {
+  svk::Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.tgt = tgt;
+  p.drf = drf;
+  p.stride = stride;
+  p.tok = tok;
+  p.uni = uni;
+  p.cu_k = cu_k;
+  p.temp = temp;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.sum_k = sum_k;
+  p.n_out = n_out;
+  p.next_out = next_out;
+  p.st_out = st_out;
+  p.flags = flags;
+  p.fixed_shift = 62 - bit_length(static_cast<unsigned long long>(V));
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status sv_verify_greedy(const void* target, sv_dtype dtype, int64_t row_stride,
+                           const int32_t* draft_tokens, const int32_t* cu_k, int32_t batch,
+                           int32_t k, int32_t sum_k, int32_t vocab, int32_t* n_accepted,
+                           int32_t* next_token, uint32_t* status, uint32_t flags, void* stream) {
+  sv_status s = check_common(target, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
+                             n_accepted, next_token, status, flags);
+  if (s != SV_OK || batch == 0) return s;
+  if (dtype != SV_F32 && dtype != SV_BF16 && dtype != SV_F16)
+    return fail(SV_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  const int elem = dtype == SV_F32 ? 4 : 2;
+  Plan pl;
+  if (!make_plan(false, batch, vocab, elem, pl)) return fail(SV_ERR_UNSUPPORTED, "vocab %d too large", vocab);
+  svk::Params p = base_params(target, nullptr, row_stride, draft_tokens, nullptr, cu_k, nullptr,
+                              batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
+  p.use_tma = aligned16(target) && (row_stride * elem) % 16 == 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case SV_F32: return launch<svk::MODE_GREEDY, float>(p, pl, st);
+    case SV_BF16: return launch<svk::MODE_GREEDY, __nv_bfloat16>(p, pl, st);
+    default: return launch<svk::MODE_GREEDY, __half>(p, pl, st);
+  }
+}
+
+sv_status sv_accept(const float* target_probs, const float* draft_probs, int64_t row_stride,
+                    const int32_t* draft_tokens, const float* uniforms, const int32_t* cu_k,
+                    int32_t batch, int32_t k, int32_t sum_k, int32_t vocab, int32_t* n_accepted,
+                    int32_t* next_token, uint32_t* status, uint32_t flags, void* stream) {
+  sv_status s = check_common(target_probs, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
+                             n_accepted, next_token, status, flags);
+  if (s != SV_OK || batch == 0) return s;
+  if (sum_k > 0 && !draft_probs) return fail(SV_ERR_ARG, "draft_probs is NULL");
+  if (!uniforms) return fail(SV_ERR_ARG, "uniforms is NULL");
+  Plan pl;
+  if (!make_plan(true, batch, vocab, 4, pl))
+    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large for a resident row pair", vocab);
+  svk::Params p = base_params(target_probs, draft_probs, row_stride, draft_tokens, uniforms, cu_k,
+                              nullptr, batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
+  p.use_tma = aligned16(target_probs) && (!draft_probs || aligned16(draft_probs)) &&
+              (row_stride * 4) % 16 == 0;
+  return launch<svk::MODE_PROBS, float>(p, pl, static_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_accept_from_logits(const void* target_logits, const void* draft_logits,
+                                sv_dtype dtype, int64_t row_stride, const float* temperature,
+                                const int32_t* draft_tokens, const float* uniforms,
+                                const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
+                                int32_t vocab, int32_t* n_accepted, int32_t* next_token,
+                                uint32_t* status, float* warped_target_out,
+                                float* warped_draft_out, uint32_t flags, void* stream) {
+  sv_status s = check_common(target_logits, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
+                             n_accepted, next_token, status, flags);
+  if (s != SV_OK || batch == 0) return s;
+  if (dtype != SV_F32 && dtype != SV_BF16 && dtype != SV_F16)
+    return fail(SV_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (sum_k > 0 && !draft_logits) return fail(SV_ERR_ARG, "draft_logits is NULL");
+  if (!uniforms) return fail(SV_ERR_ARG, "uniforms is NULL");
+  if (!temperature) return fail(SV_ERR_ARG, "temperature is NULL");
+  const int elem = dtype == SV_F32 ? 4 : 2;
+  Plan pl;
+  if (!make_plan(true, batch, vocab, elem, pl))
+    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large for a resident row pair", vocab);
+  svk::Params p = base_params(target_logits, draft_logits, row_stride, draft_tokens, uniforms, cu_k,
+                              temperature, batch, k, vocab, sum_k, n_accepted, next_token, status,
+                              flags);
+  p.wt_out = warped_target_out;
+  p.wd_out = warped_draft_out;
+  p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
+              (row_stride * elem) % 16 == 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dtype) {
+    case SV_F32: return launch<svk::MODE_LOGITS, float>(p, pl, st);
+    case SV_BF16: return launch<svk::MODE_LOGITS, __nv_bfloat16>(p, pl, st);
+    default: return launch<svk::MODE_LOGITS, __half>(p, pl, st);
+  }
+}
+
+const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_ARG: return "SV_ERR_ARG: invalid argument";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: CUDA runtime error";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: unsupported shape";
+  }
+  return "unknown sv_status";
+}
+
+const char* sv_last_error(void) { return g_err; }
+
+int32_t sv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+"""The C ABI library loads without a GPU, exports every symbol include/sv.h
+declares, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+import __graft_entry__
+from speculative_decoding_verification_decode_gb300 import _lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _lib.header_symbols()
+    assert set(declared) == set(_lib.SIGNATURES), declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code in range(4):
+        assert lib.sv_status_string(code).startswith(b"SV_")
+    assert lib.sv_status_string(99) == b"unknown sv_status"
+    assert lib.sv_version() >= 100
+
+
+NULL = None
+
+
+def greedy(lib, **kw):
+    args = dict(target=1 << 12, dtype=0, stride=16, tok=1 << 12, cu=NULL, B=2, K=3, sum_k=6, V=16,
+                n=1 << 12, nxt=1 << 12, st=1 << 12, flags=0, stream=NULL)
+    args.update(kw)
+    return lib.sv_verify_greedy(*args.values())
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(B=-1), b"batch"),
+    (dict(K=-2), b"k must"),
+    (dict(V=0), b"vocab"),
+    (dict(stride=8), b"row_stride"),
+    (dict(sum_k=5), b"sum_k must equal"),
+    (dict(flags=8), b"flag"),
+    (dict(target=NULL), b"target"),
+    (dict(tok=NULL), b"draft_tokens"),
+    (dict(n=NULL), b"output"),
+    (dict(dtype=7), b"dtype"),
+])
+def test_greedy_argument_errors(lib, kw, frag):
+    assert greedy(lib, **kw) == _lib.SV_ERR_ARG
+    assert frag in lib.sv_last_error()
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert greedy(lib, B=0, sum_k=0, target=NULL, tok=NULL, n=NULL, nxt=NULL, st=NULL) == _lib.SV_OK
+
+
+def test_accept_argument_errors(lib):
+    rc = lib.sv_accept(1 << 12, NULL, 16, 1 << 12, 1 << 12, NULL, 2, 3, 6, 16,
+                       1 << 12, 1 << 12, 1 << 12, 0, NULL)
+    assert rc == _lib.SV_ERR_ARG and b"draft_probs" in lib.sv_last_error()
+    rc = lib.sv_accept(1 << 12, 1 << 12, 16, 1 << 12, NULL, NULL, 2, 3, 6, 16,
+                       1 << 12, 1 << 12, 1 << 12, 0, NULL)
+    assert rc == _lib.SV_ERR_ARG and b"uniforms" in lib.sv_last_error()
+
+
+def test_logits_argument_errors(lib):
+    rc = lib.sv_accept_from_logits(1 << 12, 1 << 12, 1, 16, NULL, 1 << 12, 1 << 12, NULL, 2, 3, 6,
+                                   16, 1 << 12, 1 << 12, 1 << 12, NULL, NULL, 0, NULL)
+    assert rc == _lib.SV_ERR_ARG and b"temperature" in lib.sv_last_error()
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load()
