@@ -1,0 +1,456 @@
+"""Benchmark of the verification step on one GB300 (or N replicas).
+
+Default workload: B=64 sequences, K=5 drafts, V=128256, bf16 logits, fused
+temperature-0.8 softmax, rejection sampling (one sv_accept_from_logits call
+per step).  Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config config2]
+    python bench.py --impl reference      # the CPU oracle on the host cores
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; between timed steps the L2 is flushed by writing a
+512 MB buffer (then reading another one so no dirty lines are left), outside
+the events.  SM clocks are sampled with nvidia-smi during the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIG_TEXT = {
+    "config1": "B=1 K=4 V=32000 f32 probabilities, rejection sampling (600 rounds as B=600)",
+    "config2": "B=64 K=5 V=128256 bf16 logits, temperature 0.8, rejection sampling",
+    "config3": "B=256 K=4 V=152064 f32 probabilities, greedy",
+    "config4": "B=32 ragged K_b~U{0..8} V=129280 f32 probabilities, rejection sampling",
+    "config5": "B=1024 K=3 V=32000 f16 logits, half greedy / half sampled",
+}
+KERNEL_NAMES = {
+    "config1": "sv_verify_kernel<1, float>",
+    "config2": "sv_verify_kernel<2, __nv_bfloat16>",
+    "config3": "sv_verify_kernel<0, float>",
+    "config4": "sv_verify_kernel<1, float>",
+    "config5": "sv_verify_kernel<2, __half>",
+}
+METRIC = "verified rows/s and achieved HBM GB/s vs GB300 peak at B=64 K=5 V=128256"
+PROFILE_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_config2_traffic.md")
+SRC_FILES = [os.path.join(ROOT, "speculative_decoding_verification_decode_gb300", "csrc", f)
+             for f in ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh")]
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in SRC_FILES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not sha or not val or sha.group(1) != kernel_source_sha():
+        return None
+    return int(val.group(1))
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value, dist, device=None):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ workload helpers
+
+def device_inputs(wl, torch, dev):
+    def td(a, dt=None):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        if dt == "bf16":
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+    return dict(target=td(wl.target, wl.dtype), draft=td(wl.draft, wl.dtype), tokens=td(wl.tokens),
+                uniforms=td(wl.uniforms), cu_k=td(wl.cu_k), temperature=td(wl.temperature))
+
+
+def host_inputs(wl, torch):
+    def th(a, dt=None):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
+        return t.pin_memory()
+    return dict(target=th(wl.target, wl.dtype), draft=th(wl.draft, wl.dtype), tokens=th(wl.tokens),
+                uniforms=th(wl.uniforms), cu_k=th(wl.cu_k), temperature=th(wl.temperature))
+
+
+def call(sv, wl, x):
+    k = wl.K if wl.cu_k is not None else None
+    if wl.mode == "greedy":
+        return sv.verify_greedy(x["target"], x["tokens"], x["cu_k"], k)
+    if wl.mode in ("accept", "both"):
+        return sv.accept(x["target"], x["draft"], x["tokens"], x["uniforms"], x["cu_k"], k)
+    return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
+                                 x["uniforms"], x["cu_k"], k)
+
+
+def algorithmic_bytes(wl, n_acc):
+    """Bytes the method must move with early exit: target rows 0..n_b and
+    draft rows 0..min(n_b, K_b - 1) of every sampled sequence (the resident
+    row pair serves the residual / bonus scan, so nothing is read twice);
+    target rows 0..n_b of greedy sequences."""
+    kb = wl.k_per_seq
+    n = n_acc.astype(np.int64)
+    t_rows = n + 1
+    if wl.mode == "greedy":
+        d_rows = np.zeros_like(n)
+    else:
+        d_rows = np.minimum(n + 1, kb)
+        if wl.temperature is not None:
+            d_rows = np.where(wl.temperature > 0, d_rows, 0)
+    return int((t_rows + d_rows).sum()) * wl.V * wl.elem_size
+
+
+def oracle_rows_per_s(wl, budget_s=20.0):
+    """The CPU oracle as it stands on a bounded prefix of the batch (one core)."""
+    import oracle
+    kb = wl.k_per_seq
+    t_start = time.perf_counter()
+    done_rows = 0
+    done_seq = 0
+    tr0 = 0
+    dr0 = 0
+    while done_seq < wl.B and time.perf_counter() - t_start < budget_s:
+        b = done_seq
+        k = int(kb[b])
+        tsl = slice(tr0, tr0 + k + 1)
+        dsl = slice(dr0, dr0 + k)
+        if wl.mode == "greedy":
+            oracle.verify_greedy(wl.target[tsl], wl.dtype, wl.tokens[dsl], 1, k)
+        elif wl.mode in ("accept", "both"):
+            oracle.accept(wl.target[tsl], wl.draft[dsl], wl.tokens[dsl], wl.uniforms[tsl], 1, k)
+        else:
+            oracle.accept_from_logits(wl.target[tsl], wl.draft[dsl], wl.dtype,
+                                      wl.temperature[b:b + 1], wl.tokens[dsl], wl.uniforms[tsl], 1, k)
+        done_rows += k + 1
+        done_seq += 1
+        tr0 += k + 1
+        dr0 += k
+    dt = time.perf_counter() - t_start
+    return done_rows / dt, done_seq, dt
+
+
+# ------------------------------------------------------------------ arms
+
+def run_gpu(args):
+    import torch
+
+    import speculative_decoding_verification_decode_gb300 as sv
+    import workloads
+    from speculative_decoding_verification_decode_gb300._build import build
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    build()
+    sv.load_library()
+
+    # every rank verifies its own batch (independent sequences: weak scaling)
+    seed_shift = rank * 1000
+    base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5}[args.config]
+    wl = workloads.make_config(args.config, seed=workloads.configs.SEED_BASE + base_seed + seed_shift)
+    x = device_inputs(wl, torch, dev)
+    rows_per_step = int((wl.k_per_seq + 1).sum())
+    stream = torch.cuda.current_stream(dev)
+
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    for _ in range(args.warmup):
+        flush()
+        r = call(sv, wl, x)
+    torch.cuda.synchronize(dev)
+    n_acc = r.n_accepted.cpu().numpy()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            call(sv, wl, x)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = float(np.mean(per_step_ms))
+    ms = max_over_ranks(ms_local, dist, dev)
+
+    # end to end through the public API with pinned host buffers
+    hx = host_inputs(wl, torch)
+    h2d = sum(t.numel() * t.element_size() for t in hx.values() if t is not None)
+    d2h = 3 * wl.B * 4
+    for _ in range(2):
+        call(sv, wl, hx)
+    torch.cuda.synchronize(dev)
+    e_s = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier(dist, dev)
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        rr = call(sv, wl, hx)
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+    assert np.array_equal(rr.n_accepted.numpy(), n_acc)
+
+    result = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_gbs()
+        alg = algorithmic_bytes(wl, n_acc)
+        formula = wl.formula_bytes()
+        achieved = alg / (ms_local * 1e-3) / 1e9
+        traffic = profiled_traffic() if args.config == "config2" else None
+        value = world * rows_per_step / (ms * 1e-3)
+        cpu_val, cpu_seq, cpu_dt = oracle_rows_per_s(wl, budget_s=args.cpu_budget)
+        result = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "verified rows/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded Philox; shapes and distributions of the workload)",
+            "config": {
+                "workload": f"{args.config}: {CONFIG_TEXT[args.config]}",
+                "B": wl.B, "K": wl.K, "V": wl.V, "input_dtype": wl.dtype,
+                "rows_per_step": rows_per_step,
+                "rounds_per_s": world * wl.B / (ms * 1e-3),
+                "us_per_round": ms * 1e3,
+                "mean_accepted": float(n_acc.mean()),
+                "formula_bytes_per_step": formula,
+                "formula_gbs": formula / (ms * 1e-3) / 1e9,
+                "algorithmic_bytes_per_step": alg,
+                "l2": "flushed between timed steps (512 MB write, then a 512 MB read)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": KERNEL_NAMES[args.config],
+                "achieved": achieved,
+                "peak": peak,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+            },
+            "cpu_baseline": {
+                "value": cpu_val,
+                "unit": "verified rows/s",
+                "cores": 1,
+                "kind": "oracle",
+                "sample": f"first {cpu_seq} of {wl.B} sequences of the same workload "
+                          f"({cpu_dt:.1f} s, single thread numpy/Python)",
+            },
+            "e2e": {
+                "value": world * rows_per_step / (e2e_ms * 1e-3),
+                "unit": "verified rows/s",
+                "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms,
+            },
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores (the reference arm of this repo)."""
+    import workloads
+
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None
+    wl = workloads.make_config(args.config)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        v, nseq, dt = oracle_rows_per_s(wl, budget_s=args.ref_step_budget)
+        if i >= args.warmup:
+            per_step.append((v, nseq, dt))
+    value = float(np.mean([v for v, _, _ in per_step]))
+    nseq = per_step[-1][1]
+    ms = float(np.mean([dt / n for _, n, dt in per_step])) * wl.B * 1e3
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "verified rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded Philox; shapes and distributions of the workload)",
+        "config": {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "B": wl.B, "K": wl.K,
+                   "V": wl.V, "input_dtype": wl.dtype},
+        "cpu_baseline": {"value": value, "unit": "verified rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the first {nseq} of {wl.B} sequences "
+                                   f"(bounded to {args.ref_step_budget:.0f} s of CPU work)"},
+        "e2e": {"value": value, "unit": "verified rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--ref-step-budget", type=float, default=6.0,
+                    help="seconds of oracle work per step of the reference arm")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -44,46 +44,69 @@ int bit_length(unsigned long long v) {
 }
 
 struct Plan {
-  int C, slice, ck_el, nck, S;
+  int C, slice, slot_bytes, nck, S;
+  int vsum_off, tail_off;
   size_t smem;
 };
 
-// One cluster of C CTAs per sequence.  Greedy rows stream through a 4-slot
-// ring; sampling keeps a row pair (2 * nck slots) resident plus lookahead,
-// so C grows until a slice fits in the ring.
-bool make_plan(bool sampling, int B, int V, int elem, Plan& p) {
+constexpr size_t kSmemPerSM = 227 * 1024;  // usable shared memory per SM (bytes)
+constexpr size_t kSmemTwoCtas = kSmemPerSM / 2 - 1024;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Layout of one CTA's dynamic shared memory for a given cluster size C and
+// ring depth S: [ring S x slot][per-vector draw sums][SmemTail].
+void layout(bool sampling, int V, int elem, int C, int look, Plan& p) {
   const int vec = 16 / elem;
-  const int ck_el = svk::kSlotBytes / elem;
-  const long long nvec = (V + vec - 1) / vec;
-  const int sms = sm_count();
-  int C = static_cast<int>((2LL * sms + B - 1) / (B > 0 ? B : 1));
-  if (C < 1) C = 1;
-  if (sampling) {
-    // at least a pair of resident slices of <= 2 slots each
-    const long long c_res = (V + 2LL * ck_el - 1) / (2LL * ck_el);
-    if (c_res > C) C = static_cast<int>(c_res > svk::kMaxCluster ? svk::kMaxCluster : c_res);
-  }
-  if (C > svk::kMaxCluster) C = svk::kMaxCluster;
-  if (C > nvec) C = static_cast<int>(nvec);
   long long slice = (V + C - 1) / C;
   slice = (slice + vec - 1) / vec * vec;
-  C = static_cast<int>((V + slice - 1) / slice);
-  const int nck = static_cast<int>((slice + ck_el - 1) / ck_el);
-  int S;
-  if (sampling) {
-    const int look = nck < 2 ? nck : 2;
-    S = 2 * nck + (look > 0 ? look : 1);
-  } else {
-    S = 4;
-  }
-  if (S > svk::kMaxSlots) return false;
-  p.C = C;
+  p.C = static_cast<int>((V + slice - 1) / slice);
   p.slice = static_cast<int>(slice);
-  p.ck_el = ck_el;
-  p.nck = nck;
-  p.S = S;
-  p.smem = static_cast<size_t>(S) * svk::kSlotBytes + sizeof(svk::SmemTail);
-  return true;
+  const long long slice_bytes = slice * elem;
+  p.slot_bytes = static_cast<int>(slice_bytes < 16384 ? round_up(slice_bytes, 16) : 16384);
+  p.nck = static_cast<int>((slice_bytes + p.slot_bytes - 1) / p.slot_bytes);
+  p.S = sampling ? 2 * p.nck + look : look;
+  const size_t ring = static_cast<size_t>(p.S) * p.slot_bytes;
+  size_t vs = 0;
+  if (sampling) {
+    vs = static_cast<size_t>(p.nck) * (p.slot_bytes / 16) * 8;
+    if (vs < 2 * svk::kBuckets * 8) vs = 2 * svk::kBuckets * 8;
+  }
+  p.vsum_off = static_cast<int>(round_up(ring, 128));
+  p.tail_off = static_cast<int>(round_up(p.vsum_off + vs, 128));
+  p.smem = p.tail_off + sizeof(svk::SmemTail);
+}
+
+// One cluster of C CTAs per sequence.  Sampling keeps the current row pair
+// resident (2 * nck slots) plus lookahead; greedy streams through the ring.
+// C grows until two CTAs fit per SM and the batch gives enough CTAs.
+bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
+  const int vec = 16 / elem;
+  const long long nvec = (V + vec - 1) / vec;
+  const long long want = (sampling ? 2LL : 4LL) * sm_count();
+  bool found = false;
+  for (int C = 1; C <= svk::kMaxCluster; C *= 2) {
+    if (C > 1 && C > nvec) break;
+    Plan p;
+    if (sampling) {
+      layout(true, V, elem, C, 1, p);
+      // as much lookahead as two CTAs per SM allow (at most one row pair)
+      for (int look = 2; look <= 2 * p.nck; ++look) {
+        Plan q;
+        layout(true, V, elem, C, look, q);
+        if (q.smem > kSmemTwoCtas || q.S > svk::kMaxSlots) break;
+        p = q;
+      }
+    } else {
+      layout(false, V, elem, C, 6, p);
+    }
+    if (p.S > svk::kMaxSlots || p.smem > kSmemPerSM) continue;
+    const bool two = p.smem <= kSmemTwoCtas;
+    out = p;
+    found = true;
+    if (two && static_cast<long long>(B) * p.C >= want) break;
+  }
+  return found;
 }
 
 template <int MODE, typename T>
@@ -98,8 +121,10 @@ sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
       return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(cluster): %s", cudaGetErrorString(e));
   }
   prm.slice = pl.slice;
-  prm.ck_el = pl.ck_el;
+  prm.slot_bytes = pl.slot_bytes;
   prm.S = pl.S;
+  prm.vsum_off = pl.vsum_off;
+  prm.tail_off = pl.tail_off;
   const unsigned gy = static_cast<unsigned>(prm.B < 65535 ? prm.B : 65535);
   const unsigned gz = static_cast<unsigned>((prm.B + gy - 1) / gy);
   cudaLaunchConfig_t cfg = {};

@@ -1,26 +1,28 @@
 // Verification kernel: one thread-block cluster per sequence, one V-slice per CTA.
 //
 // Work of one sequence b (K_b drafts, rows 0..K_b):
-//   * each CTA streams its slice of every needed row through a shared-memory
-//     ring filled by 1-D bulk copies (cp.async.bulk + mbarrier); thread 0 keeps
-//     up to S chunks in flight, running ahead into later rows;
+//   * a producer warp streams this CTA's slice of every needed row into a
+//     shared-memory ring with 1-D bulk copies (cp.async.bulk, full/empty
+//     mbarriers), running ahead of the consumers by up to S chunks;
+//   * eight consumer warps reduce each chunk (argmax, row mass, or an online
+//     softmax with a tracked error bound);
 //   * per row the CTAs combine their partial statistics through distributed
 //     shared memory: each CTA pushes a small record into every peer and
 //     arrives on the peer's mbarrier; every CTA then takes the same decision
 //     from the same records in the same order (no global-memory scratch);
-//   * greedy rows are released as soon as they are reduced; in sampling mode
+//   * greedy chunks are released as soon as they are reduced; in sampling mode
 //     the current row pair stays resident until its decision, so the exact
 //     fallback, the residual and the inverse-CDF scan read shared memory only;
 //   * the walk stops at the first miss / rejection; later rows are not read
-//     (except chunks already in flight, which are drained before exit).
+//     (chunks already in flight are drained before exit).
 //
 // Decisions in sampling mode are the exact real predicate
 //     u * q(t) * Zp  <  p(t) * Zq
-// on the exact sums Zp, Zq of the f32 row weights: an fp32/fp64 sum with a
+// on the exact sums Zp, Zq of the f32 row weights: an approximate sum with a
 // rigorous error bound decides whenever the bound allows, otherwise the CTAs
 // sum the resident rows exactly (integer significand buckets, 32-bit limbs)
 // and compare big integers.  Inverse-CDF draws run in 64-bit fixed point so
-// every level (thread, block, cluster) of the scan is exactly consistent.
+// every level (vector, thread, block, cluster) of the scan is consistent.
 #pragma once
 #include <cfloat>
 #include <climits>
@@ -31,10 +33,11 @@
 
 namespace svk {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSlotBytes = 16384;
-constexpr int kMaxSlots = 12;
+constexpr int kConsumers = 256;  // consumer threads (8 warps)
+constexpr int kWarps = kConsumers / 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kMaxSlots = 16;
+constexpr int kMaxSlotBytes = 32768;
 constexpr int kMaxCluster = 16;
 constexpr int kRecWords = 32;
 constexpr int kBuckets = 254;
@@ -48,6 +51,11 @@ enum : int { MODE_GREEDY = 0, MODE_PROBS = 1, MODE_LOGITS = 2 };
 constexpr uint32_t ST_BAD_TOKEN = 1u, ST_BAD_VALUE = 2u, ST_ZERO_MASS = 4u, ST_NEAR = 8u,
                    ST_EXACT = 16u, ST_TIMEOUT = 32u, ST_BAD_LAYOUT = 64u;
 constexpr uint32_t FLAG_FORCE_EXACT = 1u;
+
+constexpr double kU32 = 5.9604644775390625e-8;  // 2^-24, unit roundoff of f32
+// Relative error bound used for ex2.approx.ftz.f32 (normal results); the
+// measured maximum on GB300 is checked against it by a GPU test.
+constexpr double kEx2Rel = 4.76837158203125e-7;  // 2^-21
 
 struct Params {
   const void* tgt;
@@ -64,24 +72,28 @@ struct Params {
   float* wt_out;
   float* wd_out;
   unsigned flags;
-  int slice;  // elements per CTA slice (multiple of the vector width)
-  int ck_el;  // elements per ring slot
-  int S;      // ring slots
+  int slice;       // elements per CTA slice (multiple of the vector width)
+  int slot_bytes;  // bytes per ring slot (multiple of 16)
+  int S;           // ring slots
   int use_tma;
   int fixed_shift;
+  int vsum_off;  // byte offset of the per-vector draw sums (sampling)
+  int tail_off;  // byte offset of SmemTail
 };
 
 struct __align__(16) SmemTail {
   uint32_t recs[2][kMaxCluster][kRecWords];
   uint32_t myrec[kRecWords];
-  unsigned long long buckets[2][kBuckets];
-  double redd[kWarps * 2];
+  double redd[kWarps * 4];
   unsigned long long redu[kWarps];
   float redf[kWarps * 2];
-  int redi[kWarps];
+  int redi[kWarps * 2];
   uint64_t xbar[2];
   uint64_t full[kMaxSlots];
-  int misc[8];
+  uint64_t empty[kMaxSlots];
+  double bd[8];    // broadcast of decision inputs from thread 0
+  int bi[8];
+  volatile int stop;  // consumers -> producer: issue nothing more
 };
 
 // ------------------------------------------------------------------ element types
@@ -123,7 +135,10 @@ template <typename T>
 __device__ __forceinline__ void load_vec(const T* s, int vi, float* x) {
   if constexpr (sizeof(T) == 4) {
     const float4 v = reinterpret_cast<const float4*>(s)[vi];
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
   } else {
     const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -158,17 +173,30 @@ __device__ __forceinline__ float vec_max_nan(const T* s, int vi) {
   }
 }
 
+// Pairwise sum of N floats (depth log2 N).
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* x) {
+  if constexpr (N == 1) {
+    return x[0];
+  } else {
+    return __fadd_rn(tree_sum<N / 2>(x), tree_sum<N / 2>(x + N / 2));
+  }
+}
+
 // ------------------------------------------------------------------ accumulators
 
 // fp32 partial sums of at most kFlush vectors, folded into an fp64 total.
-// Every element passes through at most 10 fp32 roundings (7 inside an
-// 8-element vector sum, 3 across the partial), so the total is within
-// 10 * 2^-24 (relative) of the exact sum; the filter below uses 16 * 2^-24.
+// Each element passes through at most 3 (vector tree) + 7 (partial) fp32
+// roundings, so the total is within 10 * 2^-24 (relative) of the exact sum.
 struct Acc {
   double d;
   float f;
   int c;
-  __device__ void init() { d = 0.0; f = 0.f; c = 0; }
+  __device__ __forceinline__ void init() {
+    d = 0.0;
+    f = 0.f;
+    c = 0;
+  }
   template <int kFlush>
   __device__ __forceinline__ void add(float t) {
     f = __fadd_rn(f, t);
@@ -178,21 +206,14 @@ struct Acc {
       c = 0;
     }
   }
-  __device__ double total() const { return d + static_cast<double>(f); }
+  __device__ __forceinline__ double total() const { return d + static_cast<double>(f); }
 };
 
-template <int N>
-__device__ __forceinline__ float seq_sum(const float* x) {
-  float t = x[0];
-#pragma unroll
-  for (int k = 1; k < N; ++k) t = __fadd_rn(t, x[k]);
-  return t;
-}
+// ------------------------------------------------------------------ logits -> weights
 
-// ------------------------------------------------------------------ warps (logits -> weights)
-
-// 16-bit logits: w = 2^((l - m) * k); l - m is exact for 16-bit inputs in
-// practice (and always correctly rounded), one rounding for the product.
+// The defined weights of a warped row (the values whose exact sum is the
+// row mass): w = 2^((l - m) * k) with m the row maximum and k = log2(e)/T.
+// 16-bit logits: one fp32 subtract and multiply, then ex2.approx.ftz.
 struct Warp16 {
   float m, k;
   __device__ __forceinline__ float operator()(float l) const {
@@ -229,18 +250,95 @@ struct NoWarp {
   __device__ __forceinline__ float operator()(float x) const { return x; }
 };
 
-// ------------------------------------------------------------------ block reductions
+// Online softmax of one thread's elements: running maximum m, and
+//   s = sum 2^(-nx),  w = sum 2^(-nx) * nx,   nx = (m - l) * k >= 0,
+// rescaled when m grows.  It approximates the row mass Z = sum w_v of the
+// defined weights; the error bound is
+//   |S - Z| <= S * ((R + 2)(e + u) + 2e + 16u) + W * 4 ln2 u   (times 2)
+// with e the ex2 bound, u = 2^-24 and R the number of rescale steps.
+struct Online {
+  float m;
+  float s32, w32;
+  double s64, w64;
+  int nv, r;
+  __device__ __forceinline__ void init() {
+    m = -kInfF;
+    s32 = w32 = 0.f;
+    s64 = w64 = 0.0;
+    nv = 0;
+    r = 0;
+  }
+  __device__ __forceinline__ void rescale_to(float mnew, float k) {
+    const float d = __fmul_rn(__fsub_rn(mnew, m), k);
+    const float f = ex2_ftz(-d);
+    w64 = (w64 + static_cast<double>(d) * s64) * static_cast<double>(f);
+    s64 *= static_cast<double>(f);
+    w32 = __fmul_rn(__fmaf_rn(d, s32, w32), f);
+    s32 = __fmul_rn(s32, f);
+    m = mnew;
+    ++r;
+  }
+  template <int VEC, int FL>
+  __device__ __forceinline__ void add_vec(const float* x, float vm, float k) {
+    if (!(vm <= m)) {
+      if (!(vm > -kInfF)) return;  // NaN (flagged by the caller) or all -Inf
+      if (m == -kInfF) m = vm;
+      else rescale_to(vm, k);
+    }
+    if (m == -kInfF) return;
+    float e[VEC];
+    float wa = 0.f, wb = 0.f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float nx = fminf(__fmul_rn(__fsub_rn(m, x[j]), k), 3.0e38f);
+      e[j] = ex2_ftz(-nx);
+      if (j & 1) wb = __fmaf_rn(e[j], nx, wb);
+      else wa = __fmaf_rn(e[j], nx, wa);
+    }
+    s32 = __fadd_rn(s32, tree_sum<VEC>(e));
+    w32 = __fadd_rn(w32, __fadd_rn(wa, wb));
+    if (++nv == FL) {
+      s64 += static_cast<double>(s32);
+      w64 += static_cast<double>(w32);
+      s32 = w32 = 0.f;
+      nv = 0;
+    }
+  }
+  __device__ __forceinline__ double S() const { return s64 + static_cast<double>(s32); }
+  __device__ __forceinline__ double W() const { return w64 + static_cast<double>(w32); }
+};
 
-__device__ __forceinline__ double block_sum_d(double v, double* red) {
+__device__ __forceinline__ double online_bound(double S, double W, int R) {
+  const double cs = (R + 2) * (kEx2Rel + kU32) + 2.0 * kEx2Rel + 16.0 * kU32;
+  const double cw = 4.0 * 0.6931471805599453 * kU32;
+  return 2.0 * (S * cs + W * cw) + 1e-30;
+}
+
+// ------------------------------------------------------------------ block reductions (consumers)
+
+__device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double s = 0.0;
+  return v;
+}
+
+// Sums of up to four doubles across the consumer threads (fixed order).
+template <int N>
+__device__ __forceinline__ void block_sum_dn(double* v, double* red) {
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) s += red[w];
-  __syncthreads();
-  return s;
+  for (int j = 0; j < N; ++j) v[j] = warp_sum_d(v[j]);
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int j = 0; j < N; ++j) red[j * kWarps + (threadIdx.x >> 5)] = v[j];
+  bar_consumers<kConsumers>();
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += red[j * kWarps + w];
+    v[j] = s;
+  }
+  bar_consumers<kConsumers>();
 }
 
 __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
@@ -248,28 +346,48 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
+  bar_consumers<kConsumers>();
   unsigned long long s = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) s += red[w];
-  __syncthreads();
+  bar_consumers<kConsumers>();
   return s;
 }
 
-// op = 0: NaN-propagating max, 1: NaN-propagating min.
+// kOp 0: NaN-propagating max, 1: NaN-propagating min, of two floats at once.
 template <int kOp>
-__device__ __forceinline__ float block_ext_f(float v, float* red) {
+__device__ __forceinline__ void block_ext_f2(float& a, float& b, float* red) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    const float w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = kOp == 0 ? fmax_nan(v, w) : fmin_nan(v, w);
+    const float x = __shfl_xor_sync(0xFFFFFFFFu, a, o);
+    const float y = __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    a = kOp == 0 ? fmax_nan(a, x) : fmin_nan(a, x);
+    b = kOp == 0 ? fmax_nan(b, y) : fmin_nan(b, y);
   }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float s = red[0];
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = a;
+    red[kWarps + (threadIdx.x >> 5)] = b;
+  }
+  bar_consumers<kConsumers>();
+  a = red[0];
+  b = red[kWarps];
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) s = kOp == 0 ? fmax_nan(s, red[w]) : fmin_nan(s, red[w]);
-  __syncthreads();
+  for (int w = 1; w < kWarps; ++w) {
+    a = kOp == 0 ? fmax_nan(a, red[w]) : fmin_nan(a, red[w]);
+    b = kOp == 0 ? fmax_nan(b, red[kWarps + w]) : fmin_nan(b, red[kWarps + w]);
+  }
+  bar_consumers<kConsumers>();
+}
+
+__device__ __forceinline__ int block_max_i(int v, int* red) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  bar_consumers<kConsumers>();
+  int s = red[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) s = max(s, red[w]);
+  bar_consumers<kConsumers>();
   return s;
 }
 
@@ -286,19 +404,25 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, float* redf, int*
   for (int o = 16; o; o >>= 1) {
     const float w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
     const int j = __shfl_xor_sync(0xFFFFFFFFu, i, o);
-    if (arg_better(w, j, v, i)) { v = w; i = j; }
+    if (arg_better(w, j, v, i)) {
+      v = w;
+      i = j;
+    }
   }
   if ((threadIdx.x & 31) == 0) {
     redf[threadIdx.x >> 5] = v;
     redi[threadIdx.x >> 5] = i;
   }
-  __syncthreads();
+  bar_consumers<kConsumers>();
   v = redf[0];
   i = redi[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w)
-    if (arg_better(redf[w], redi[w], v, i)) { v = redf[w]; i = redi[w]; }
-  __syncthreads();
+    if (arg_better(redf[w], redi[w], v, i)) {
+      v = redf[w];
+      i = redi[w];
+    }
+  bar_consumers<kConsumers>();
 }
 
 __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
@@ -312,14 +436,14 @@ __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long 
     if (lane >= o) inc += n;
   }
   if (lane == 31) red[w] = inc;
-  __syncthreads();
+  bar_consumers<kConsumers>();
   unsigned long long before = 0, tot = 0;
 #pragma unroll
   for (int k = 0; k < kWarps; ++k) {
     if (k < w) before += red[k];
     tot += red[k];
   }
-  __syncthreads();
+  bar_consumers<kConsumers>();
   total = tot;
   return before + inc - v;
 }
@@ -341,9 +465,8 @@ __device__ __forceinline__ void bucket_add(unsigned long long* bk, float x) {
 }
 
 // sum_s bk[s] * 2^s  ->  kLimbs little-endian 32-bit limbs.
-__device__ void buckets_to_limbs(const unsigned long long* bk, uint32_t* limbs) {
+__device__ __noinline__ void buckets_to_limbs(const unsigned long long* bk, uint32_t* limbs) {
   unsigned long long acc[kLimbs];
-#pragma unroll
   for (int i = 0; i < kLimbs; ++i) acc[i] = 0;
   for (int s = 0; s < kBuckets; ++s) {
     const unsigned long long v = bk[s];
@@ -367,11 +490,11 @@ struct Big {
   uint32_t w[kBigLimbs];
 };
 
-__device__ void big_set(Big& a, const uint32_t* limbs) {
+__device__ __forceinline__ void big_set(Big& a, const uint32_t* limbs) {
   for (int i = 0; i < kBigLimbs; ++i) a.w[i] = i < kLimbs ? limbs[i] : 0u;
 }
 
-__device__ void big_mul_u32(Big& a, uint32_t m) {
+__device__ __forceinline__ void big_mul_u32(Big& a, uint32_t m) {
   unsigned long long carry = 0;
   for (int i = 0; i < kBigLimbs; ++i) {
     const unsigned long long t = static_cast<unsigned long long>(a.w[i]) * m + carry;
@@ -380,7 +503,7 @@ __device__ void big_mul_u32(Big& a, uint32_t m) {
   }
 }
 
-__device__ void big_shl(Big& a, int bits) {
+__device__ __forceinline__ void big_shl(Big& a, int bits) {
   const int q = bits >> 5, r = bits & 31;
   for (int i = kBigLimbs - 1; i >= 0; --i) {
     const int src = i - q;
@@ -393,14 +516,15 @@ __device__ void big_shl(Big& a, int bits) {
   }
 }
 
-__device__ int big_cmp(const Big& a, const Big& b) {
+__device__ __forceinline__ int big_cmp(const Big& a, const Big& b) {
   for (int i = kBigLimbs - 1; i >= 0; --i)
     if (a.w[i] != b.w[i]) return a.w[i] < b.w[i] ? -1 : 1;
   return 0;
 }
 
-// Exact  u * q_t * Sp  <  p_t * Sq  (all scaled by 2^447; see f32_parts).
-__device__ bool exact_accept(float u, float pt, float qt, const uint32_t* sp, const uint32_t* sq) {
+// Exact  u * q_t * Sp  <  p_t * Sq  (both sides scaled by 2^447; see f32_parts).
+__device__ __noinline__ bool exact_accept(float u, float pt, float qt, const uint32_t* sp,
+                                          const uint32_t* sq) {
   uint32_t Mu, Mq, Mp;
   int su, sq_, sp_;
   f32_parts(u, Mu, su);
@@ -419,21 +543,22 @@ __device__ bool exact_accept(float u, float pt, float qt, const uint32_t* sp, co
   return big_cmp(L, R) < 0;
 }
 
-__device__ double limbs_to_double(const uint32_t* l) {
+__device__ __forceinline__ double limbs_to_double(const uint32_t* l) {
   double z = 0.0;
   for (int i = kLimbs - 1; i >= 0; --i) z = z * 4294967296.0 + static_cast<double>(l[i]);
   return ldexp(z, -149);
 }
 
-// 1: certain accept, 0: certain reject, -1: inside the error band.
-__device__ __forceinline__ int filter_decide(float u, float pt, float qt, double Zp, double Zq) {
+// 1: certain accept, 0: certain reject, -1: inside the error band.  Zp, Zq
+// are approximate masses with |Zp - exact| <= Bp and |Zq - exact| <= Bq.
+__device__ __forceinline__ int filter_decide(float u, float pt, float qt, double Zp, double Bp,
+                                             double Zq, double Bq) {
   const double a = static_cast<double>(u) * static_cast<double>(qt);  // exact
   const double bp = static_cast<double>(pt);
   if (bp == 0.0) return 0;  // rhs = 0 <= lhs
   if (a == 0.0) return 1;   // lhs = 0 < rhs  (pt > 0, Zq > 0 checked earlier)
   const double L = a * Zp, R = bp * Zq;
-  const double eps = 16.0 * 5.9604644775390625e-8;
-  const double E = (L + R) * (eps + 4.5e-16);
+  const double E = a * Bp + bp * Bq + (L + R) * 4.5e-16;
   if (R - L > E) return 1;
   if (L - R > E) return 0;
   return -1;
@@ -453,15 +578,18 @@ __device__ __forceinline__ unsigned long long tau_of(float u, unsigned long long
   return (lo >> sh) | (hi << (64 - sh));
 }
 
-// Draw weights in 64-bit fixed point: residual max(0, phat - qhat) or phat.
+// Normalised draw weights: residual max(0, phat - qhat) or phat alone.
 struct DrawW {
   float sp, ap, sq, aq, scale;
   int resid;
-  __device__ __forceinline__ unsigned long long operator()(float p, float q) const {
+  __device__ __forceinline__ float operator()(float p, float q) const {
     const float a = __fmul_rn(__fmul_rn(p, sp), ap);
-    float r = a;
-    if (resid) r = fmaxf(__fsub_rn(a, __fmul_rn(__fmul_rn(q, sq), aq)), 0.f);
-    return __float2ull_rz(__fmul_rn(r, scale));
+    if (!resid) return a;
+    return fmaxf(__fsub_rn(a, __fmul_rn(__fmul_rn(q, sq), aq)), 0.f);
+  }
+  // fixed point of a (partial) vector sum
+  __device__ __forceinline__ unsigned long long fix(float v) const {
+    return __float2ull_rz(__fmul_rn(v, scale));
   }
 };
 

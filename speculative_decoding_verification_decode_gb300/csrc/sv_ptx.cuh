@@ -157,3 +157,37 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 }
 
 }  // namespace svk
+
+namespace svk {
+
+// Named barrier 1 over the `n` consumer threads (the producer warp never joins).
+template <int N>
+__device__ __forceinline__ void bar_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ int bar_consumers_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.s32 pi, %1, 0;\n"
+      " bar.red.or.pred po, 1, %2, pi;\n selp.s32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(pred), "n"(N)
+      : "memory");
+  return r;
+}
+
+template <int N>
+__device__ __forceinline__ int bar_consumers_and(int pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.s32 pi, %1, 0;\n"
+      " bar.red.and.pred po, 1, %2, pi;\n selp.s32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"(pred), "n"(N)
+      : "memory");
+  return r;
+}
+
+}  // namespace svk
