@@ -56,7 +56,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Layout of one CTA's dynamic shared memory for a given cluster size C and
 // ring depth S: [ring S x slot][per-vector draw sums][SmemTail].
-void layout(bool sampling, int V, int elem, int C, int look, Plan& p) {
+void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
   const int vec = 16 / elem;
   long long slice = (V + C - 1) / C;
   slice = (slice + vec - 1) / vec * vec;
@@ -65,11 +65,16 @@ void layout(bool sampling, int V, int elem, int C, int look, Plan& p) {
   const long long slice_bytes = slice * elem;
   p.slot_bytes = static_cast<int>(slice_bytes < 16384 ? round_up(slice_bytes, 16) : 16384);
   p.nck = static_cast<int>((slice_bytes + p.slot_bytes - 1) / p.slot_bytes);
-  p.S = sampling ? 2 * p.nck + look : look;
-  const size_t ring = static_cast<size_t>(p.S) * p.slot_bytes;
+  p.S = ring_slots;
+  size_t ring = static_cast<size_t>(p.S) * p.slot_bytes;
   size_t vs = 0;
   if (sampling) {
-    vs = static_cast<size_t>(p.nck) * (p.slot_bytes / 16) * 8;
+    // the current row pair stays resident until its decision, plus one chunk
+    // of lookahead into the next row
+    p.S = 2 * p.nck + 1;
+    ring = static_cast<size_t>(p.S) * p.slot_bytes;
+    // one u64 per 16-byte vector of the slice, or the exact-sum buckets
+    vs = static_cast<size_t>((slice + vec - 1) / vec) * 8;
     if (vs < 2 * svk::kBuckets * 8) vs = 2 * svk::kBuckets * 8;
   }
   p.vsum_off = static_cast<int>(round_up(ring, 128));
@@ -77,34 +82,21 @@ void layout(bool sampling, int V, int elem, int C, int look, Plan& p) {
   p.smem = p.tail_off + sizeof(svk::SmemTail);
 }
 
-// One cluster of C CTAs per sequence.  Sampling keeps the current row pair
-// resident (2 * nck slots) plus lookahead; greedy streams through the ring.
-// C grows until two CTAs fit per SM and the batch gives enough CTAs.
+// One cluster of C CTAs per sequence; the smallest C that gives the batch at
+// least two CTAs per SM while two CTAs still fit on an SM.
 bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
   const int vec = 16 / elem;
   const long long nvec = (V + vec - 1) / vec;
-  const long long want = (sampling ? 2LL : 4LL) * sm_count();
+  const long long want = 2LL * sm_count();
   bool found = false;
   for (int C = 1; C <= svk::kMaxCluster; C *= 2) {
     if (C > 1 && C > nvec) break;
     Plan p;
-    if (sampling) {
-      layout(true, V, elem, C, 1, p);
-      // as much lookahead as two CTAs per SM allow (at most one row pair)
-      for (int look = 2; look <= 2 * p.nck; ++look) {
-        Plan q;
-        layout(true, V, elem, C, look, q);
-        if (q.smem > kSmemTwoCtas || q.S > svk::kMaxSlots) break;
-        p = q;
-      }
-    } else {
-      layout(false, V, elem, C, 6, p);
-    }
-    if (p.S > svk::kMaxSlots || p.smem > kSmemPerSM) continue;
-    const bool two = p.smem <= kSmemTwoCtas;
+    layout(sampling, V, elem, C, 4, p);
+    if (p.smem > kSmemPerSM || p.S > svk::kMaxSlots) continue;
     out = p;
     found = true;
-    if (two && static_cast<long long>(B) * p.C >= want) break;
+    if (p.smem <= kSmemTwoCtas && static_cast<long long>(B) * p.C >= want) break;
   }
   return found;
 }
@@ -125,6 +117,7 @@ sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
   prm.S = pl.S;
   prm.vsum_off = pl.vsum_off;
   prm.tail_off = pl.tail_off;
+  prm.look = 1;
   const unsigned gy = static_cast<unsigned>(prm.B < 65535 ? prm.B : 65535);
   const unsigned gz = static_cast<unsigned>((prm.B + gy - 1) / gy);
   cudaLaunchConfig_t cfg = {};

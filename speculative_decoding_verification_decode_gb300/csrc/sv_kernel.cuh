@@ -43,6 +43,7 @@ constexpr int kRecWords = 32;
 constexpr int kBuckets = 254;
 constexpr int kLimbs = 12;
 constexpr int kBigLimbs = 32;
+constexpr int kMaxGather = 32;  // rows whose decision inputs are prefetched at start
 
 enum : int { MODE_GREEDY = 0, MODE_PROBS = 1, MODE_LOGITS = 2 };
 
@@ -78,22 +79,29 @@ struct Params {
   int use_tma;
   int fixed_shift;
   int vsum_off;  // byte offset of the per-vector draw sums (sampling)
+  int look;      // chunks the producer may stream into a row not yet reached
   int tail_off;  // byte offset of SmemTail
 };
 
 struct __align__(16) SmemTail {
-  uint32_t recs[2][kMaxCluster][kRecWords];
-  uint32_t myrec[kRecWords];
-  double redd[kWarps * 4];
-  unsigned long long redu[kWarps];
-  float redf[kWarps * 2];
-  int redi[kWarps * 2];
+  uint32_t recs[2][kMaxCluster][kRecWords];  // records pushed by the cluster's CTAs
+  uint32_t myrec[kRecWords];                 // this CTA's outgoing record
+  float wf[kWarps][8];                       // per-warp partial results
+  int wi[kWarps][4];
+  unsigned long long wu[kWarps];
+  double bd[8];  // broadcast of decision values from thread 0
+  int bi[8];
+  float dpar[4];  // draw weight parameters (computed once by thread 0)
+  // decision inputs of rows 0..kMaxGather-1, loaded at the start
+  int g_t[kMaxGather];
+  float g_u[kMaxGather], g_p[kMaxGather], g_q[kMaxGather];
   uint64_t xbar[2];
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
-  double bd[8];    // broadcast of decision inputs from thread 0
-  int bi[8];
-  volatile int stop;  // consumers -> producer: issue nothing more
+  volatile int stop;           // consumers -> producer: issue nothing more
+  volatile int go_row;         // consumers -> producer: rows decided so far
+  volatile int producer_done;  // producer -> consumers: no copy in flight
+  uint64_t redo_bar;           // completion of the draw pass's bulk copies
 };
 
 // ------------------------------------------------------------------ element types
@@ -183,31 +191,58 @@ __device__ __forceinline__ float tree_sum(const float* x) {
   }
 }
 
+// ------------------------------------------------------------------ double-float (fp32 pairs)
+// hi + lo with |lo| <= ulp(hi)/2; relative error of each operation ~2^-44.
+// Used by thread 0 instead of fp64 (GB300's fp64 rate is a small fraction of
+// its fp32 rate and would sit on the per-row critical path).
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  const DF s = two_sum(x.hi, y.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ DF df_mul_f(DF x, float y) {
+  DF p = two_prod(x.hi, y);
+  p.lo = __fmaf_rn(x.lo, y, p.lo);
+  return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ DF df_mul(DF x, DF y) {
+  DF p = two_prod(x.hi, y.hi);
+  p.lo = __fmaf_rn(x.hi, y.lo, __fmaf_rn(x.lo, y.hi, p.lo));
+  return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ DF df_neg(DF x) { return {-x.hi, -x.lo}; }
+
 // ------------------------------------------------------------------ accumulators
 
-// fp32 partial sums of at most kFlush vectors, folded into an fp64 total.
-// Each element passes through at most 3 (vector tree) + 7 (partial) fp32
-// roundings, so the total is within 10 * 2^-24 (relative) of the exact sum.
+// Per-thread fp32 sum of vector sums.  A thread that adds n_v vector sums
+// (each a pairwise tree of VEC elements) is within (n_v + log2 VEC) * 2^-24 of
+// its exact sum; the block and cluster levels add 6 more roundings (a 5-level
+// warp tree in fp32, then fp64).  sum_bound() states the total bound.
 struct Acc {
-  double d;
   float f;
-  int c;
-  __device__ __forceinline__ void init() {
-    d = 0.0;
-    f = 0.f;
-    c = 0;
-  }
-  template <int kFlush>
-  __device__ __forceinline__ void add(float t) {
-    f = __fadd_rn(f, t);
-    if (++c == kFlush) {
-      d += static_cast<double>(f);
-      f = 0.f;
-      c = 0;
-    }
-  }
-  __device__ __forceinline__ double total() const { return d + static_cast<double>(f); }
+  __device__ __forceinline__ void init() { f = 0.f; }
+  __device__ __forceinline__ void add(float t) { f = __fadd_rn(f, t); }
 };
+
+__device__ __forceinline__ float sum_bound(float Z, int nadd) {
+  return 2.02f * Z * static_cast<float>((nadd + 8) * kU32);
+}
 
 // ------------------------------------------------------------------ logits -> weights
 
@@ -252,33 +287,28 @@ struct NoWarp {
 
 // Online softmax of one thread's elements: running maximum m, and
 //   s = sum 2^(-nx),  w = sum 2^(-nx) * nx,   nx = (m - l) * k >= 0,
-// rescaled when m grows.  It approximates the row mass Z = sum w_v of the
-// defined weights; the error bound is
-//   |S - Z| <= S * ((R + 2)(e + u) + 2e + 16u) + W * 4 ln2 u   (times 2)
-// with e the ex2 bound, u = 2^-24 and R the number of rescale steps.
+// rescaled when m grows (all in fp32).  It approximates the row mass
+// Z = sum w_v of the defined weights within
+//   |S - Z| <= 2 * (S * ((R + 3)(e + u) + 2e + (n + 8) u) + W * 4 ln2 u)
+// with e the ex2 bound, u = 2^-24, R the rescale steps of any element and n
+// the fp32 additions of any element inside its thread.
 struct Online {
-  float m;
-  float s32, w32;
-  double s64, w64;
-  int nv, r;
+  float m, s, w;
+  int r;
   __device__ __forceinline__ void init() {
     m = -kInfF;
-    s32 = w32 = 0.f;
-    s64 = w64 = 0.0;
-    nv = 0;
+    s = w = 0.f;
     r = 0;
   }
   __device__ __forceinline__ void rescale_to(float mnew, float k) {
     const float d = __fmul_rn(__fsub_rn(mnew, m), k);
     const float f = ex2_ftz(-d);
-    w64 = (w64 + static_cast<double>(d) * s64) * static_cast<double>(f);
-    s64 *= static_cast<double>(f);
-    w32 = __fmul_rn(__fmaf_rn(d, s32, w32), f);
-    s32 = __fmul_rn(s32, f);
+    w = __fmul_rn(__fmaf_rn(d, s, w), f);
+    s = __fmul_rn(s, f);
     m = mnew;
     ++r;
   }
-  template <int VEC, int FL>
+  template <int VEC>
   __device__ __forceinline__ void add_vec(const float* x, float vm, float k) {
     if (!(vm <= m)) {
       if (!(vm > -kInfF)) return;  // NaN (flagged by the caller) or all -Inf
@@ -295,100 +325,55 @@ struct Online {
       if (j & 1) wb = __fmaf_rn(e[j], nx, wb);
       else wa = __fmaf_rn(e[j], nx, wa);
     }
-    s32 = __fadd_rn(s32, tree_sum<VEC>(e));
-    w32 = __fadd_rn(w32, __fadd_rn(wa, wb));
-    if (++nv == FL) {
-      s64 += static_cast<double>(s32);
-      w64 += static_cast<double>(w32);
-      s32 = w32 = 0.f;
-      nv = 0;
-    }
+    s = __fadd_rn(s, tree_sum<VEC>(e));
+    w = __fadd_rn(w, __fadd_rn(wa, wb));
   }
-  __device__ __forceinline__ double S() const { return s64 + static_cast<double>(s32); }
-  __device__ __forceinline__ double W() const { return w64 + static_cast<double>(w32); }
 };
 
-__device__ __forceinline__ double online_bound(double S, double W, int R) {
-  const double cs = (R + 2) * (kEx2Rel + kU32) + 2.0 * kEx2Rel + 16.0 * kU32;
-  const double cw = 4.0 * 0.6931471805599453 * kU32;
-  return 2.0 * (S * cs + W * cw) + 1e-30;
+__device__ __forceinline__ float online_bound(float S, float W, int R, int nadd) {
+  const float cs = static_cast<float>((R + 3) * (kEx2Rel + kU32) + 2.0 * kEx2Rel + (nadd + 8) * kU32);
+  const float cw = static_cast<float>(4.0 * 0.6931471805599453 * kU32);
+  return 2.02f * (S * cs + W * cw);
 }
 
-// ------------------------------------------------------------------ block reductions (consumers)
+// ------------------------------------------------------------------ warp reductions
+// Per-warp results go to shared memory and thread 0 combines the eight warps
+// (one named barrier instead of a full block reduction).
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
-// Sums of up to four doubles across the consumer threads (fixed order).
-template <int N>
-__device__ __forceinline__ void block_sum_dn(double* v, double* red) {
+__device__ __forceinline__ float warp_max_nan_f(float v) {
 #pragma unroll
-  for (int j = 0; j < N; ++j) v[j] = warp_sum_d(v[j]);
-  if ((threadIdx.x & 31) == 0)
-#pragma unroll
-    for (int j = 0; j < N; ++j) red[j * kWarps + (threadIdx.x >> 5)] = v[j];
-  bar_consumers<kConsumers>();
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    double s = 0.0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += red[j * kWarps + w];
-    v[j] = s;
-  }
-  bar_consumers<kConsumers>();
+  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
 }
 
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
-                                                            unsigned long long* red) {
+__device__ __forceinline__ float warp_min_nan_f(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  bar_consumers<kConsumers>();
-  unsigned long long s = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) s += red[w];
-  bar_consumers<kConsumers>();
-  return s;
+  for (int o = 16; o; o >>= 1) v = fmin_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
 }
 
-// kOp 0: NaN-propagating max, 1: NaN-propagating min, of two floats at once.
-template <int kOp>
-__device__ __forceinline__ void block_ext_f2(float& a, float& b, float* red) {
+__device__ __forceinline__ float warp_max_f(float v) {  // inputs never NaN
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float x = __shfl_xor_sync(0xFFFFFFFFu, a, o);
-    const float y = __shfl_xor_sync(0xFFFFFFFFu, b, o);
-    a = kOp == 0 ? fmax_nan(a, x) : fmin_nan(a, x);
-    b = kOp == 0 ? fmax_nan(b, y) : fmin_nan(b, y);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red[threadIdx.x >> 5] = a;
-    red[kWarps + (threadIdx.x >> 5)] = b;
-  }
-  bar_consumers<kConsumers>();
-  a = red[0];
-  b = red[kWarps];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
-    a = kOp == 0 ? fmax_nan(a, red[w]) : fmin_nan(a, red[w]);
-    b = kOp == 0 ? fmax_nan(b, red[kWarps + w]) : fmin_nan(b, red[kWarps + w]);
-  }
-  bar_consumers<kConsumers>();
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
 }
 
-__device__ __forceinline__ int block_max_i(int v, int* red) {
+__device__ __forceinline__ int warp_max_i(int v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  bar_consumers<kConsumers>();
-  int s = red[0];
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
-  for (int w = 1; w < kWarps; ++w) s = max(s, red[w]);
-  bar_consumers<kConsumers>();
-  return s;
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
 }
 
 // Argmax candidate ordering: a valid index beats "none" (INT_MAX); larger value
@@ -399,7 +384,7 @@ __device__ __forceinline__ bool arg_better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-__device__ __forceinline__ void block_argmax(float& v, int& i, float* redf, int* redi) {
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     const float w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -409,22 +394,9 @@ __device__ __forceinline__ void block_argmax(float& v, int& i, float* redf, int*
       i = j;
     }
   }
-  if ((threadIdx.x & 31) == 0) {
-    redf[threadIdx.x >> 5] = v;
-    redi[threadIdx.x >> 5] = i;
-  }
-  bar_consumers<kConsumers>();
-  v = redf[0];
-  i = redi[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w)
-    if (arg_better(redf[w], redi[w], v, i)) {
-      v = redf[w];
-      i = redi[w];
-    }
-  bar_consumers<kConsumers>();
 }
 
+// Exclusive scan of one u64 per consumer thread (all consumers call it).
 __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
                                                                   unsigned long long* red,
                                                                   unsigned long long& total) {
@@ -549,18 +521,22 @@ __device__ __forceinline__ double limbs_to_double(const uint32_t* l) {
   return ldexp(z, -149);
 }
 
-// 1: certain accept, 0: certain reject, -1: inside the error band.  Zp, Zq
-// are approximate masses with |Zp - exact| <= Bp and |Zq - exact| <= Bq.
-__device__ __forceinline__ int filter_decide(float u, float pt, float qt, double Zp, double Bp,
-                                             double Zq, double Bq) {
-  const double a = static_cast<double>(u) * static_cast<double>(qt);  // exact
-  const double bp = static_cast<double>(pt);
-  if (bp == 0.0) return 0;  // rhs = 0 <= lhs
-  if (a == 0.0) return 1;   // lhs = 0 < rhs  (pt > 0, Zq > 0 checked earlier)
-  const double L = a * Zp, R = bp * Zq;
-  const double E = a * Bp + bp * Bq + (L + R) * 4.5e-16;
-  if (R - L > E) return 1;
-  if (L - R > E) return 0;
+// 1: certain accept, 0: certain reject, -1: inside the error band (or a scale
+// where fp32 pairs could lose accuracy).  Zp, Zq are approximate masses with
+// |Zp - exact| <= Bp and |Zq - exact| <= Bq.
+__device__ __forceinline__ int filter_decide(float u, float pt, float qt, DF Zp, float Bp, DF Zq,
+                                             float Bq) {
+  if (pt == 0.f) return 0;  // rhs = 0 <= lhs
+  if (u == 0.f || qt == 0.f) return 1;  // lhs = 0 < rhs  (pt > 0, Zq > 0 checked earlier)
+  const DF a = two_prod(u, qt);  // exact unless tiny
+  const float lo = 0x1p-90f, hi = 0x1p90f;
+  if (!(a.hi >= lo && pt >= lo && Zp.hi >= lo && Zp.hi <= hi && Zq.hi >= lo && Zq.hi <= hi))
+    return -1;
+  const DF L = df_mul(a, Zp), R = df_mul_f(Zq, pt);
+  const DF D = df_add(R, df_neg(L));
+  const float E = 1.01f * (a.hi * Bp + pt * Bq + (L.hi + R.hi) * 0x1p-40f);
+  if (D.hi > E) return 1;
+  if (D.hi < -E) return 0;
   return -1;
 }
 
@@ -578,8 +554,17 @@ __device__ __forceinline__ unsigned long long tau_of(float u, unsigned long long
   return (lo >> sh) | (hi << (64 - sh));
 }
 
-// Normalised draw weights: residual max(0, phat - qhat) or phat alone.
-struct DrawW {
+// floor(y) for 0 <= y < 2^63 from the fp32 bits (integer pipe; truncation).
+__device__ __forceinline__ unsigned long long floor_u64(float y) {
+  const uint32_t b = __float_as_uint(y);
+  const int e = static_cast<int>(b >> 23) - 127;
+  if (e < 0) return 0ull;
+  const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;
+  return e >= 23 ? (m << (e - 23)) : (m >> (23 - e));
+}
+
+// Normalised draw weights of f32 probabilities: max(0, phat - qhat), or phat.
+struct DrawProbs {
   float sp, ap, sq, aq, scale;
   int resid;
   __device__ __forceinline__ float operator()(float p, float q) const {
@@ -587,9 +572,25 @@ struct DrawW {
     if (!resid) return a;
     return fmaxf(__fsub_rn(a, __fmul_rn(__fmul_rn(q, sq), aq)), 0.f);
   }
-  // fixed point of a (partial) vector sum
   __device__ __forceinline__ unsigned long long fix(float v) const {
-    return __float2ull_rz(__fmul_rn(v, scale));
+    return floor_u64(__fmul_rn(v, scale));
+  }
+};
+
+// Normalised draw weights of logits: the normalisation is folded into the
+// exponent, 2^(l k + c) with c = -m k - log2 Z (one FMA and one ex2 per row).
+// Only the draw uses these (they need not equal the defined weights bit for
+// bit; both passes of the draw use the same function).
+struct DrawLogits {
+  float k, cp, cq, scale;
+  int resid;
+  __device__ __forceinline__ float operator()(float lp, float lq) const {
+    const float a = ex2_ftz(__fmaf_rn(lp, k, cp));
+    if (!resid) return a;
+    return fmaxf(__fsub_rn(a, ex2_ftz(__fmaf_rn(lq, k, cq))), 0.f);
+  }
+  __device__ __forceinline__ unsigned long long fix(float v) const {
+    return floor_u64(__fmul_rn(v, scale));
   }
 };
 

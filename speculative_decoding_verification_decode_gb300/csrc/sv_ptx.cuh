@@ -55,14 +55,20 @@ __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
 
 // One poll of phase `parity`; acquire at cluster scope so that data written by
 // peer CTAs before their release-arrive is visible afterwards.
+// One wait on phase `parity` that may suspend the thread in hardware for up
+// to `kSuspendNs` (so waiting warps do not take issue slots); acquire at
+// cluster scope so that data written by peer CTAs before their release-arrive
+// is visible afterwards.
+constexpr uint32_t kSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -71,16 +77,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded waits: give up after kWaitPolls unsuccessful tries (each may suspend
+// for up to kSuspendNs) and report false.
+constexpr uint32_t kWaitPolls = 1u << 18;
+
+// A poll without suspension (for waiters that must also watch a flag).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
-
-// Bounded waits: give up after `limit` polls and report false.
-constexpr uint32_t kWaitPolls = 1u << 24;
 
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitPolls; ++i)
@@ -188,6 +208,28 @@ __device__ __forceinline__ int bar_consumers_and(int pred) {
       : "r"(pred), "n"(N)
       : "memory");
   return r;
+}
+
+}  // namespace svk
+
+namespace svk {
+
+// Loads that are issued exactly where they appear (volatile asm is not moved),
+// so their latency overlaps the work that follows.
+__device__ __forceinline__ int ld_issue_s32(const int* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_issue_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ unsigned short ld_issue_u16(const unsigned short* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
 }
 
 }  // namespace svk

@@ -7,9 +7,9 @@
 namespace svk {
 
 // ------------------------------------------------------------------ chunk passes
-// `s` points at a shared-memory chunk of `n` consecutive row elements whose
-// first element is column `e0` of the row.  Consumer thread `c` handles the
-// 16-byte vectors c, c + 256, ... (conflict-free, coalesced).
+// `s` points at `n` consecutive row elements (shared memory, or global memory
+// for the second looks at a row) whose first element is column `e0`.
+// Consumer thread c handles the 16-byte vectors c, c + 256, ...
 
 template <typename T>
 __device__ __forceinline__ void chunk_argmax(const T* s, int n, int e0, float& bv, int& bi,
@@ -51,19 +51,19 @@ __device__ __forceinline__ void chunk_mass_f32(const float* s, int n, Acc& a, fl
     const float4 v1 = reinterpret_cast<const float4*>(s)[vi + kConsumers];
     const float x0[4] = {v0.x, v0.y, v0.z, v0.w};
     const float x1[4] = {v1.x, v1.y, v1.z, v1.w};
-    a.add<8>(tree_sum<4>(x0));
-    a.add<8>(tree_sum<4>(x1));
+    a.add(tree_sum<4>(x0));
+    a.add(tree_sum<4>(x1));
     mn = fmin_nan(mn, fmin_nan(fmin_nan(fmin_nan(v0.x, v0.y), fmin_nan(v0.z, v0.w)),
                                fmin_nan(fmin_nan(v1.x, v1.y), fmin_nan(v1.z, v1.w))));
   }
   if (vi < nv) {
     const float4 v = reinterpret_cast<const float4*>(s)[vi];
     const float x[4] = {v.x, v.y, v.z, v.w};
-    a.add<8>(tree_sum<4>(x));
+    a.add(tree_sum<4>(x));
     mn = fmin_nan(mn, fmin_nan(fmin_nan(v.x, v.y), fmin_nan(v.z, v.w)));
   }
   for (int e = (nv << 2) + threadIdx.x; e < n; e += kConsumers) {
-    a.add<8>(s[e]);
+    a.add(s[e]);
     mn = fmin_nan(mn, s[e]);
   }
 }
@@ -73,67 +73,113 @@ __device__ __forceinline__ void chunk_mass_f32(const float* s, int n, Acc& a, fl
 template <typename T>
 __device__ __forceinline__ void chunk_online(const T* s, int n, float k, Online& o, float& mx) {
   constexpr int VEC = ElemTraits<T>::kVec;
-  constexpr int FL = ElemTraits<T>::kFlush;
   const int nv = n / VEC;
   for (int vi = threadIdx.x; vi < nv; vi += kConsumers) {
     const float vm = vec_max_nan(s, vi);
     mx = fmax_nan(mx, vm);
     float x[VEC];
     load_vec(s, vi, x);
-    o.add_vec<VEC, FL>(x, vm, k);
+    o.add_vec<VEC>(x, vm, k);
   }
   for (int e = nv * VEC + threadIdx.x; e < n; e += kConsumers) {
     const float x = ElemTraits<T>::to_f(s[e]);
     mx = fmax_nan(mx, x);
-    o.add_vec<1, FL>(&x, x, k);
+    o.add_vec<1>(&x, x, k);
   }
 }
 
-template <typename T, typename W>
-__device__ __forceinline__ void chunk_write_weights(const T* s, int n, int e0, const W& wf,
-                                                    float* out) {
-  for (int e = threadIdx.x; e < n; e += kConsumers) out[e0 + e] = wf(ElemTraits<T>::to_f(s[e]));
-}
-
-template <typename T, typename W>
-__device__ __forceinline__ void chunk_exact(const T* s, int n, const W& wf, unsigned long long* bk,
-                                            uint32_t& bad) {
-  for (int e = threadIdx.x; e < n; e += kConsumers) {
-    const float x = wf(ElemTraits<T>::to_f(s[e]));
-    if (!(x <= FLT_MAX)) bad = 1u;  // +Inf (NaN and negatives were rejected before)
-    else bucket_add(bk, x);
+// Element e of a row slice in global memory.
+template <typename T>
+__device__ __forceinline__ float gload(const T* p, int e) {
+  if constexpr (sizeof(T) == 4) {
+    return __ldg(reinterpret_cast<const float*>(p) + e);
+  } else {
+    const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p) + e);
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    else return __half2float(__ushort_as_half(b));
   }
 }
 
-// Draw weights of vector `vi` of a chunk pair (`sq` may be null): writes up to
-// VEC weights and returns how many elements the vector holds.
-template <typename T, typename W>
-__device__ __forceinline__ int vec_draw_weights(const T* sp, const T* sq, int n, int vi,
-                                                const W& wfp, const W& wfq, const DrawW& dw,
-                                                float* r) {
+// Vector vi (16 bytes) of a 16-byte aligned row slice in global memory.
+template <typename T>
+__device__ __forceinline__ void gload_vec(const T* p, int vi, float* x) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + vi);
+  if constexpr (sizeof(T) == 4) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        x[2 * k] = bf_lo(w[k]);
+        x[2 * k + 1] = bf_hi(w[k]);
+      } else {
+        x[2 * k] = h_lo(w[k]);
+        x[2 * k + 1] = h_hi(w[k]);
+      }
+    }
+  }
+}
+
+// Draw weights of vector vi of a row slice pair in global memory (`q` may be
+// null).  Always fills VEC entries (zero past the slice end); returns the
+// number of real elements.
+template <typename T, typename D>
+__device__ __forceinline__ int vec_draw_weights(const T* p, const T* q, int n, int vi, bool vec_ok,
+                                                const D& dw, float* r) {
   constexpr int VEC = ElemTraits<T>::kVec;
   const int e0 = vi * VEC;
-  if (e0 + VEC <= n) {
-    float xp[VEC], xq[VEC];
-    load_vec(sp, vi, xp);
-    if (sq) load_vec(sq, vi, xq);
+  float xp[VEC], xq[VEC];
+  int cnt = VEC;
+  if (vec_ok && e0 + VEC <= n) {
+    gload_vec<T>(p, vi, xp);
+    if (q) gload_vec<T>(q, vi, xq);
+  } else {
+    cnt = min(VEC, n - e0);
 #pragma unroll
-    for (int k = 0; k < VEC; ++k) r[k] = dw(wfp(xp[k]), sq ? wfq(xq[k]) : 0.f);
-    return VEC;
+    for (int k = 0; k < VEC; ++k) {
+      xp[k] = k < cnt ? gload<T>(p, e0 + k) : 0.f;
+      xq[k] = (q && k < cnt) ? gload<T>(q, e0 + k) : 0.f;
+    }
   }
-  const int cnt = n - e0;
-  for (int k = 0; k < cnt; ++k) {
-    const float p = wfp(ElemTraits<T>::to_f(sp[e0 + k]));
-    const float q = sq ? wfq(ElemTraits<T>::to_f(sq[e0 + k])) : 0.f;
-    r[k] = dw(p, q);
-  }
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) r[k] = k < cnt ? dw(xp[k], q ? xq[k] : 0.f) : 0.f;
   return cnt;
 }
 
-// Left-to-right fp32 sum of r[0..cnt) (the order the owner's walk repeats).
-__device__ __forceinline__ float seq_sum_n(const float* r, int cnt) {
+// Draw weights of vector vi of a row slice pair staged in shared memory.
+template <typename T, typename D>
+__device__ __forceinline__ int svec_draw_weights(const T* p, const T* q, int n, int vi, const D& dw,
+                                                 float* r) {
+  constexpr int VEC = ElemTraits<T>::kVec;
+  const int e0 = vi * VEC;
+  float xp[VEC], xq[VEC];
+  int cnt = VEC;
+  if (e0 + VEC <= n) {
+    load_vec(p, vi, xp);
+    if (q) load_vec(q, vi, xq);
+  } else {
+    cnt = n - e0;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      xp[k] = k < cnt ? ElemTraits<T>::to_f(p[e0 + k]) : 0.f;
+      xq[k] = (q && k < cnt) ? ElemTraits<T>::to_f(q[e0 + k]) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) r[k] = k < cnt ? dw(xp[k], q ? xq[k] : 0.f) : 0.f;
+  return cnt;
+}
+
+// Left-to-right fp32 sum of r[0..VEC) (the order the owner's walk repeats).
+template <int VEC>
+__device__ __forceinline__ float seq_sum(const float* r) {
   float t = r[0];
-  for (int k = 1; k < cnt; ++k) t = __fadd_rn(t, r[k]);
+#pragma unroll
+  for (int k = 1; k < VEC; ++k) t = __fadd_rn(t, r[k]);
   return t;
 }
 
@@ -199,30 +245,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   const int v_hi = min(P.V, v_lo + P.slice);
   const int n_el = max(0, v_hi - v_lo);
   const int nck = (n_el + ck_el - 1) / ck_el;
-  const long long total_items = sampling ? static_cast<long long>(kb) * 2 * nck + nck
-                                         : static_cast<long long>(kb + 1) * nck;
-
-  // item g of this CTA's load sequence: (row, target/draft, chunk) -> source
-  auto item = [&](long long g, const T*& src, int& e0, int& n) {
-    long long r;
-    int j;
-    bool isq = false;
-    if (sampling) {
-      r = g / (2 * nck);
-      const int w = static_cast<int>(g - r * 2 * nck);
-      isq = w >= nck;
-      j = isq ? w - nck : w;
-    } else {
-      r = g / nck;
-      j = static_cast<int>(g - r * nck);
-    }
-    e0 = v_lo + j * ck_el;
-    n = min(v_hi, e0 + ck_el) - e0;
-    const long long row = isq ? d0 + r : t0 + r;
-    src = (isq ? drf : tgt) + row * P.stride + e0;
-  };
-  auto slot_ptr = [&](long long g) {
-    return reinterpret_cast<const T*>(ring + static_cast<long long>(g % S) * P.slot_bytes);
+  const int last_n = n_el - (nck - 1) * ck_el;
+  // start of this CTA's slice of target row r (draft row r when q)
+  auto row_slice = [&](bool q, int r) -> const T* {
+    return q ? drf + (d0 + r) * P.stride + v_lo : tgt + (t0 + r) * P.stride + v_lo;
   };
 
   // ---------------------------------------------------------------- barriers
@@ -233,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     }
     mbar_init(&sm.xbar[0], C);
     mbar_init(&sm.xbar[1], C);
+    mbar_init(&sm.redo_bar, 1);
     sm.stop = 0;
+    sm.go_row = 0;
+    sm.producer_done = 0;
     fence_mbar_init_cluster();
   }
   __syncthreads();
@@ -242,87 +271,150 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   // ================================================================ producer warp
   if (tid >= kConsumers) {
     const int lane = tid - kConsumers;
-    long long g = 0;
-    for (; g < total_items; ++g) {
-      const int slot = static_cast<int>(g % S);
-      int go = 1;
-      if (lane == 0) {
-        if (g >= S) {
-          const uint32_t par = static_cast<uint32_t>(((g / S) - 1) & 1);
-          uint32_t polls = 0;
-          while (!mbar_try_wait(&sm.empty[slot], par)) {
-            if (sm.stop || ++polls == kWaitPolls) {
-              go = 0;
-              break;
+    int slot = 0;
+    uint32_t round = 0;
+    bool stopped = false;
+    for (int r = 0; r <= kb && !stopped; ++r) {
+      const int parts = (sampling && r < kb) ? 2 : 1;
+      for (int part = 0; part < parts && !stopped; ++part) {
+        const T* rowp = row_slice(part == 1, r);
+        for (int j = 0; j < nck; ++j) {
+          int go = 1;
+          if (lane == 0) {
+            if (round > 0) {
+              uint32_t polls = 0;  // poll (not suspend): the stop flag must be seen at once
+              while (!mbar_test(&sm.empty[slot], (round - 1) & 1u)) {
+                if (sm.stop || ++polls == kWaitPolls * 64u) {
+                  go = 0;
+                  break;
+                }
+                __nanosleep(64);
+              }
+            }
+            // sampling: at most P.look chunks into a row whose predecessor is
+            // still undecided (a rejection would waste them)
+            if (go && sampling && part * nck + j >= P.look) {
+              uint32_t polls = 0;
+              while (r > sm.go_row && !sm.stop) {
+                __nanosleep(256);
+                if (++polls == kWaitPolls * 16u) break;
+              }
+            }
+            if (sm.stop) go = 0;
+          }
+          go = __shfl_sync(0xFFFFFFFFu, go, 0);
+          if (!go) {
+            stopped = true;
+            break;
+          }
+          const int n = j == nck - 1 ? last_n : ck_el;
+          const T* src = rowp + j * ck_el;
+          T* dst = reinterpret_cast<T*>(ring + slot * P.slot_bytes);
+          const uint32_t bytes = static_cast<uint32_t>(n) * ELEM;
+          const uint32_t tma = P.use_tma ? (bytes & ~15u) : 0u;
+          for (int e = static_cast<int>(tma / ELEM) + lane; e < n; e += 32) dst[e] = src[e];
+          __syncwarp();
+          if (lane == 0) {
+            if (tma) {
+              mbar_arrive_expect_tx(&sm.full[slot], tma);
+              bulk_g2s(dst, src, tma, &sm.full[slot]);
+            } else {
+              mbar_arrive_local(&sm.full[slot]);
             }
           }
-        }
-        if (sm.stop) go = 0;
-      }
-      go = __shfl_sync(0xFFFFFFFFu, go, 0);
-      if (!go) break;
-      const T* src;
-      int e0, n;
-      item(g, src, e0, n);
-      const uint32_t bytes = static_cast<uint32_t>(n) * ELEM;
-      const uint32_t tma = P.use_tma ? (bytes & ~15u) : 0u;
-      T* dst = reinterpret_cast<T*>(ring + static_cast<long long>(slot) * P.slot_bytes);
-      for (int e = static_cast<int>(tma / ELEM) + lane; e < n; e += 32) dst[e] = src[e];
-      __syncwarp();
-      if (lane == 0) {
-        if (tma) {
-          mbar_arrive_expect_tx(&sm.full[slot], tma);
-          bulk_g2s(dst, src, tma, &sm.full[slot]);
-        } else {
-          mbar_arrive_local(&sm.full[slot]);
+          if (++slot == S) {
+            slot = 0;
+            ++round;
+          }
         }
       }
     }
     // no bulk copy may still be writing this CTA's shared memory at exit
-    if (lane == 0)
-      for (long long gg = g > S ? g - S : 0; gg < g; ++gg)
-        mbar_wait_bounded(&sm.full[gg % S], static_cast<uint32_t>((gg / S) & 1));
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) {
+        if (s < slot) mbar_wait_bounded(&sm.full[s], round & 1u);
+        else if (round > 0) mbar_wait_bounded(&sm.full[s], (round - 1) & 1u);
+      }
+      __threadfence_block();
+      sm.producer_done = 1;
+    }
     return;
   }
 
   // ================================================================ consumers
-  const int lane = tid & 31;
+  const int lane = tid & 31, warp = tid >> 5;
+  // The last consumer warp fetches every row's decision inputs (draft token,
+  // uniform, p(t), q(t)) now, while the first chunks are still in flight.
+  if (warp == kWarps - 1 && lane < kMaxGather && lane <= kb) {
+    const int i = lane;
+    sm.g_u[i] = (sampling && P.uni) ? ld_issue_f32(P.uni + t0 + i) : 0.f;
+    int t = -1;
+    float gp = 0.f, gq = 0.f;
+    if (i < kb) {
+      t = ld_issue_s32(P.tok + d0 + i);
+      if (sampling && t >= 0 && t < P.V) {
+        if constexpr (sizeof(T) == 4) {
+          gp = ld_issue_f32(reinterpret_cast<const float*>(tgt + (t0 + i) * P.stride + t));
+          gq = ld_issue_f32(reinterpret_cast<const float*>(drf + (d0 + i) * P.stride + t));
+        } else {
+          const unsigned short hp =
+              ld_issue_u16(reinterpret_cast<const unsigned short*>(tgt + (t0 + i) * P.stride + t));
+          const unsigned short hq =
+              ld_issue_u16(reinterpret_cast<const unsigned short*>(drf + (d0 + i) * P.stride + t));
+          gp = TR::to_f(*reinterpret_cast<const T*>(&hp));
+          gq = TR::to_f(*reinterpret_cast<const T*>(&hq));
+        }
+      }
+    }
+    sm.g_t[i] = t;
+    sm.g_p[i] = gp;
+    sm.g_q[i] = gq;
+  }
+  // row i's inputs (thread 0, after a consumer barrier has passed)
+  auto row_token = [&](int i) -> int { return i < kMaxGather ? sm.g_t[i] : P.tok[d0 + i]; };
   uint32_t tmo = 0;
-  auto acquire = [&](long long g) {
-    if (!mbar_wait_bounded(&sm.full[g % S], static_cast<uint32_t>((g / S) & 1))) tmo = 1u;
+  int cslot = 0, rslot = 0;  // acquire and release cursors (same order)
+  uint32_t cround = 0;
+  auto acquire = [&]() -> const T* {
+    if (!mbar_wait_bounded(&sm.full[cslot], cround & 1u)) tmo = 1u;
+    const T* s = reinterpret_cast<const T*>(ring + cslot * P.slot_bytes);
+    if (++cslot == S) {
+      cslot = 0;
+      ++cround;
+    }
+    return s;
   };
-  auto release = [&](long long g) {
+  auto release = [&]() {
     __syncwarp();
-    if (lane == 0) mbar_arrive_local(&sm.empty[g % S]);
+    if (lane == 0) mbar_arrive_local(&sm.empty[rslot]);
+    if (++rslot == S) rslot = 0;
   };
 
+  // exchange of sm.myrec with every CTA of the cluster (thread 0 only)
   int xc = 0, last_slot = 0;
-  auto xchg = [&](int words) -> bool {
-    bar_consumers<kConsumers>();
+  auto send_recv = [&](int words) -> bool {
     const int slot = xc & 1;
     const uint32_t par = static_cast<uint32_t>((xc >> 1) & 1);
     ++xc;
     last_slot = slot;
-    if (tid < static_cast<int>(C)) {
-      const uint32_t dst = dsmem_addr(&sm.recs[slot][rank][0], static_cast<uint32_t>(tid));
+    for (uint32_t c = 0; c < C; ++c) {
+      const uint32_t dst = dsmem_addr(&sm.recs[slot][rank][0], c);
       for (int w = 0; w < words; w += 4)
         dsmem_st_v4(dst + 4u * w, *reinterpret_cast<const uint4*>(&sm.myrec[w]));
-      dsmem_arrive_release(dsmem_addr(&sm.xbar[slot], static_cast<uint32_t>(tid)));
+      dsmem_arrive_release(dsmem_addr(&sm.xbar[slot], c));
     }
-    const bool ok = mbar_wait_cluster_bounded(&sm.xbar[slot], par);
-    return bar_consumers_and<kConsumers>(ok) != 0;
+    return mbar_wait_cluster_bounded(&sm.xbar[slot], par);
   };
   auto rec = [&](uint32_t c, int w) -> uint32_t { return sm.recs[last_slot][c][w]; };
-  auto rec_d = [&](uint32_t c, int w) -> double {
-    return __hiloint2double(static_cast<int>(rec(c, w + 1)), static_cast<int>(rec(c, w)));
-  };
+  auto recf = [&](uint32_t c, int w) -> float { return __uint_as_float(rec(c, w)); };
   auto rec_u64 = [&](uint32_t c, int w) -> unsigned long long {
     return static_cast<unsigned long long>(rec(c, w)) |
            (static_cast<unsigned long long>(rec(c, w + 1)) << 32);
   };
-  auto put_d = [&](int w, double v) {
-    sm.myrec[w] = static_cast<uint32_t>(__double2loint(v));
-    sm.myrec[w + 1] = static_cast<uint32_t>(__double2hiint(v));
+  auto putf = [&](int w, float v) { sm.myrec[w] = __float_as_uint(v); };
+  auto put_u64 = [&](int w, unsigned long long v) {
+    sm.myrec[w] = static_cast<uint32_t>(v);
+    sm.myrec[w + 1] = static_cast<uint32_t>(v >> 32);
   };
   auto finish = [&](int n, int nxt, uint32_t s) {  // thread 0 of the writing CTA
     P.n_out[b] = n;
@@ -330,76 +422,85 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     P.st_out[b] = s;
   };
 
-  uint32_t st = 0;  // status bits (thread 0)
   bool abort = false;
 
   if (!sampling) {
     // ============================================================== greedy
+    uint32_t st = 0;
     for (int i = 0;; ++i) {
       float bv = __int_as_float(0x7FFFFFFF);  // NaN: no candidate yet
       int bi = INT_MAX;
       uint32_t nanf = 0;
       for (int j = 0; j < nck; ++j) {
-        const long long g = static_cast<long long>(i) * nck + j;
-        acquire(g);
-        const T* src;
-        int e0, n;
-        item(g, src, e0, n);
-        chunk_argmax<T>(slot_ptr(g), n, e0, bv, bi, nanf);
-        release(g);
+        const T* s = acquire();
+        chunk_argmax<T>(s, j == nck - 1 ? last_n : ck_el, v_lo + j * ck_el, bv, bi, nanf);
+        release();
       }
       if (bv != bv) bi = INT_MAX;
-      block_argmax(bv, bi, sm.redf, sm.redi);
-      nanf = static_cast<uint32_t>(bar_consumers_or<kConsumers>(static_cast<int>(nanf)));
-      tmo = static_cast<uint32_t>(bar_consumers_or<kConsumers>(static_cast<int>(tmo)));
+      warp_argmax(bv, bi);
+      const uint32_t fl = __reduce_or_sync(0xFFFFFFFFu, nanf | (tmo << 1));
+      if (lane == 0) {
+        sm.wf[warp][0] = bv;
+        sm.wi[warp][0] = bi;
+        sm.wi[warp][1] = static_cast<int>(fl);
+      }
+      bar_consumers<kConsumers>();
       if (tid == 0) {
-        sm.myrec[0] = __float_as_uint(bv);
-        sm.myrec[1] = static_cast<uint32_t>(bi);
-        sm.myrec[2] = nanf | (tmo << 1);
+        float v = sm.wf[0][0];
+        int a = sm.wi[0][0];
+        uint32_t f = static_cast<uint32_t>(sm.wi[0][1]);
+        for (int w = 1; w < kWarps; ++w) {
+          f |= static_cast<uint32_t>(sm.wi[w][1]);
+          if (arg_better(sm.wf[w][0], sm.wi[w][0], v, a)) {
+            v = sm.wf[w][0];
+            a = sm.wi[w][0];
+          }
+        }
+        sm.myrec[0] = __float_as_uint(v);
+        sm.myrec[1] = static_cast<uint32_t>(a);
+        sm.myrec[2] = f;
         sm.myrec[3] = 0u;
-      }
-      if (!xchg(4)) {
-        abort = true;
-        break;
-      }
-      float v = 0.f;
-      int a = INT_MAX;
-      uint32_t fl = 0;
-      for (uint32_t c = 0; c < C; ++c) {
-        const float vc = __uint_as_float(rec(c, 0));
-        const int ic = static_cast<int>(rec(c, 1));
-        fl |= rec(c, 2);
-        if (arg_better(vc, ic, v, a)) {
-          v = vc;
-          a = ic;
+        int act = ACT_CONTINUE;
+        if (!send_recv(4)) {
+          act = ACT_ABORT;
+        } else {
+          v = 0.f;
+          a = INT_MAX;
+          f = 0;
+          for (uint32_t c = 0; c < C; ++c) {
+            f |= rec(c, 2);
+            if (arg_better(recf(c, 0), static_cast<int>(rec(c, 1)), v, a)) {
+              v = recf(c, 0);
+              a = static_cast<int>(rec(c, 1));
+            }
+          }
+          if (f & 2u) {
+            act = ACT_ABORT;
+          } else {
+            if (a == INT_MAX) a = 0;  // an all-NaN row
+            if (f & 1u) st |= ST_BAD_VALUE;
+            if (i == kb) {
+              act = ACT_STOP;
+              if (rank == 0) finish(kb, a, st);
+            } else {
+              const int t = row_token(i);
+              if (t < 0 || t >= P.V) {
+                act = ACT_STOP;
+                if (rank == 0) finish(i, a, st | ST_BAD_TOKEN);
+              } else if (t != a) {
+                act = ACT_STOP;
+                if (rank == 0) finish(i, a, st);
+              }
+            }
+          }
         }
+        if (act != ACT_CONTINUE) sm.stop = 1;
+        sm.bi[0] = act;
       }
-      if (fl & 2u) {
-        abort = true;
-        break;
-      }
-      if (a == INT_MAX) a = 0;  // an all-NaN row
-      if (fl & 1u) st |= ST_BAD_VALUE;
-      bool stop = false;
-      uint32_t extra = 0;
-      if (i == kb) {
-        stop = true;
-      } else {
-        const int t = P.tok[d0 + i];
-        if (t < 0 || t >= P.V) {
-          stop = true;
-          extra = ST_BAD_TOKEN;
-        } else if (t != a) {
-          stop = true;
-        }
-      }
-      if (stop) {
-        if (tid == 0) {
-          sm.stop = 1;
-          if (rank == 0) finish(i, a, st | extra);
-        }
-        break;
-      }
+      bar_consumers<kConsumers>();
+      const int act = sm.bi[0];
+      if (act == ACT_ABORT) abort = true;
+      if (act != ACT_CONTINUE) break;
     }
   } else {
     // ============================================================== sampling
@@ -427,21 +528,37 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     };
     const bool force_exact = (P.flags & FLAG_FORCE_EXACT) != 0u;
     unsigned long long* buckets = vsum;  // the exact pass and the draw never overlap
+    // fp32 additions any element goes through inside its thread
+    int nadd = 0;
+    for (int j = 0; j < nck; ++j) {
+      const int n = j == nck - 1 ? last_n : ck_el;
+      nadd += (n / VEC + kConsumers - 1) / kConsumers + (n % VEC ? 1 : 0);
+    }
+    nadd += (VEC == 8 ? 3 : 2);
 
-    // Exact masses of the resident rows at item `base` (collective).  Thread 0
-    // receives the summed limbs in lp / lq and the +Inf flags.
+    // thread 0's state: status, exact limbs, the next row's draft token
+    uint32_t st = 0;
     uint32_t lp[kLimbs], lq[kLimbs];
-    auto exact_pass = [&](long long base, bool with_q, const WarpT& wfp, const WarpT& wfq,
+    int row_slot = 0;  // ring slot of the current row's first chunk
+
+    // Exact masses of row i (collective; reads the row slices from global
+    // memory).  Thread 0 receives the summed limbs and the +Inf flags.
+    auto exact_pass = [&](int i, bool with_q, const WarpT& wfp, const WarpT& wfq,
                           uint32_t& infl) -> bool {
       for (int k = tid; k < 2 * kBuckets; k += kConsumers) buckets[k] = 0ull;
       bar_consumers<kConsumers>();
       uint32_t bp = 0, bq = 0;
-      for (int j = 0; j < nck; ++j) {
-        const T* src;
-        int e0, n;
-        item(base + j, src, e0, n);
-        chunk_exact<T>(slot_ptr(base + j), n, wfp, buckets, bp);
-        if (with_q) chunk_exact<T>(slot_ptr(base + nck + j), n, wfq, buckets + kBuckets, bq);
+      const T* p = row_slice(false, i);
+      const T* q = with_q ? row_slice(true, i) : nullptr;
+      for (int e = tid; e < n_el; e += kConsumers) {
+        const float x = wfp(gload<T>(p, e));
+        if (!(x <= FLT_MAX)) bp = 1u;  // +Inf (NaN and negatives were rejected before)
+        else bucket_add(buckets, x);
+        if (q) {
+          const float y = wfq(gload<T>(q, e));
+          if (!(y <= FLT_MAX)) bq = 1u;
+          else bucket_add(buckets + kBuckets, y);
+        }
       }
       bp = static_cast<uint32_t>(bar_consumers_or<kConsumers>(static_cast<int>(bp)));
       bq = static_cast<uint32_t>(bar_consumers_or<kConsumers>(static_cast<int>(bq)));
@@ -450,131 +567,153 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         buckets_to_limbs(buckets + kBuckets, &sm.myrec[kLimbs]);
         sm.myrec[2 * kLimbs] = bp | (bq << 1);
         sm.myrec[2 * kLimbs + 1] = sm.myrec[2 * kLimbs + 2] = sm.myrec[2 * kLimbs + 3] = 0u;
-      }
-      if (!xchg(2 * kLimbs + 4)) return false;
-      if (tid == 0) {
-        unsigned long long ap[kLimbs], aq[kLimbs];
-        for (int k = 0; k < kLimbs; ++k) ap[k] = aq[k] = 0ull;
-        infl = 0;
-        for (uint32_t c = 0; c < C; ++c) {
-          for (int k = 0; k < kLimbs; ++k) {
-            ap[k] += rec(c, k);
-            aq[k] += rec(c, kLimbs + k);
+        const bool ok = send_recv(2 * kLimbs + 4);
+        if (ok) {
+          unsigned long long ap[kLimbs], aq[kLimbs];
+          for (int k = 0; k < kLimbs; ++k) ap[k] = aq[k] = 0ull;
+          infl = 0;
+          for (uint32_t c = 0; c < C; ++c) {
+            for (int k = 0; k < kLimbs; ++k) {
+              ap[k] += rec(c, k);
+              aq[k] += rec(c, kLimbs + k);
+            }
+            infl |= rec(c, 2 * kLimbs);
           }
-          infl |= rec(c, 2 * kLimbs);
+          unsigned long long cp = 0, cq = 0;
+          for (int k = 0; k < kLimbs; ++k) {
+            cp += ap[k];
+            cq += aq[k];
+            lp[k] = static_cast<uint32_t>(cp);
+            lq[k] = static_cast<uint32_t>(cq);
+            cp >>= 32;
+            cq >>= 32;
+          }
         }
-        unsigned long long cp = 0, cq = 0;
-        for (int k = 0; k < kLimbs; ++k) {
-          cp += ap[k];
-          cq += aq[k];
-          lp[k] = static_cast<uint32_t>(cp);
-          lq[k] = static_cast<uint32_t>(cq);
-          cp >>= 32;
-          cq >>= 32;
-        }
+        sm.bi[5] = ok ? 1 : 0;
       }
-      return true;
+      bar_consumers<kConsumers>();
+      return sm.bi[5] != 0;
     };
 
-    // Inverse-CDF draw over the resident row at item `base` (collective).
-    // Returns 0 when done (the owning CTA wrote the outputs), 1 when the
-    // residual is empty, -1 when a device wait gave up.
-    auto draw = [&](long long base, bool resid, const WarpT& wfp, const WarpT& wfq, double Zp,
-                    double Zq, int n_acc, uint32_t st_in, float u_draw) -> int {
-      DrawW dw;
-      norm_factors(Zp, dw.sp, dw.ap);
-      norm_factors(resid ? Zq : 1.0, dw.sq, dw.aq);
+    // Inverse-CDF draw over row i, whose chunks are still resident in the ring (collective).  Returns 0
+    // when done (the owning CTA wrote the outputs), 1 when the residual is
+    // empty, -1 when a device wait gave up.
+    using DrawT = typename std::conditional<MODE == MODE_LOGITS, DrawLogits, DrawProbs>::type;
+    auto draw = [&](bool resid, int n_acc, uint32_t st_in, float u_draw) -> int {
+      DrawT dw;
       dw.scale = __uint_as_float(static_cast<uint32_t>(127 + P.fixed_shift) << 23);
       dw.resid = resid ? 1 : 0;
-      const int vpc = ck_el / VEC;  // vectors per full chunk
+      if constexpr (MODE == MODE_LOGITS) {
+        dw.k = khi;  // c = -m k - log2 Z, folded into one FMA per element
+        dw.cp = sm.dpar[0];
+        dw.cq = sm.dpar[1];
+      } else {
+        dw.sp = sm.dpar[0];
+        dw.ap = sm.dpar[1];
+        dw.sq = sm.dpar[2];
+        dw.aq = sm.dpar[3];
+      }
+      // resident chunk j of the target (draft) slice and its vector count
+      const int vpc = ck_el / VEC;
+      auto chunk_of = [&](bool qpart, int j) -> const T* {
+        int s = row_slot + (qpart ? nck : 0) + j;
+        if (s >= S) s -= S;
+        if (s >= S) s -= S;
+        return reinterpret_cast<const T*>(ring + s * P.slot_bytes);
+      };
+      const int nvt = (n_el + VEC - 1) / VEC;
       unsigned long long mine = 0;
       for (int j = 0; j < nck; ++j) {
-        const T* src;
-        int e0, n;
-        item(base + j, src, e0, n);
-        const T* sp = slot_ptr(base + j);
-        const T* sq = resid ? slot_ptr(base + nck + j) : nullptr;
+        const T* p = chunk_of(false, j);
+        const T* q = resid ? chunk_of(true, j) : nullptr;
+        const int n = j == nck - 1 ? last_n : ck_el;
         const int nv = (n + VEC - 1) / VEC;
         for (int vi = tid; vi < nv; vi += kConsumers) {
           float r[VEC];
-          const int cnt = vec_draw_weights<T>(sp, sq, n, vi, wfp, wfq, dw, r);
-          const unsigned long long f = dw.fix(seq_sum_n(r, cnt));
+          svec_draw_weights<T>(p, q, n, vi, dw, r);
+          const unsigned long long f = dw.fix(seq_sum<VEC>(r));
           vsum[j * vpc + vi] = f;
           mine += f;
         }
       }
-      mine = block_sum_u64(mine, sm.redu);
+      mine = warp_sum_u64(mine);
+      if (lane == 0) sm.wu[warp] = mine;
+      bar_consumers<kConsumers>();
       if (tid == 0) {
-        sm.myrec[0] = static_cast<uint32_t>(mine);
-        sm.myrec[1] = static_cast<uint32_t>(mine >> 32);
+        unsigned long long tot = 0;
+        for (int w = 0; w < kWarps; ++w) tot += sm.wu[w];
+        put_u64(0, tot);
         sm.myrec[2] = sm.myrec[3] = 0u;
-      }
-      if (!xchg(4)) return -1;
-      unsigned long long R = 0;
-      for (uint32_t c = 0; c < C; ++c) R += rec_u64(c, 0);
-      if (R == 0) {
-        if (resid) return 1;
-        if (tid == 0 && rank == 0) finish(n_acc, -1, st_in | ST_ZERO_MASS);
-        return 0;
-      }
-      const unsigned long long tau = tau_of(u_draw, R);
-      unsigned long long cum = 0, tloc = 0;
-      uint32_t owner = C;
-      for (uint32_t c = 0; c < C; ++c) {
-        const unsigned long long rc = rec_u64(c, 0);
-        if (tau < cum + rc) {
-          owner = c;
-          tloc = tau - cum;
-          break;
+        int code = 0;
+        if (!send_recv(4)) {
+          code = -1;
+        } else {
+          unsigned long long R = 0;
+          for (uint32_t c = 0; c < C; ++c) R += rec_u64(c, 0);
+          if (R == 0) {
+            code = resid ? 1 : 0;
+            if (!resid && rank == 0) finish(n_acc, -1, st_in | ST_ZERO_MASS);
+          } else {
+            const unsigned long long tau = tau_of(u_draw, R);
+            unsigned long long cum = 0, tloc = 0;
+            uint32_t owner = C;
+            for (uint32_t c = 0; c < C; ++c) {
+              const unsigned long long rc = rec_u64(c, 0);
+              if (tau < cum + rc) {
+                owner = c;
+                tloc = tau - cum;
+                break;
+              }
+              cum += rc;
+            }
+            if (owner == C) {  // cannot happen: tau < R
+              if (rank == 0) finish(n_acc, -1, st_in | ST_TIMEOUT);
+            } else if (owner == rank) {
+              code = 2;  // this CTA walks its slice
+              sm.wu[0] = tloc;
+              sm.wu[1] = R;
+            }
+          }
         }
-        cum += rc;
+        sm.bi[0] = code;
       }
-      if (owner == C) {  // cannot happen: tau < R
-        if (tid == 0 && rank == 0) finish(n_acc, -1, st_in | ST_TIMEOUT);
-        return 0;
-      }
-      if (rank != owner) return 0;
+      bar_consumers<kConsumers>();
+      const int code = sm.bi[0];
+      if (code != 2) return code;
       // ---- the owner: a scan of its per-vector sums, then one vector's elements
-      int nvt = 0;
-      for (int j = 0; j < nck; ++j) {
-        const T* src;
-        int e0, n;
-        item(base + j, src, e0, n);
-        nvt = j * vpc + (n + VEC - 1) / VEC;
-      }
+      const unsigned long long tloc = sm.wu[0];
+      const double Rd = static_cast<double>(sm.wu[1]);
+      bar_consumers<kConsumers>();  // sm.wu is reused by the scan
       const int seg = (nvt + kConsumers - 1) / kConsumers;
       const int lo = min(nvt, tid * seg), hi = min(nvt, lo + seg);
       unsigned long long s = 0;
-      for (int q = lo; q < hi; ++q) s += vsum[q];
+      for (int v = lo; v < hi; ++v) s += vsum[v];
       unsigned long long tot;
-      const unsigned long long ex = block_excl_scan_u64(s, sm.redu, tot);
-      if (tid == 0) sm.bi[0] = -1;
+      const unsigned long long ex = block_excl_scan_u64(s, sm.wu, tot);
+      if (tid == 0) sm.bi[1] = -1;
       bar_consumers<kConsumers>();
       if (tloc >= ex && tloc < ex + s) {
         unsigned long long c0 = ex;
-        int q = lo;
-        for (; q < hi - 1; ++q) {
-          if (tloc < c0 + vsum[q]) break;
-          c0 += vsum[q];
+        int v = lo;
+        for (; v < hi - 1; ++v) {
+          if (tloc < c0 + vsum[v]) break;
+          c0 += vsum[v];
         }
-        const int j = q / vpc, vi = q - j * vpc;
-        const T* src;
-        int e0, n;
-        item(base + j, src, e0, n);
+        const int j = v / vpc, vi = v - j * vpc;  // once per draw
         float r[VEC];
-        const int cnt = vec_draw_weights<T>(slot_ptr(base + j),
-                                            resid ? slot_ptr(base + nck + j) : nullptr, n, vi,
-                                            wfp, wfq, dw, r);
-        float acc = 0.f;
+        const int cnt = svec_draw_weights<T>(chunk_of(false, j), resid ? chunk_of(true, j) : nullptr,
+                                             j == nck - 1 ? last_n : ck_el, vi, dw, r);
+        float acc = r[0];
         unsigned long long prev = c0;
-        for (int k = 0; k < cnt; ++k) {
-          acc = k == 0 ? r[0] : __fadd_rn(acc, r[k]);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          if (k > 0) acc = __fadd_rn(acc, r[k]);
           const unsigned long long cur = c0 + dw.fix(acc);
-          if (tloc < cur || k == cnt - 1) {
+          if (k < cnt && (tloc < cur || k == cnt - 1)) {
             const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
             const unsigned long long dmin = dlo < dhi ? dlo : dhi;
-            sm.bi[0] = e0 + vi * VEC + k;
-            sm.bi[1] = static_cast<double>(dmin) <= 1e-5 * static_cast<double>(R) ? 1 : 0;
+            sm.bi[1] = v_lo + j * ck_el + vi * VEC + k;
+            sm.bi[2] = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
             break;
           }
           prev = cur;
@@ -582,8 +721,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       }
       bar_consumers<kConsumers>();
       if (tid == 0) {
-        const int found = sm.bi[0];
-        const uint32_t near = (found >= 0 && sm.bi[1]) ? ST_NEAR : 0u;
+        const int found = sm.bi[1];
+        const uint32_t near = (found >= 0 && sm.bi[2]) ? ST_NEAR : 0u;
         finish(n_acc, found, found >= 0 ? (st_in | near) : (st_in | ST_TIMEOUT));
       }
       return 0;
@@ -591,16 +730,15 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
 
     for (int i = 0;; ++i) {
       const bool bonus = i == kb;
-      const long long base = static_cast<long long>(i) * 2 * nck;
-      const int nit = bonus ? nck : 2 * nck;
 
-      // decision inputs gathered early by thread 0 (their latency overlaps the pass)
+      // decision inputs: rows below kMaxGather were fetched at the start; later
+      // rows are loaded now by thread 0 (their latency overlaps the pass)
       int t = -1;
-      float gp = 0.f, gq = 0.f, u = 0.f;
-      if (tid == 0) {
-        u = P.uni[t0 + i];
+      float u = 0.f, gp = 0.f, gq = 0.f;
+      if (tid == 0 && i >= kMaxGather) {
+        u = ld_issue_f32(P.uni + t0 + i);
         if (!bonus) {
-          t = P.tok[d0 + i];
+          t = ld_issue_s32(P.tok + d0 + i);
           if (t >= 0 && t < P.V) {
             gp = TR::to_f(tgt[(t0 + i) * P.stride + t]);
             gq = TR::to_f(drf[(d0 + i) * P.stride + t]);
@@ -608,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         }
       }
 
-      // ---- the pass over this row's chunks, as they arrive
+      // ---- the pass over this row's chunks as they stream in
       Acc ap, aq;
       Online op, oq;
       ap.init();
@@ -617,179 +755,247 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       oq.init();
       float ep = MODE == MODE_PROBS ? kInfF : -kInfF;  // probs: min; logits: max (validity)
       float eq = ep;
-      for (int j = 0; j < nit; ++j) {
-        const long long g = base + j;
-        acquire(g);
-        const T* src;
-        int e0, n;
-        item(g, src, e0, n);
-        const bool isq = j >= nck;
-        if constexpr (MODE == MODE_PROBS)
-          chunk_mass_f32(reinterpret_cast<const float*>(slot_ptr(g)), n, isq ? aq : ap,
-                         isq ? eq : ep);
-        else
-          chunk_online<T>(slot_ptr(g), n, khi, isq ? oq : op, isq ? eq : ep);
+      row_slot = cslot;  // the row's chunks stay resident until its decision
+      for (int part = 0; part < (bonus ? 1 : 2); ++part) {
+        for (int j = 0; j < nck; ++j) {
+          const T* s = acquire();
+          const int n = j == nck - 1 ? last_n : ck_el;
+          if constexpr (MODE == MODE_PROBS)
+            chunk_mass_f32(reinterpret_cast<const float*>(s), n, part ? aq : ap, part ? eq : ep);
+          else
+            chunk_online<T>(s, n, khi, part ? oq : op, part ? eq : ep);
+        }
       }
 
-      // ---- CTA partials -> record
-      tmo = static_cast<uint32_t>(bar_consumers_or<kConsumers>(static_cast<int>(tmo)));
+      // ---- warp partials -> shared memory
+      const uint32_t tm = __reduce_or_sync(0xFFFFFFFFu, tmo);
       if constexpr (MODE == MODE_PROBS) {
-        double v[2] = {ap.total(), aq.total()};
-        block_sum_dn<2>(v, sm.redd);
-        block_ext_f2<1>(ep, eq, sm.redf);
-        if (tid == 0) {
-          put_d(0, v[0]);
-          put_d(2, v[1]);
-          sm.myrec[4] = __float_as_uint(ep);
-          sm.myrec[5] = __float_as_uint(eq);
-          sm.myrec[6] = tmo;
-          sm.myrec[7] = 0u;
-        }
-        if (!xchg(8)) {
-          abort = true;
-          break;
+        const float s0 = warp_sum_f(ap.f), s1 = warp_sum_f(aq.f);
+        const float m0 = warp_min_nan_f(ep), m1 = warp_min_nan_f(eq);
+        if (lane == 0) {
+          sm.wf[warp][0] = s0;
+          sm.wf[warp][1] = s1;
+          sm.wf[warp][2] = m0;
+          sm.wf[warp][3] = m1;
+          sm.wi[warp][0] = static_cast<int>(tm);
         }
       } else {
-        float mcp = op.m, mcq = oq.m;
-        block_ext_f2<0>(mcp, mcq, sm.redf);  // CTA running maxima (never NaN)
-        block_ext_f2<0>(ep, eq, sm.redf);    // NaN-propagating maxima (validity)
-        const int rr = block_max_i(max(op.r, oq.r), sm.redi);
-        double v[4] = {0.0, 0.0, 0.0, 0.0};
+        // rescale each lane's sums to the warp maximum (one more rescale step)
+        const float wmp = warp_max_f(op.m), wmq = warp_max_f(oq.m);
+        float sp = 0.f, wp = 0.f, sq = 0.f, wq = 0.f;
         if (op.m > -kInfF) {
-          const float d = __fmul_rn(__fsub_rn(mcp, op.m), khi);
-          const double f = static_cast<double>(ex2_ftz(-d));
-          v[0] = op.S() * f;
-          v[1] = (op.W() + static_cast<double>(d) * op.S()) * f;
+          const float d = __fmul_rn(__fsub_rn(wmp, op.m), khi);
+          const float f = ex2_ftz(-d);
+          sp = __fmul_rn(op.s, f);
+          wp = __fmul_rn(__fmaf_rn(d, op.s, op.w), f);
         }
         if (oq.m > -kInfF) {
-          const float d = __fmul_rn(__fsub_rn(mcq, oq.m), khi);
-          const double f = static_cast<double>(ex2_ftz(-d));
-          v[2] = oq.S() * f;
-          v[3] = (oq.W() + static_cast<double>(d) * oq.S()) * f;
+          const float d = __fmul_rn(__fsub_rn(wmq, oq.m), khi);
+          const float f = ex2_ftz(-d);
+          sq = __fmul_rn(oq.s, f);
+          wq = __fmul_rn(__fmaf_rn(d, oq.s, oq.w), f);
         }
-        block_sum_dn<4>(v, sm.redd);
-        if (tid == 0) {
-          sm.myrec[0] = __float_as_uint(mcp);
-          sm.myrec[1] = __float_as_uint(mcq);
-          sm.myrec[2] = __float_as_uint(ep);
-          sm.myrec[3] = __float_as_uint(eq);
-          put_d(4, v[0]);
-          put_d(6, v[1]);
-          put_d(8, v[2]);
-          put_d(10, v[3]);
-          sm.myrec[12] = static_cast<uint32_t>(rr);
-          sm.myrec[13] = tmo;
-          sm.myrec[14] = sm.myrec[15] = 0u;
-        }
-        if (!xchg(16)) {
-          abort = true;
-          break;
+        sp = warp_sum_f(sp);
+        wp = warp_sum_f(wp);
+        sq = warp_sum_f(sq);
+        wq = warp_sum_f(wq);
+        const float vmp = warp_max_nan_f(ep), vmq = warp_max_nan_f(eq);
+        const int rr = warp_max_i(max(op.r, oq.r));
+        if (lane == 0) {
+          sm.wf[warp][0] = wmp;
+          sm.wf[warp][1] = sp;
+          sm.wf[warp][2] = wp;
+          sm.wf[warp][3] = wmq;
+          sm.wf[warp][4] = sq;
+          sm.wf[warp][5] = wq;
+          sm.wf[warp][6] = vmp;
+          sm.wf[warp][7] = vmq;
+          sm.wi[warp][0] = static_cast<int>(tm);
+          sm.wi[warp][1] = rr;
         }
       }
+      bar_consumers<kConsumers>();
 
-      // ---- thread 0 combines the records (same order in every CTA)
+      // ---- thread 0: CTA record, exchange, combine (fp32 pairs), decide
+      if (tid == 0 && i < kMaxGather) {
+        u = sm.g_u[i];
+        t = bonus ? -1 : sm.g_t[i];
+        gp = sm.g_p[i];
+        gq = sm.g_q[i];
+      }
       if (tid == 0) {
-        double Zp = 0.0, Zq = 0.0, Bp = 0.0, Bq = 0.0;
-        float mp, mq, vp, vq;  // logits: row maxima / validity maxima; probs: minima
+        int act = ACT_CONTINUE;
+        DF Zp = {0.f, 0.f}, Zq = {0.f, 0.f};
+        float Bp = 0.f, Bq = 0.f;
+        float mp = 0.f, mq = 0.f, vp, vq;
         uint32_t anytmo = 0;
         if constexpr (MODE == MODE_PROBS) {
-          vp = vq = kInfF;
-          for (uint32_t c = 0; c < C; ++c) {
-            Zp += rec_d(c, 0);
-            Zq += rec_d(c, 2);
-            vp = fmin_nan(vp, __uint_as_float(rec(c, 4)));
-            vq = fmin_nan(vq, __uint_as_float(rec(c, 5)));
-            anytmo |= rec(c, 6);
+          DF s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
+          float m0 = kInfF, m1 = kInfF;
+          uint32_t tf = 0;
+          for (int w = 0; w < kWarps; ++w) {
+            s0 = df_add(s0, {sm.wf[w][0], 0.f});
+            s1 = df_add(s1, {sm.wf[w][1], 0.f});
+            m0 = fmin_nan(m0, sm.wf[w][2]);
+            m1 = fmin_nan(m1, sm.wf[w][3]);
+            tf |= static_cast<uint32_t>(sm.wi[w][0]);
           }
-          mp = mq = 0.f;
-          Bp = Zp * 16.0 * kU32;
-          Bq = Zq * 16.0 * kU32;
+          putf(0, s0.hi);
+          putf(1, s0.lo);
+          putf(2, s1.hi);
+          putf(3, s1.lo);
+          putf(4, m0);
+          putf(5, m1);
+          sm.myrec[6] = tf;
+          sm.myrec[7] = 0u;
+          if (!send_recv(8)) anytmo = 1;
+          vp = vq = kInfF;
+          if (!anytmo)
+            for (uint32_t c = 0; c < C; ++c) {
+              Zp = df_add(Zp, {recf(c, 0), recf(c, 1)});
+              Zq = df_add(Zq, {recf(c, 2), recf(c, 3)});
+              vp = fmin_nan(vp, recf(c, 4));
+              vq = fmin_nan(vq, recf(c, 5));
+              anytmo |= rec(c, 6);
+            }
+          Bp = sum_bound(Zp.hi, nadd);
+          Bq = sum_bound(Zq.hi, nadd);
         } else {
+          // warps -> CTA (one more rescale step)
+          float cmp = -kInfF, cmq = -kInfF, c6 = -kInfF, c7 = -kInfF;
+          int rr = 0;
+          uint32_t tf = 0;
+          for (int w = 0; w < kWarps; ++w) {
+            cmp = fmaxf(cmp, sm.wf[w][0]);
+            cmq = fmaxf(cmq, sm.wf[w][3]);
+            c6 = fmax_nan(c6, sm.wf[w][6]);
+            c7 = fmax_nan(c7, sm.wf[w][7]);
+            rr = max(rr, sm.wi[w][1]);
+            tf |= static_cast<uint32_t>(sm.wi[w][0]);
+          }
+          DF sp = {0.f, 0.f}, sq = {0.f, 0.f};
+          float wp = 0.f, wq = 0.f;
+          for (int w = 0; w < kWarps; ++w) {
+            if (sm.wf[w][0] > -kInfF) {
+              const float d = __fmul_rn(__fsub_rn(cmp, sm.wf[w][0]), khi);
+              const float f = ex2_ftz(-d);
+              sp = df_add(sp, two_prod(sm.wf[w][1], f));
+              wp = __fadd_rn(wp, __fmul_rn(__fmaf_rn(d, sm.wf[w][1], sm.wf[w][2]), f));
+            }
+            if (sm.wf[w][3] > -kInfF) {
+              const float d = __fmul_rn(__fsub_rn(cmq, sm.wf[w][3]), khi);
+              const float f = ex2_ftz(-d);
+              sq = df_add(sq, two_prod(sm.wf[w][4], f));
+              wq = __fadd_rn(wq, __fmul_rn(__fmaf_rn(d, sm.wf[w][4], sm.wf[w][5]), f));
+            }
+          }
+          putf(0, cmp);
+          putf(1, cmq);
+          putf(2, c6);
+          putf(3, c7);
+          putf(4, sp.hi);
+          putf(5, sp.lo);
+          putf(6, wp);
+          putf(7, sq.hi);
+          putf(8, sq.lo);
+          putf(9, wq);
+          sm.myrec[10] = static_cast<uint32_t>(rr);
+          sm.myrec[11] = tf;
+          if (!send_recv(12)) anytmo = 1;
           mp = mq = -kInfF;
           vp = vq = -kInfF;
           int R = 0;
-          for (uint32_t c = 0; c < C; ++c) {
-            mp = fmaxf(mp, __uint_as_float(rec(c, 0)));
-            mq = fmaxf(mq, __uint_as_float(rec(c, 1)));
-            vp = fmax_nan(vp, __uint_as_float(rec(c, 2)));
-            vq = fmax_nan(vq, __uint_as_float(rec(c, 3)));
-            R = max(R, static_cast<int>(rec(c, 12)));
-            anytmo |= rec(c, 13);
-          }
-          double Wp = 0.0, Wq = 0.0;
-          for (uint32_t c = 0; c < C; ++c) {
-            const float mcp = __uint_as_float(rec(c, 0)), mcq = __uint_as_float(rec(c, 1));
-            if (mcp > -kInfF) {
-              const float d = __fmul_rn(__fsub_rn(mp, mcp), khi);
-              const double f = exp2(-static_cast<double>(d));
-              Zp += rec_d(c, 4) * f;
-              Wp += (rec_d(c, 6) + static_cast<double>(d) * rec_d(c, 4)) * f;
+          if (!anytmo)
+            for (uint32_t c = 0; c < C; ++c) {
+              mp = fmaxf(mp, recf(c, 0));
+              mq = fmaxf(mq, recf(c, 1));
+              vp = fmax_nan(vp, recf(c, 2));
+              vq = fmax_nan(vq, recf(c, 3));
+              R = max(R, static_cast<int>(rec(c, 10)));
+              anytmo |= rec(c, 11);
             }
-            if (mcq > -kInfF) {
-              const float d = __fmul_rn(__fsub_rn(mq, mcq), khi);
-              const double f = exp2(-static_cast<double>(d));
-              Zq += rec_d(c, 8) * f;
-              Wq += (rec_d(c, 10) + static_cast<double>(d) * rec_d(c, 8)) * f;
+          float Wp = 0.f, Wq = 0.f;
+          if (!anytmo)
+            for (uint32_t c = 0; c < C; ++c) {  // CTAs -> cluster (one more rescale step)
+              const float mcp = recf(c, 0), mcq = recf(c, 1);
+              if (mcp > -kInfF) {
+                const float d = __fmul_rn(__fsub_rn(mp, mcp), khi);
+                const float f = ex2_ftz(-d);
+                Zp = df_add(Zp, df_mul_f({recf(c, 4), recf(c, 5)}, f));
+                Wp = __fadd_rn(Wp, __fmul_rn(__fmaf_rn(d, recf(c, 4), recf(c, 6)), f));
+              }
+              if (mcq > -kInfF) {
+                const float d = __fmul_rn(__fsub_rn(mq, mcq), khi);
+                const float f = ex2_ftz(-d);
+                Zq = df_add(Zq, df_mul_f({recf(c, 7), recf(c, 8)}, f));
+                Wq = __fadd_rn(Wq, __fmul_rn(__fmaf_rn(d, recf(c, 7), recf(c, 9)), f));
+              }
             }
-          }
-          Bp = online_bound(Zp, Wp, R) + static_cast<double>(P.V) * 1.2e-38;
-          Bq = online_bound(Zq, Wq, R) + static_cast<double>(P.V) * 1.2e-38;
+          Bp = online_bound(Zp.hi, Wp, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
+          Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
         }
         uint32_t err = 0;
-        if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
-        bool p_bad, q_bad;
-        if constexpr (MODE == MODE_PROBS) {
-          p_bad = !(vp >= 0.f);  // NaN or a negative value
-          q_bad = !bonus && !(vq >= 0.f);
+        bool p_bad = false, q_bad = false, need_x = false;
+        if (anytmo) {
+          act = ACT_ABORT;
         } else {
-          p_bad = !(vp < kInfF);  // NaN or +Inf logit
-          q_bad = !bonus && !(vq < kInfF);
+          if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
+          if constexpr (MODE == MODE_PROBS) {
+            p_bad = !(vp >= 0.f);  // NaN or a negative value
+            q_bad = !bonus && !(vq >= 0.f);
+            // a non-finite approximate mass means a +Inf element or an fp32
+            // overflow of the partial sums: the exact pass tells them apart
+            need_x = !err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (!bonus && !(Zq.hi <= FLT_MAX)));
+          } else {
+            p_bad = !(vp < kInfF);  // NaN or +Inf logit
+            q_bad = !bonus && !(vq < kInfF);
+          }
+          if (need_x) act = ACT_EXACT;
         }
-        // probabilities: a non-finite approximate mass means a +Inf element
-        // or an fp32 overflow of the partial sums; the exact pass tells.
-        const bool need_inf_check = MODE == MODE_PROBS && !anytmo && !err && !p_bad && !q_bad &&
-                                    (!(Zp <= DBL_MAX) || (!bonus && !(Zq <= DBL_MAX)));
-        sm.bi[0] = anytmo ? ACT_ABORT : ACT_CONTINUE;
+        sm.bi[0] = act;
         sm.bi[1] = static_cast<int>(err);
-        sm.bi[2] = (p_bad ? 1 : 0) | (q_bad ? 2 : 0) | (need_inf_check ? 4 : 0);
-        sm.bd[0] = Zp;
-        sm.bd[1] = Zq;
-        sm.bd[2] = Bp;
-        sm.bd[3] = Bq;
-        sm.bd[4] = static_cast<double>(mp);
-        sm.bd[5] = static_cast<double>(mq);
+        sm.bi[2] = (p_bad ? 1 : 0) | (q_bad ? 2 : 0);
+        sm.wf[0][0] = Zp.hi;
+        sm.wf[0][1] = Zp.lo;
+        sm.wf[0][2] = Zq.hi;
+        sm.wf[0][3] = Zq.lo;
+        sm.wf[0][4] = Bp;
+        sm.wf[0][5] = Bq;
+        sm.wf[0][6] = mp;
+        sm.wf[0][7] = mq;
       }
       bar_consumers<kConsumers>();
       if (sm.bi[0] == ACT_ABORT) {
         abort = true;
         break;
       }
-      const float mp = static_cast<float>(sm.bd[4]), mq = static_cast<float>(sm.bd[5]);
+      const float mp = sm.wf[0][6], mq = sm.wf[0][7];
       const WarpT wfp = make_warp(mp), wfq = make_warp(mq);
       bool have_exact = false;
-      if (sm.bi[2] & 4) {
+      double Zp_ex = 0.0, Zq_ex = 0.0;  // thread 0: exact masses when known
+      if (sm.bi[0] == ACT_EXACT) {  // +Inf check / overflow: exact masses now
         uint32_t infl = 0;
-        if (!exact_pass(base, !bonus, wfp, wfq, infl)) {
+        if (!exact_pass(i, !bonus, wfp, wfq, infl)) {
           abort = true;
           break;
         }
         if (tid == 0) {
-          sm.bi[2] = (sm.bi[2] & 3) | (infl & 1u ? 1 : 0) | (infl & 2u ? 2 : 0);
-          sm.bd[0] = limbs_to_double(lp);
-          sm.bd[1] = bonus ? 0.0 : limbs_to_double(lq);
+          sm.bi[2] |= (infl & 1u ? 1 : 0) | (infl & 2u ? 2 : 0);
+          Zp_ex = limbs_to_double(lp);
+          Zq_ex = bonus ? 0.0 : limbs_to_double(lq);
         }
         have_exact = true;
       }
-      // ---- input errors in the oracle's order, then the accept test
+      // ---- input errors in the oracle's order, then the accept test (thread 0)
       if (tid == 0) {
-        const double Zp = sm.bd[0], Zq = sm.bd[1];
+        const DF Zp = {sm.wf[0][0], sm.wf[0][1]}, Zq = {sm.wf[0][2], sm.wf[0][3]};
         uint32_t err = static_cast<uint32_t>(sm.bi[1]);
         const bool p_bad = sm.bi[2] & 1, q_bad = (sm.bi[2] >> 1) & 1;
         if (!err && p_bad) err = ST_BAD_VALUE;
         if (!err && q_bad) err = ST_BAD_VALUE;
         if (!err && !(u >= 0.f && u < 1.f)) err = ST_BAD_VALUE;
-        const bool p_zero = MODE == MODE_PROBS ? Zp == 0.0 : mp == -kInfF;
-        const bool q_zero = MODE == MODE_PROBS ? Zq == 0.0 : mq == -kInfF;
+        const bool p_zero = MODE == MODE_PROBS ? (have_exact ? Zp_ex == 0.0 : Zp.hi == 0.f) : mp == -kInfF;
+        const bool q_zero = MODE == MODE_PROBS ? (have_exact ? Zq_ex == 0.0 : Zq.hi == 0.f) : mq == -kInfF;
         int act;
         if (err) {
           if (rank == 0) finish(i, -1, st | err);
@@ -804,69 +1010,84 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           act = ACT_STOP;
         } else {
           const float pt = wfp(gp), qt = wfq(gq);
-          sm.bd[6] = pt;
-          sm.bd[7] = qt;
+          sm.wf[1][0] = pt;
+          sm.wf[1][1] = qt;
           if (have_exact) {
             act = exact_accept(u, pt, qt, lp, lq) ? ACT_CONTINUE : ACT_DRAW;
             st |= ST_EXACT;
           } else {
-            const int dec = filter_decide(u, pt, qt, Zp, sm.bd[2], Zq, sm.bd[3]);
+            const int dec = filter_decide(u, pt, qt, Zp, sm.wf[0][4], Zq, sm.wf[0][5]);
             act = (force_exact || dec < 0) ? ACT_EXACT : (dec ? ACT_CONTINUE : ACT_DRAW);
           }
         }
+        if (act == ACT_CONTINUE) sm.go_row = i + 1;
         if (act == ACT_STOP || act == ACT_DRAW) sm.stop = 1;
         sm.bi[0] = act;
-        sm.bi[4] = static_cast<int>(st);
       }
       bar_consumers<kConsumers>();
       int act = sm.bi[0];
       if (act == ACT_EXACT) {
         uint32_t infl = 0;
-        if (!exact_pass(base, true, wfp, wfq, infl)) {
+        if (!exact_pass(i, true, wfp, wfq, infl)) {
           abort = true;
           break;
         }
         if (tid == 0) {
-          act = exact_accept(u, static_cast<float>(sm.bd[6]), static_cast<float>(sm.bd[7]), lp, lq)
-                    ? ACT_CONTINUE
-                    : ACT_DRAW;
+          act = exact_accept(u, sm.wf[1][0], sm.wf[1][1], lp, lq) ? ACT_CONTINUE : ACT_DRAW;
           st |= ST_EXACT;
+          Zp_ex = limbs_to_double(lp);
+          Zq_ex = limbs_to_double(lq);
+          have_exact = true;
+          if (act == ACT_CONTINUE) sm.go_row = i + 1;
           if (act == ACT_DRAW) sm.stop = 1;
           sm.bi[0] = act;
-          sm.bi[4] = static_cast<int>(st);
         }
         bar_consumers<kConsumers>();
         act = sm.bi[0];
       }
       // warped weights of this row for the caller (testing aid)
       if (MODE == MODE_LOGITS && (P.wt_out || P.wd_out) && act != ACT_STOP) {
-        for (int j = 0; j < nck; ++j) {
-          const T* src;
-          int e0, n;
-          item(base + j, src, e0, n);
-          if (P.wt_out)
-            chunk_write_weights<T>(slot_ptr(base + j), n, e0, wfp,
-                                   P.wt_out + (t0 + i) * static_cast<long long>(P.V));
+        const T* p = row_slice(false, i);
+        const T* q = row_slice(true, i);
+        for (int e = tid; e < n_el; e += kConsumers) {
+          if (P.wt_out) P.wt_out[(t0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfp(gload<T>(p, e));
           if (P.wd_out && !bonus)
-            chunk_write_weights<T>(slot_ptr(base + nck + j), n, e0, wfq,
-                                   P.wd_out + (d0 + i) * static_cast<long long>(P.V));
+            P.wd_out[(d0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfq(gload<T>(q, e));
         }
       }
       if (act == ACT_STOP) break;
       if (act == ACT_CONTINUE) {
-        for (int j = 0; j < nit; ++j) release(base + j);
+        for (int j = 0; j < (bonus ? nck : 2 * nck); ++j) release();
         continue;
       }
       // ---- ACT_DRAW: the bonus from p_K, or the residual after the first rejection
-      const uint32_t st_now = static_cast<uint32_t>(sm.bi[4]);
-      const float u_draw = P.uni[t0 + kb];
+      if (tid == 0) {
+        sm.bi[3] = static_cast<int>(st);
+        const float ud = kb < kMaxGather ? sm.g_u[kb] : ld_issue_f32(P.uni + t0 + kb);
+        sm.wf[1][2] = ud;
+        // draw parameters (normalisations) in fp32, once
+        const float zp = have_exact ? static_cast<float>(Zp_ex) : __fadd_rn(sm.wf[0][0], sm.wf[0][1]);
+        const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : __fadd_rn(sm.wf[0][2], sm.wf[0][3]));
+        if constexpr (MODE == MODE_LOGITS) {
+          const DF mk = two_prod(mp, khi), qk = two_prod(mq, khi);
+          sm.dpar[0] = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
+          sm.dpar[1] = bonus ? 0.f : -__fadd_rn(qk.hi, __fadd_rn(qk.lo, log2f(zq)));
+        } else {
+          const double zpd = have_exact ? Zp_ex : static_cast<double>(zp);
+          const double zqd = have_exact && !bonus ? Zq_ex : static_cast<double>(zq);
+          norm_factors(zpd, sm.dpar[0], sm.dpar[1]);
+          norm_factors(zqd, sm.dpar[2], sm.dpar[3]);
+        }
+      }
+      bar_consumers<kConsumers>();
+      const uint32_t st_now = static_cast<uint32_t>(sm.bi[3]);
+      const float u_draw = sm.wf[1][2];
       if (!bonus && !(u_draw >= 0.f && u_draw < 1.f)) {
         if (tid == 0 && rank == 0) finish(i, -1, st_now | ST_BAD_VALUE);
         break;
       }
-      const double Zp = sm.bd[0], Zq = sm.bd[1];
-      int code = draw(base, !bonus, wfp, wfq, Zp, bonus ? 1.0 : Zq, bonus ? kb : i, st_now, u_draw);
-      if (code == 1) code = draw(base, false, wfp, wfq, Zp, 1.0, i, st_now | ST_ZERO_MASS, u_draw);
+      int code = draw(!bonus, bonus ? kb : i, st_now, u_draw);
+      if (code == 1) code = draw(false, i, st_now | ST_ZERO_MASS, u_draw);
       if (code < 0) abort = true;
       break;
     }
