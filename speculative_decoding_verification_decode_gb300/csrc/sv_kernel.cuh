@@ -228,6 +228,17 @@ __device__ __forceinline__ DF df_mul(DF x, DF y) {
 }
 __device__ __forceinline__ DF df_neg(DF x) { return {-x.hi, -x.lo}; }
 
+// Butterfly sum across a warp (the addition is commutative bit for bit, so
+// every lane ends with the same pair).
+__device__ __forceinline__ DF warp_sum_df(DF v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const DF w = {__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+    v = df_add(v, w);
+  }
+  return v;
+}
+
 // ------------------------------------------------------------------ accumulators
 
 // Per-thread fp32 sum of vector sums.  A thread that adds n_v vector sums

@@ -180,6 +180,16 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 
 namespace svk {
 
+// A full-mask ballot at the head of warp-collective code that follows
+// lane-divergent code or a warp-role branch.  It lets the compiler treat the
+// warp as converged from here on, so the shuffles and votes that follow take
+// the plain path; without it, reductions in such places ran several times
+// slower on sm_103a.
+__device__ __forceinline__ void warp_converged() {
+  const unsigned b = __ballot_sync(0xFFFFFFFFu, 1);
+  asm volatile("" ::"r"(b));
+}
+
 // Named barrier 1 over the `n` consumer threads (the producer warp never joins).
 template <int N>
 __device__ __forceinline__ void bar_consumers() {

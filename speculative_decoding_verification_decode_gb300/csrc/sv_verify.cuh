@@ -267,10 +267,14 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   }
   __syncthreads();
   cluster_sync_all();  // every peer's barriers exist before the first remote arrive
+  // The warp index taken from lane 0 is warp-uniform for the compiler too, so
+  // branches on it are not treated as divergent and the warp-collective code
+  // inside them compiles to its converged form.
+  const int warp = __shfl_sync(0xFFFFFFFFu, tid >> 5, 0);
+  const int lane = tid & 31;
 
   // ================================================================ producer warp
-  if (tid >= kConsumers) {
-    const int lane = tid - kConsumers;
+  if (warp == kWarps) {
     int slot = 0;
     uint32_t round = 0;
     bool stopped = false;
@@ -342,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   }
 
   // ================================================================ consumers
-  const int lane = tid & 31, warp = tid >> 5;
   // The last consumer warp fetches every row's decision inputs (draft token,
   // uniform, p(t), q(t)) now, while the first chunks are still in flight.
   if (warp == kWarps - 1 && lane < kMaxGather && lane <= kb) {
@@ -390,20 +393,24 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     if (++rslot == S) rslot = 0;
   };
 
-  // exchange of sm.myrec with every CTA of the cluster (thread 0 only)
+  // Exchange of sm.myrec with every CTA of the cluster: a collective of
+  // warp 0 (lane c pushes the record into CTA c, then every lane waits until
+  // all C records have arrived here).
   int xc = 0, last_slot = 0;
   auto send_recv = [&](int words) -> bool {
+    warp_converged();
     const int slot = xc & 1;
     const uint32_t par = static_cast<uint32_t>((xc >> 1) & 1);
     ++xc;
     last_slot = slot;
-    for (uint32_t c = 0; c < C; ++c) {
-      const uint32_t dst = dsmem_addr(&sm.recs[slot][rank][0], c);
+    if (lane < static_cast<int>(C)) {
+      const uint32_t dst = dsmem_addr(&sm.recs[slot][rank][0], static_cast<uint32_t>(lane));
       for (int w = 0; w < words; w += 4)
         dsmem_st_v4(dst + 4u * w, *reinterpret_cast<const uint4*>(&sm.myrec[w]));
-      dsmem_arrive_release(dsmem_addr(&sm.xbar[slot], c));
+      dsmem_arrive_release(dsmem_addr(&sm.xbar[slot], static_cast<uint32_t>(lane)));
     }
-    return mbar_wait_cluster_bounded(&sm.xbar[slot], par);
+    const bool ok = mbar_wait_cluster_bounded(&sm.xbar[slot], par);
+    return __all_sync(0xFFFFFFFFu, ok) != 0;
   };
   auto rec = [&](uint32_t c, int w) -> uint32_t { return sm.recs[last_slot][c][w]; };
   auto recf = [&](uint32_t c, int w) -> float { return __uint_as_float(rec(c, w)); };
@@ -437,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         release();
       }
       if (bv != bv) bi = INT_MAX;
+      warp_converged();
       warp_argmax(bv, bi);
       const uint32_t fl = __reduce_or_sync(0xFFFFFFFFu, nanf | (tmo << 1));
       if (lane == 0) {
@@ -445,38 +453,33 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         sm.wi[warp][1] = static_cast<int>(fl);
       }
       bar_consumers<kConsumers>();
-      if (tid == 0) {
-        float v = sm.wf[0][0];
-        int a = sm.wi[0][0];
-        uint32_t f = static_cast<uint32_t>(sm.wi[0][1]);
-        for (int w = 1; w < kWarps; ++w) {
-          f |= static_cast<uint32_t>(sm.wi[w][1]);
-          if (arg_better(sm.wf[w][0], sm.wi[w][0], v, a)) {
-            v = sm.wf[w][0];
-            a = sm.wi[w][0];
-          }
+      if (warp == 0) {
+        warp_converged();
+        // lanes 0..7: the warps' candidates; then the cluster's records
+        float v = lane < kWarps ? sm.wf[lane][0] : 0.f;
+        int a = lane < kWarps ? sm.wi[lane][0] : INT_MAX;
+        uint32_t f = lane < kWarps ? static_cast<uint32_t>(sm.wi[lane][1]) : 0u;
+        warp_argmax(v, a);
+        f = __reduce_or_sync(0xFFFFFFFFu, f);
+        if (lane == 0) {
+          sm.myrec[0] = __float_as_uint(v);
+          sm.myrec[1] = static_cast<uint32_t>(a);
+          sm.myrec[2] = f;
+          sm.myrec[3] = 0u;
         }
-        sm.myrec[0] = __float_as_uint(v);
-        sm.myrec[1] = static_cast<uint32_t>(a);
-        sm.myrec[2] = f;
-        sm.myrec[3] = 0u;
         int act = ACT_CONTINUE;
         if (!send_recv(4)) {
           act = ACT_ABORT;
         } else {
-          v = 0.f;
-          a = INT_MAX;
-          f = 0;
-          for (uint32_t c = 0; c < C; ++c) {
-            f |= rec(c, 2);
-            if (arg_better(recf(c, 0), static_cast<int>(rec(c, 1)), v, a)) {
-              v = recf(c, 0);
-              a = static_cast<int>(rec(c, 1));
-            }
-          }
+          warp_converged();
+          const bool mine = lane < static_cast<int>(C);
+          v = mine ? recf(lane, 0) : 0.f;
+          a = mine ? static_cast<int>(rec(lane, 1)) : INT_MAX;
+          f = __reduce_or_sync(0xFFFFFFFFu, mine ? rec(lane, 2) : 0u);
+          warp_argmax(v, a);
           if (f & 2u) {
             act = ACT_ABORT;
-          } else {
+          } else if (lane == 0) {
             if (a == INT_MAX) a = 0;  // an all-NaN row
             if (f & 1u) st |= ST_BAD_VALUE;
             if (i == kb) {
@@ -494,8 +497,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
             }
           }
         }
-        if (act != ACT_CONTINUE) sm.stop = 1;
-        sm.bi[0] = act;
+        if (lane == 0) {
+          if (act != ACT_CONTINUE) sm.stop = 1;
+          sm.bi[0] = act;
+        }
       }
       bar_consumers<kConsumers>();
       const int act = sm.bi[0];
@@ -567,7 +572,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         buckets_to_limbs(buckets + kBuckets, &sm.myrec[kLimbs]);
         sm.myrec[2 * kLimbs] = bp | (bq << 1);
         sm.myrec[2 * kLimbs + 1] = sm.myrec[2 * kLimbs + 2] = sm.myrec[2 * kLimbs + 3] = 0u;
-        const bool ok = send_recv(2 * kLimbs + 4);
+      }
+      bool ok = true;
+      if (warp == 0) ok = send_recv(2 * kLimbs + 4);
+      if (tid == 0) {
         if (ok) {
           unsigned long long ap[kLimbs], aq[kLimbs];
           for (int k = 0; k < kLimbs; ++k) ap[k] = aq[k] = 0ull;
@@ -636,46 +644,51 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           mine += f;
         }
       }
+      warp_converged();
       mine = warp_sum_u64(mine);
       if (lane == 0) sm.wu[warp] = mine;
       bar_consumers<kConsumers>();
-      if (tid == 0) {
-        unsigned long long tot = 0;
-        for (int w = 0; w < kWarps; ++w) tot += sm.wu[w];
-        put_u64(0, tot);
-        sm.myrec[2] = sm.myrec[3] = 0u;
+      if (warp == 0) {
+        warp_converged();
+        const unsigned long long tot = warp_sum_u64(lane < kWarps ? sm.wu[lane] : 0ull);
+        if (lane == 0) {
+          put_u64(0, tot);
+          sm.myrec[2] = sm.myrec[3] = 0u;
+        }
         int code = 0;
         if (!send_recv(4)) {
           code = -1;
         } else {
-          unsigned long long R = 0;
-          for (uint32_t c = 0; c < C; ++c) R += rec_u64(c, 0);
+          warp_converged();
+          // lanes 0..C-1: the CTAs' totals, an inclusive scan across lanes
+          const unsigned long long rc = lane < static_cast<int>(C) ? rec_u64(lane, 0) : 0ull;
+          unsigned long long inc = rc;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += n;
+          }
+          const unsigned long long R = __shfl_sync(0xFFFFFFFFu, inc, 31);
           if (R == 0) {
             code = resid ? 1 : 0;
-            if (!resid && rank == 0) finish(n_acc, -1, st_in | ST_ZERO_MASS);
+            if (lane == 0 && !resid && rank == 0) finish(n_acc, -1, st_in | ST_ZERO_MASS);
           } else {
             const unsigned long long tau = tau_of(u_draw, R);
-            unsigned long long cum = 0, tloc = 0;
-            uint32_t owner = C;
-            for (uint32_t c = 0; c < C; ++c) {
-              const unsigned long long rc = rec_u64(c, 0);
-              if (tau < cum + rc) {
-                owner = c;
-                tloc = tau - cum;
-                break;
-              }
-              cum += rc;
-            }
-            if (owner == C) {  // cannot happen: tau < R
-              if (rank == 0) finish(n_acc, -1, st_in | ST_TIMEOUT);
-            } else if (owner == rank) {
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, lane < static_cast<int>(C) && tau < inc);
+            const int owner = hit ? __ffs(hit) - 1 : -1;
+            const unsigned long long before = owner >= 0 ? __shfl_sync(0xFFFFFFFFu, inc - rc, owner) : 0ull;
+            if (owner < 0) {  // cannot happen: tau < R
+              if (lane == 0 && rank == 0) finish(n_acc, -1, st_in | ST_TIMEOUT);
+            } else if (owner == static_cast<int>(rank)) {
               code = 2;  // this CTA walks its slice
-              sm.wu[0] = tloc;
-              sm.wu[1] = R;
+              if (lane == 0) {
+                sm.wu[0] = tau - before;
+                sm.wu[1] = R;
+              }
             }
           }
         }
-        sm.bi[0] = code;
+        if (lane == 0) sm.bi[0] = code;
       }
       bar_consumers<kConsumers>();
       const int code = sm.bi[0];
@@ -689,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       unsigned long long s = 0;
       for (int v = lo; v < hi; ++v) s += vsum[v];
       unsigned long long tot;
+      warp_converged();
       const unsigned long long ex = block_excl_scan_u64(s, sm.wu, tot);
       if (tid == 0) sm.bi[1] = -1;
       bar_consumers<kConsumers>();
@@ -768,6 +782,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       }
 
       // ---- warp partials -> shared memory
+      warp_converged();
       const uint32_t tm = __reduce_or_sync(0xFFFFFFFFu, tmo);
       if constexpr (MODE == MODE_PROBS) {
         const float s0 = warp_sum_f(ap.f), s1 = warp_sum_f(aq.f);
@@ -823,146 +838,152 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         gp = sm.g_p[i];
         gq = sm.g_q[i];
       }
-      if (tid == 0) {
+      if (warp == 0) {
+        warp_converged();
+        // lane w < 8 holds warp w's partials, lane c < C will hold CTA c's record
+        const bool wl = lane < kWarps;
+        const bool cl = lane < static_cast<int>(C);
         int act = ACT_CONTINUE;
         DF Zp = {0.f, 0.f}, Zq = {0.f, 0.f};
         float Bp = 0.f, Bq = 0.f;
         float mp = 0.f, mq = 0.f, vp, vq;
         uint32_t anytmo = 0;
         if constexpr (MODE == MODE_PROBS) {
-          DF s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
-          float m0 = kInfF, m1 = kInfF;
-          uint32_t tf = 0;
-          for (int w = 0; w < kWarps; ++w) {
-            s0 = df_add(s0, {sm.wf[w][0], 0.f});
-            s1 = df_add(s1, {sm.wf[w][1], 0.f});
-            m0 = fmin_nan(m0, sm.wf[w][2]);
-            m1 = fmin_nan(m1, sm.wf[w][3]);
-            tf |= static_cast<uint32_t>(sm.wi[w][0]);
+          const DF s0 = warp_sum_df({wl ? sm.wf[lane][0] : 0.f, 0.f});
+          const DF s1 = warp_sum_df({wl ? sm.wf[lane][1] : 0.f, 0.f});
+          const float m0 = warp_min_nan_f(wl ? sm.wf[lane][2] : kInfF);
+          const float m1 = warp_min_nan_f(wl ? sm.wf[lane][3] : kInfF);
+          const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(sm.wi[lane][0]) : 0u);
+          if (lane == 0) {
+            putf(0, s0.hi);
+            putf(1, s0.lo);
+            putf(2, s1.hi);
+            putf(3, s1.lo);
+            putf(4, m0);
+            putf(5, m1);
+            sm.myrec[6] = tf;
+            sm.myrec[7] = 0u;
           }
-          putf(0, s0.hi);
-          putf(1, s0.lo);
-          putf(2, s1.hi);
-          putf(3, s1.lo);
-          putf(4, m0);
-          putf(5, m1);
-          sm.myrec[6] = tf;
-          sm.myrec[7] = 0u;
           if (!send_recv(8)) anytmo = 1;
           vp = vq = kInfF;
-          if (!anytmo)
-            for (uint32_t c = 0; c < C; ++c) {
-              Zp = df_add(Zp, {recf(c, 0), recf(c, 1)});
-              Zq = df_add(Zq, {recf(c, 2), recf(c, 3)});
-              vp = fmin_nan(vp, recf(c, 4));
-              vq = fmin_nan(vq, recf(c, 5));
-              anytmo |= rec(c, 6);
-            }
+          if (!anytmo) {
+            warp_converged();
+            Zp = warp_sum_df({cl ? recf(lane, 0) : 0.f, cl ? recf(lane, 1) : 0.f});
+            Zq = warp_sum_df({cl ? recf(lane, 2) : 0.f, cl ? recf(lane, 3) : 0.f});
+            vp = warp_min_nan_f(cl ? recf(lane, 4) : kInfF);
+            vq = warp_min_nan_f(cl ? recf(lane, 5) : kInfF);
+            anytmo = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 6) : 0u);
+          }
           Bp = sum_bound(Zp.hi, nadd);
           Bq = sum_bound(Zq.hi, nadd);
         } else {
           // warps -> CTA (one more rescale step)
-          float cmp = -kInfF, cmq = -kInfF, c6 = -kInfF, c7 = -kInfF;
-          int rr = 0;
-          uint32_t tf = 0;
-          for (int w = 0; w < kWarps; ++w) {
-            cmp = fmaxf(cmp, sm.wf[w][0]);
-            cmq = fmaxf(cmq, sm.wf[w][3]);
-            c6 = fmax_nan(c6, sm.wf[w][6]);
-            c7 = fmax_nan(c7, sm.wf[w][7]);
-            rr = max(rr, sm.wi[w][1]);
-            tf |= static_cast<uint32_t>(sm.wi[w][0]);
-          }
+          const float wmp = wl ? sm.wf[lane][0] : -kInfF, wmq = wl ? sm.wf[lane][3] : -kInfF;
+          const float cmp = warp_max_f(wmp), cmq = warp_max_f(wmq);
+          const float c6 = warp_max_nan_f(wl ? sm.wf[lane][6] : -kInfF);
+          const float c7 = warp_max_nan_f(wl ? sm.wf[lane][7] : -kInfF);
+          const int rr = warp_max_i(wl ? sm.wi[lane][1] : 0);
+          const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(sm.wi[lane][0]) : 0u);
           DF sp = {0.f, 0.f}, sq = {0.f, 0.f};
           float wp = 0.f, wq = 0.f;
-          for (int w = 0; w < kWarps; ++w) {
-            if (sm.wf[w][0] > -kInfF) {
-              const float d = __fmul_rn(__fsub_rn(cmp, sm.wf[w][0]), khi);
-              const float f = ex2_ftz(-d);
-              sp = df_add(sp, two_prod(sm.wf[w][1], f));
-              wp = __fadd_rn(wp, __fmul_rn(__fmaf_rn(d, sm.wf[w][1], sm.wf[w][2]), f));
-            }
-            if (sm.wf[w][3] > -kInfF) {
-              const float d = __fmul_rn(__fsub_rn(cmq, sm.wf[w][3]), khi);
-              const float f = ex2_ftz(-d);
-              sq = df_add(sq, two_prod(sm.wf[w][4], f));
-              wq = __fadd_rn(wq, __fmul_rn(__fmaf_rn(d, sm.wf[w][4], sm.wf[w][5]), f));
-            }
+          if (wmp > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(cmp, wmp), khi);
+            const float f = ex2_ftz(-d);
+            sp = two_prod(sm.wf[lane][1], f);
+            wp = __fmul_rn(__fmaf_rn(d, sm.wf[lane][1], sm.wf[lane][2]), f);
           }
-          putf(0, cmp);
-          putf(1, cmq);
-          putf(2, c6);
-          putf(3, c7);
-          putf(4, sp.hi);
-          putf(5, sp.lo);
-          putf(6, wp);
-          putf(7, sq.hi);
-          putf(8, sq.lo);
-          putf(9, wq);
-          sm.myrec[10] = static_cast<uint32_t>(rr);
-          sm.myrec[11] = tf;
+          if (wmq > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(cmq, wmq), khi);
+            const float f = ex2_ftz(-d);
+            sq = two_prod(sm.wf[lane][4], f);
+            wq = __fmul_rn(__fmaf_rn(d, sm.wf[lane][4], sm.wf[lane][5]), f);
+          }
+          warp_converged();
+          sp = warp_sum_df(sp);
+          sq = warp_sum_df(sq);
+          wp = warp_sum_f(wp);
+          wq = warp_sum_f(wq);
+          if (lane == 0) {
+            putf(0, cmp);
+            putf(1, cmq);
+            putf(2, c6);
+            putf(3, c7);
+            putf(4, sp.hi);
+            putf(5, sp.lo);
+            putf(6, wp);
+            putf(7, sq.hi);
+            putf(8, sq.lo);
+            putf(9, wq);
+            sm.myrec[10] = static_cast<uint32_t>(rr);
+            sm.myrec[11] = tf;
+          }
           if (!send_recv(12)) anytmo = 1;
           mp = mq = -kInfF;
           vp = vq = -kInfF;
-          int R = 0;
-          if (!anytmo)
-            for (uint32_t c = 0; c < C; ++c) {
-              mp = fmaxf(mp, recf(c, 0));
-              mq = fmaxf(mq, recf(c, 1));
-              vp = fmax_nan(vp, recf(c, 2));
-              vq = fmax_nan(vq, recf(c, 3));
-              R = max(R, static_cast<int>(rec(c, 10)));
-              anytmo |= rec(c, 11);
+          if (!anytmo) {
+            warp_converged();
+            const float rmp = cl ? recf(lane, 0) : -kInfF, rmq = cl ? recf(lane, 1) : -kInfF;
+            mp = warp_max_f(rmp);
+            mq = warp_max_f(rmq);
+            vp = warp_max_nan_f(cl ? recf(lane, 2) : -kInfF);
+            vq = warp_max_nan_f(cl ? recf(lane, 3) : -kInfF);
+            const int R = warp_max_i(cl ? static_cast<int>(rec(lane, 10)) : 0);
+            anytmo = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 11) : 0u);
+            // CTAs -> cluster (one more rescale step)
+            DF zp = {0.f, 0.f}, zq = {0.f, 0.f};
+            float w1 = 0.f, w2 = 0.f;
+            if (rmp > -kInfF) {
+              const float d = __fmul_rn(__fsub_rn(mp, rmp), khi);
+              const float f = ex2_ftz(-d);
+              zp = df_mul_f({recf(lane, 4), recf(lane, 5)}, f);
+              w1 = __fmul_rn(__fmaf_rn(d, recf(lane, 4), recf(lane, 6)), f);
             }
-          float Wp = 0.f, Wq = 0.f;
-          if (!anytmo)
-            for (uint32_t c = 0; c < C; ++c) {  // CTAs -> cluster (one more rescale step)
-              const float mcp = recf(c, 0), mcq = recf(c, 1);
-              if (mcp > -kInfF) {
-                const float d = __fmul_rn(__fsub_rn(mp, mcp), khi);
-                const float f = ex2_ftz(-d);
-                Zp = df_add(Zp, df_mul_f({recf(c, 4), recf(c, 5)}, f));
-                Wp = __fadd_rn(Wp, __fmul_rn(__fmaf_rn(d, recf(c, 4), recf(c, 6)), f));
-              }
-              if (mcq > -kInfF) {
-                const float d = __fmul_rn(__fsub_rn(mq, mcq), khi);
-                const float f = ex2_ftz(-d);
-                Zq = df_add(Zq, df_mul_f({recf(c, 7), recf(c, 8)}, f));
-                Wq = __fadd_rn(Wq, __fmul_rn(__fmaf_rn(d, recf(c, 7), recf(c, 9)), f));
-              }
+            if (rmq > -kInfF) {
+              const float d = __fmul_rn(__fsub_rn(mq, rmq), khi);
+              const float f = ex2_ftz(-d);
+              zq = df_mul_f({recf(lane, 7), recf(lane, 8)}, f);
+              w2 = __fmul_rn(__fmaf_rn(d, recf(lane, 7), recf(lane, 9)), f);
             }
-          Bp = online_bound(Zp.hi, Wp, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
-          Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
-        }
-        uint32_t err = 0;
-        bool p_bad = false, q_bad = false, need_x = false;
-        if (anytmo) {
-          act = ACT_ABORT;
-        } else {
-          if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
-          if constexpr (MODE == MODE_PROBS) {
-            p_bad = !(vp >= 0.f);  // NaN or a negative value
-            q_bad = !bonus && !(vq >= 0.f);
-            // a non-finite approximate mass means a +Inf element or an fp32
-            // overflow of the partial sums: the exact pass tells them apart
-            need_x = !err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (!bonus && !(Zq.hi <= FLT_MAX)));
-          } else {
-            p_bad = !(vp < kInfF);  // NaN or +Inf logit
-            q_bad = !bonus && !(vq < kInfF);
+            warp_converged();
+            Zp = warp_sum_df(zp);
+            Zq = warp_sum_df(zq);
+            const float Wp = warp_sum_f(w1), Wq = warp_sum_f(w2);
+            Bp = online_bound(Zp.hi, Wp, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
+            Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
           }
-          if (need_x) act = ACT_EXACT;
         }
-        sm.bi[0] = act;
-        sm.bi[1] = static_cast<int>(err);
-        sm.bi[2] = (p_bad ? 1 : 0) | (q_bad ? 2 : 0);
-        sm.wf[0][0] = Zp.hi;
-        sm.wf[0][1] = Zp.lo;
-        sm.wf[0][2] = Zq.hi;
-        sm.wf[0][3] = Zq.lo;
-        sm.wf[0][4] = Bp;
-        sm.wf[0][5] = Bq;
-        sm.wf[0][6] = mp;
-        sm.wf[0][7] = mq;
+        // lane 0: input errors seen so far and the next action
+        if (lane == 0) {
+          uint32_t err = 0;
+          bool p_bad = false, q_bad = false, need_x = false;
+          if (anytmo) {
+            act = ACT_ABORT;
+          } else {
+            if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
+            if constexpr (MODE == MODE_PROBS) {
+              p_bad = !(vp >= 0.f);  // NaN or a negative value
+              q_bad = !bonus && !(vq >= 0.f);
+              // a non-finite approximate mass means a +Inf element or an fp32
+              // overflow of the partial sums: the exact pass tells them apart
+              need_x = !err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (!bonus && !(Zq.hi <= FLT_MAX)));
+            } else {
+              p_bad = !(vp < kInfF);  // NaN or +Inf logit
+              q_bad = !bonus && !(vq < kInfF);
+            }
+            if (need_x) act = ACT_EXACT;
+          }
+          sm.bi[0] = act;
+          sm.bi[1] = static_cast<int>(err);
+          sm.bi[2] = (p_bad ? 1 : 0) | (q_bad ? 2 : 0);
+          sm.wf[0][0] = Zp.hi;
+          sm.wf[0][1] = Zp.lo;
+          sm.wf[0][2] = Zq.hi;
+          sm.wf[0][3] = Zq.lo;
+          sm.wf[0][4] = Bp;
+          sm.wf[0][5] = Bq;
+          sm.wf[0][6] = mp;
+          sm.wf[0][7] = mq;
+        }
       }
       bar_consumers<kConsumers>();
       if (sm.bi[0] == ACT_ABORT) {
