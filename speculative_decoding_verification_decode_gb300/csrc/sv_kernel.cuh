@@ -57,6 +57,7 @@ constexpr double kU32 = 5.9604644775390625e-8;  // 2^-24, unit roundoff of f32
 // Relative error bound used for ex2.approx.ftz.f32 (normal results); the
 // measured maximum on GB300 is checked against it by a GPU test.
 constexpr double kEx2Rel = 4.76837158203125e-7;  // 2^-21
+static_assert(kEx2Rel == 8.0 * kU32, "online_bound() writes e as 8u");
 
 struct Params {
   const void* tgt;
@@ -244,7 +245,7 @@ __device__ __forceinline__ DF warp_sum_df(DF v) {
 // Per-thread fp32 sum of vector sums.  A thread that adds n_v vector sums
 // (each a pairwise tree of VEC elements) is within (n_v + log2 VEC) * 2^-24 of
 // its exact sum; the block and cluster levels add 6 more roundings (a 5-level
-// warp tree in fp32, then fp64).  sum_bound() states the total bound.
+// warp tree in fp32, then fp32 pairs).  sum_bound() states the total bound.
 struct Acc {
   float f;
   __device__ __forceinline__ void init() { f = 0.f; }
@@ -252,7 +253,7 @@ struct Acc {
 };
 
 __device__ __forceinline__ float sum_bound(float Z, int nadd) {
-  return 2.02f * Z * static_cast<float>((nadd + 8) * kU32);
+  return 2.02f * Z * (static_cast<float>(nadd + 8) * 0x1p-24f);
 }
 
 // ------------------------------------------------------------------ logits -> weights
@@ -342,9 +343,30 @@ struct Online {
 };
 
 __device__ __forceinline__ float online_bound(float S, float W, int R, int nadd) {
-  const float cs = static_cast<float>((R + 3) * (kEx2Rel + kU32) + 2.0 * kEx2Rel + (nadd + 8) * kU32);
-  const float cw = static_cast<float>(4.0 * 0.6931471805599453 * kU32);
+  // (R + 3)(e + u) + 2e + (nadd + 8)u with e = 8u: an integer times u, exact
+  // in fp32 (no fp64 on this path)
+  const float cs = static_cast<float>(9 * (R + 3) + 16 + nadd + 8) * 0x1p-24f;
+  constexpr float cw = 2.7725888f * 0x1p-24f;  // 4 ln2 u, rounded up
   return 2.02f * (S * cs + W * cw);
+}
+
+// k = log2(e) / T as an fp32 pair (hi, lo) without fp64, whose rate on this
+// part is a small fraction of fp32's: the correctly rounded quotient, its
+// remainder by one FMA (exact), and a correction quotient.  k is clamped to
+// FLT_MAX (a temperature so small that 1/T overflows).
+__device__ __forceinline__ void log2e_over(float T, float& khi, float& klo) {
+  constexpr float kL2eHi = 1.44269502162933349609375f;  // fp32 nearest to log2(e)
+  constexpr float kL2eLo = 1.925963033500011e-08f;      // log2(e) - kL2eHi
+  const float q = __fdiv_rn(kL2eHi, T);
+  if (!(q < FLT_MAX)) {
+    khi = FLT_MAX;
+    klo = 0.f;
+    return;
+  }
+  const float r = __fmaf_rn(-q, T, kL2eHi);
+  const DF k = fast_two_sum(q, __fdiv_rn(__fadd_rn(r, kL2eLo), T));
+  khi = k.hi;
+  klo = k.lo;
 }
 
 // ------------------------------------------------------------------ warp reductions

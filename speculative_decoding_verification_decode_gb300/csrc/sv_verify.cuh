@@ -510,12 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   } else {
     // ============================================================== sampling
     float khi = 0.f, klo = 0.f;
-    if (MODE == MODE_LOGITS) {
-      double kd = 1.4426950408889634074 / static_cast<double>(temp);
-      if (kd > FLT_MAX) kd = FLT_MAX;
-      khi = static_cast<float>(kd);
-      klo = static_cast<float>(kd - static_cast<double>(khi));
-    }
+    if (MODE == MODE_LOGITS) log2e_over(temp, khi, klo);
     auto make_warp = [&](float m) {
       WarpT w;
       if constexpr (MODE == MODE_LOGITS) {
