@@ -53,6 +53,7 @@ constexpr size_t kSmemPerSM = 227 * 1024;  // usable shared memory per SM (bytes
 constexpr size_t kSmemTwoCtas = kSmemPerSM / 2 - 1024;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr int kSampleSlots = 6;  // ring depth cap in sampling mode
 
 // Layout of one CTA's dynamic shared memory for a given cluster size C and
 // ring depth S: [ring S x slot][per-vector draw sums][SmemTail].
@@ -69,9 +70,9 @@ void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
   size_t ring = static_cast<size_t>(p.S) * p.slot_bytes;
   size_t vs = 0;
   if (sampling) {
-    // the current row pair stays resident until its decision, plus one chunk
-    // of lookahead into the next row
-    p.S = 2 * p.nck + 1;
+    // room for the current row pair and the first chunk of the next row, at
+    // most kSampleSlots chunks (the next row streams in as slots free up)
+    p.S = 2 * p.nck + 1 < kSampleSlots ? 2 * p.nck + 1 : kSampleSlots;
     ring = static_cast<size_t>(p.S) * p.slot_bytes;
     // one u64 per 16-byte vector of the slice, or the exact-sum buckets
     vs = static_cast<size_t>((slice + vec - 1) / vec) * 8;
@@ -117,7 +118,7 @@ sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
   prm.S = pl.S;
   prm.vsum_off = pl.vsum_off;
   prm.tail_off = pl.tail_off;
-  prm.look = 1;
+  prm.look = 1;  // stream the next row while the current one is decided
   const unsigned gy = static_cast<unsigned>(prm.B < 65535 ? prm.B : 65535);
   const unsigned gz = static_cast<unsigned>((prm.B + gy - 1) / gy);
   cudaLaunchConfig_t cfg = {};
@@ -230,7 +231,7 @@ sv_status sv_accept(const float* target_probs, const float* draft_probs, int64_t
   if (!uniforms) return fail(SV_ERR_ARG, "uniforms is NULL");
   Plan pl;
   if (!make_plan(true, batch, vocab, 4, pl))
-    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large for a resident row pair", vocab);
+    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large", vocab);
   svk::Params p = base_params(target_probs, draft_probs, row_stride, draft_tokens, uniforms, cu_k,
                               nullptr, batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
   p.use_tma = aligned16(target_probs) && (!draft_probs || aligned16(draft_probs)) &&
@@ -256,7 +257,7 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
   const int elem = dtype == SV_F32 ? 4 : 2;
   Plan pl;
   if (!make_plan(true, batch, vocab, elem, pl))
-    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large for a resident row pair", vocab);
+    return fail(SV_ERR_UNSUPPORTED, "vocab %d too large", vocab);
   svk::Params p = base_params(target_logits, draft_logits, row_stride, draft_tokens, uniforms, cu_k,
                               temperature, batch, k, vocab, sum_k, n_accepted, next_token, status,
                               flags);

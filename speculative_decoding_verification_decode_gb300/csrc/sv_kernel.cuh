@@ -10,17 +10,18 @@
 //     shared memory: each CTA pushes a small record into every peer and
 //     arrives on the peer's mbarrier; every CTA then takes the same decision
 //     from the same records in the same order (no global-memory scratch);
-//   * greedy chunks are released as soon as they are reduced; in sampling mode
-//     the current row pair stays resident until its decision, so the exact
-//     fallback, the residual and the inverse-CDF scan read shared memory only;
-//   * the walk stops at the first miss / rejection; later rows are not read
-//     (chunks already in flight are drained before exit).
+//   * chunks are released as soon as they are reduced, so the producer streams
+//     the next row while the current one is being decided (one row of
+//     lookahead); the exact fallback, the residual and the inverse-CDF walk
+//     read the decided row again from global memory (mostly L2);
+//   * the walk stops at the first miss / rejection; rows past the next one
+//     are never read (chunks already in flight are drained before exit).
 //
 // Decisions in sampling mode are the exact real predicate
 //     u * q(t) * Zp  <  p(t) * Zq
 // on the exact sums Zp, Zq of the f32 row weights: an approximate sum with a
 // rigorous error bound decides whenever the bound allows, otherwise the CTAs
-// sum the resident rows exactly (integer significand buckets, 32-bit limbs)
+// sum the row exactly (integer significand buckets, 32-bit limbs)
 // and compare big integers.  Inverse-CDF draws run in 64-bit fixed point so
 // every level (vector, thread, block, cluster) of the scan is consistent.
 #pragma once
@@ -80,7 +81,7 @@ struct Params {
   int use_tma;
   int fixed_shift;
   int vsum_off;  // byte offset of the per-vector draw sums (sampling)
-  int look;      // chunks the producer may stream into a row not yet reached
+  int look;      // rows the producer may stream past the last accepted row
   int tail_off;  // byte offset of SmemTail
 };
 
@@ -172,6 +173,40 @@ __device__ __forceinline__ float vec_max_nan(const T* s, int vi) {
     return fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w));
   } else {
     const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+      const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+      return fmax_nan(bf_lo(m), bf_hi(m));
+    } else {
+      const uint32_t m = f16x2_max_nan(f16x2_max_nan(v.x, v.y), f16x2_max_nan(v.z, v.w));
+      return fmax_nan(h_lo(m), h_hi(m));
+    }
+  }
+}
+
+// One 16-byte vector of a shared-memory chunk: unpacked floats and their
+// NaN-propagating maximum (packed compare for 16-bit types), from one load.
+template <typename T>
+__device__ __forceinline__ float load_vec_max(const T* s, int vi, float* x) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 v = reinterpret_cast<const float4*>(s)[vi];
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+    return fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w));
+  } else {
+    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        x[2 * k] = bf_lo(w[k]);
+        x[2 * k + 1] = bf_hi(w[k]);
+      } else {
+        x[2 * k] = h_lo(w[k]);
+        x[2 * k + 1] = h_hi(w[k]);
+      }
+    }
     if constexpr (std::is_same<T, __nv_bfloat16>::value) {
       const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
       return fmax_nan(bf_lo(m), bf_hi(m));
@@ -339,6 +374,41 @@ struct Online {
     }
     s = __fadd_rn(s, tree_sum<VEC>(e));
     w = __fadd_rn(w, __fadd_rn(wa, wb));
+  }
+  // U vectors at once (vectors u with have[u] false are absent): one max
+  // test and rescale for the block, then U * VEC independent exps.  Each
+  // element still goes through one vector tree and one addition into s.
+  template <int U, int VEC>
+  __device__ __forceinline__ void add_block(const float (&x)[U][VEC], const bool (&have)[U], float vm,
+                                            float k) {
+    if (!(vm <= m)) {
+      if (!(vm > -kInfF)) return;  // NaN (flagged by the caller) or all -Inf
+      if (m == -kInfF) m = vm;
+      else rescale_to(vm, k);
+    }
+    if (m == -kInfF) return;
+    float t[U], wv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float e[VEC];
+      float wa = 0.f, wb = 0.f;
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        const float nx = fminf(__fmul_rn(__fsub_rn(m, x[u][j]), k), 3.0e38f);
+        e[j] = ex2_ftz(-nx);
+        if (j & 1) wb = __fmaf_rn(e[j], nx, wb);
+        else wa = __fmaf_rn(e[j], nx, wa);
+      }
+      t[u] = tree_sum<VEC>(e);
+      wv[u] = __fadd_rn(wa, wb);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (have[u]) {
+        s = __fadd_rn(s, t[u]);
+        w = __fadd_rn(w, wv[u]);
+      }
+    }
   }
 };
 

@@ -15,19 +15,29 @@ template <typename T>
 __device__ __forceinline__ void chunk_argmax(const T* s, int n, int e0, float& bv, int& bi,
                                              uint32_t& nanf) {
   constexpr int VEC = ElemTraits<T>::kVec;
+  constexpr int U = 4;  // vectors a thread tests at once
   const int nv = n / VEC;
-  for (int vi = threadIdx.x; vi < nv; vi += kConsumers) {
-    const float m = vec_max_nan(s, vi);
-    if (!(m <= bv)) {  // a new maximum, a NaN, or no candidate yet
-      float x[VEC];
-      load_vec(s, vi, x);
+  for (int base = threadIdx.x; base < nv; base += U * kConsumers) {
+    float x[U][VEC];
+    float m = -kInfF;
 #pragma unroll
-      for (int k = 0; k < VEC; ++k) {
-        if (x[k] != x[k]) {
-          nanf = 1u;
-        } else if (bv != bv || x[k] > bv) {
-          bv = x[k];
-          bi = e0 + vi * VEC + k;
+    for (int u = 0; u < U; ++u) {
+      const int vi = base + u * kConsumers;
+      if (vi < nv) m = fmax_nan(m, load_vec_max(s, vi, x[u]));
+    }
+    if (!(m <= bv)) {  // a new maximum, a NaN, or no candidate yet (rare)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int vi = base + u * kConsumers;
+        if (vi >= nv) break;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          if (x[u][k] != x[u][k]) {
+            nanf = 1u;
+          } else if (bv != bv || x[u][k] > bv) {
+            bv = x[u][k];
+            bi = e0 + vi * VEC + k;
+          }
         }
       }
     }
@@ -73,13 +83,25 @@ __device__ __forceinline__ void chunk_mass_f32(const float* s, int n, Acc& a, fl
 template <typename T>
 __device__ __forceinline__ void chunk_online(const T* s, int n, float k, Online& o, float& mx) {
   constexpr int VEC = ElemTraits<T>::kVec;
+  constexpr int U = 4;  // vectors a thread holds at once (independent exps)
   const int nv = n / VEC;
-  for (int vi = threadIdx.x; vi < nv; vi += kConsumers) {
-    const float vm = vec_max_nan(s, vi);
+  for (int base = threadIdx.x; base < nv; base += U * kConsumers) {
+    float x[U][VEC];
+    bool have[U];
+    float vm = -kInfF;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = base + u * kConsumers;
+      have[u] = vi < nv;
+      if (have[u]) {
+        vm = fmax_nan(vm, load_vec_max(s, vi, x[u]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[u][j] = -kInfF;
+      }
+    }
     mx = fmax_nan(mx, vm);
-    float x[VEC];
-    load_vec(s, vi, x);
-    o.add_vec<VEC>(x, vm, k);
+    o.add_block<U, VEC>(x, have, vm, k);
   }
   for (int e = nv * VEC + threadIdx.x; e < n; e += kConsumers) {
     const float x = ElemTraits<T>::to_f(s[e]);
@@ -97,6 +119,29 @@ __device__ __forceinline__ float gload(const T* p, int e) {
     const unsigned short b = __ldg(reinterpret_cast<const unsigned short*>(p) + e);
     if constexpr (std::is_same<T, __nv_bfloat16>::value) return __uint_as_float(static_cast<uint32_t>(b) << 16);
     else return __half2float(__ushort_as_half(b));
+  }
+}
+
+// The floats of one 16-byte vector.
+template <typename T>
+__device__ __forceinline__ void unpack_vec(const uint4 v, float* x) {
+  if constexpr (sizeof(T) == 4) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        x[2 * k] = bf_lo(w[k]);
+        x[2 * k + 1] = bf_hi(w[k]);
+      } else {
+        x[2 * k] = h_lo(w[k]);
+        x[2 * k + 1] = h_hi(w[k]);
+      }
+    }
   }
 }
 
@@ -295,11 +340,12 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
                 __nanosleep(64);
               }
             }
-            // sampling: at most P.look chunks into a row whose predecessor is
-            // still undecided (a rejection would waste them)
-            if (go && sampling && part * nck + j >= P.look) {
+            // sampling: at most P.look rows past the last accepted one (the
+            // next row streams in while this one is decided; a rejection
+            // wastes what was fetched of it)
+            if (go && sampling) {
               uint32_t polls = 0;
-              while (r > sm.go_row && !sm.stop) {
+              while (r > sm.go_row + P.look && !sm.stop) {
                 __nanosleep(256);
                 if (++polls == kWaitPolls * 16u) break;
               }
@@ -539,7 +585,6 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     // thread 0's state: status, exact limbs, the next row's draft token
     uint32_t st = 0;
     uint32_t lp[kLimbs], lq[kLimbs];
-    int row_slot = 0;  // ring slot of the current row's first chunk
 
     // Exact masses of row i (collective; reads the row slices from global
     // memory).  Thread 0 receives the summed limbs and the +Inf flags.
@@ -598,11 +643,12 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       return sm.bi[5] != 0;
     };
 
-    // Inverse-CDF draw over row i, whose chunks are still resident in the ring (collective).  Returns 0
-    // when done (the owning CTA wrote the outputs), 1 when the residual is
-    // empty, -1 when a device wait gave up.
+    // Inverse-CDF draw over row i, read again from global memory (it was just
+    // streamed, so mostly from L2; collective).  Returns 0 when done (the
+    // owning CTA wrote the outputs), 1 when the residual is empty, -1 when a
+    // device wait gave up.
     using DrawT = typename std::conditional<MODE == MODE_LOGITS, DrawLogits, DrawProbs>::type;
-    auto draw = [&](bool resid, int n_acc, uint32_t st_in, float u_draw) -> int {
+    auto draw = [&](int n_acc_row, bool resid, int n_acc, uint32_t st_in, float u_draw) -> int {
       DrawT dw;
       dw.scale = __uint_as_float(static_cast<uint32_t>(127 + P.fixed_shift) << 23);
       dw.resid = resid ? 1 : 0;
@@ -616,26 +662,39 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         dw.sq = sm.dpar[2];
         dw.aq = sm.dpar[3];
       }
-      // resident chunk j of the target (draft) slice and its vector count
-      const int vpc = ck_el / VEC;
-      auto chunk_of = [&](bool qpart, int j) -> const T* {
-        int s = row_slot + (qpart ? nck : 0) + j;
-        if (s >= S) s -= S;
-        if (s >= S) s -= S;
-        return reinterpret_cast<const T*>(ring + s * P.slot_bytes);
-      };
+      const T* gp = row_slice(false, n_acc_row);
+      const T* gq = resid ? row_slice(true, n_acc_row) : nullptr;
+      const bool vec_ok = P.use_tma != 0;  // 16-byte aligned rows (slices start on vectors)
       const int nvt = (n_el + VEC - 1) / VEC;
       unsigned long long mine = 0;
-      for (int j = 0; j < nck; ++j) {
-        const T* p = chunk_of(false, j);
-        const T* q = resid ? chunk_of(true, j) : nullptr;
-        const int n = j == nck - 1 ? last_n : ck_el;
-        const int nv = (n + VEC - 1) / VEC;
-        for (int vi = tid; vi < nv; vi += kConsumers) {
+      constexpr int U = 4;  // vectors whose loads are in flight together
+      const int nfull = vec_ok ? n_el / VEC : 0;  // whole vectors read as 16-byte loads
+      for (int base = tid; base < nvt; base += U * kConsumers) {
+        uint4 rp[U], rq[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int vi = base + u * kConsumers;
+          if (vi < nfull) {
+            rp[u] = __ldg(reinterpret_cast<const uint4*>(gp) + vi);
+            rq[u] = gq ? __ldg(reinterpret_cast<const uint4*>(gq) + vi) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int vi = base + u * kConsumers;
+          if (vi >= nvt) break;
           float r[VEC];
-          svec_draw_weights<T>(p, q, n, vi, dw, r);
+          if (vi < nfull) {
+            float xp[VEC], xq[VEC];
+            unpack_vec<T>(rp[u], xp);
+            unpack_vec<T>(rq[u], xq);
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) r[q] = dw(xp[q], gq ? xq[q] : 0.f);
+          } else {
+            vec_draw_weights<T>(gp, gq, n_el, vi, vec_ok, dw, r);
+          }
           const unsigned long long f = dw.fix(seq_sum<VEC>(r));
-          vsum[j * vpc + vi] = f;
+          vsum[vi] = f;
           mine += f;
         }
       }
@@ -708,10 +767,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           if (tloc < c0 + vsum[v]) break;
           c0 += vsum[v];
         }
-        const int j = v / vpc, vi = v - j * vpc;  // once per draw
         float r[VEC];
-        const int cnt = svec_draw_weights<T>(chunk_of(false, j), resid ? chunk_of(true, j) : nullptr,
-                                             j == nck - 1 ? last_n : ck_el, vi, dw, r);
+        const int cnt = vec_draw_weights<T>(gp, gq, n_el, v, vec_ok, dw, r);
         float acc = r[0];
         unsigned long long prev = c0;
 #pragma unroll
@@ -721,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           if (k < cnt && (tloc < cur || k == cnt - 1)) {
             const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
             const unsigned long long dmin = dlo < dhi ? dlo : dhi;
-            sm.bi[1] = v_lo + j * ck_el + vi * VEC + k;
+            sm.bi[1] = v_lo + v * VEC + k;
             sm.bi[2] = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
             break;
           }
@@ -764,7 +821,6 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       oq.init();
       float ep = MODE == MODE_PROBS ? kInfF : -kInfF;  // probs: min; logits: max (validity)
       float eq = ep;
-      row_slot = cslot;  // the row's chunks stay resident until its decision
       for (int part = 0; part < (bonus ? 1 : 2); ++part) {
         for (int j = 0; j < nck; ++j) {
           const T* s = acquire();
@@ -773,6 +829,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
             chunk_mass_f32(reinterpret_cast<const float*>(s), n, part ? aq : ap, part ? eq : ep);
           else
             chunk_online<T>(s, n, khi, part ? oq : op, part ? eq : ep);
+          release();  // the slot takes the next row's chunks while this row is decided
         }
       }
 
@@ -1072,10 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         }
       }
       if (act == ACT_STOP) break;
-      if (act == ACT_CONTINUE) {
-        for (int j = 0; j < (bonus ? nck : 2 * nck); ++j) release();
-        continue;
-      }
+      if (act == ACT_CONTINUE) continue;
       // ---- ACT_DRAW: the bonus from p_K, or the residual after the first rejection
       if (tid == 0) {
         sm.bi[3] = static_cast<int>(st);
@@ -1102,8 +1156,8 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         if (tid == 0 && rank == 0) finish(i, -1, st_now | ST_BAD_VALUE);
         break;
       }
-      int code = draw(!bonus, bonus ? kb : i, st_now, u_draw);
-      if (code == 1) code = draw(false, i, st_now | ST_ZERO_MASS, u_draw);
+      int code = draw(i, !bonus, bonus ? kb : i, st_now, u_draw);
+      if (code == 1) code = draw(i, false, i, st_now | ST_ZERO_MASS, u_draw);
       if (code < 0) abort = true;
       break;
     }
