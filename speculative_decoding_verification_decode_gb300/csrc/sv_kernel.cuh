@@ -36,7 +36,8 @@ namespace svk {
 
 constexpr int kConsumers = 256;  // consumer threads (8 warps)
 constexpr int kWarps = kConsumers / 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kDecideWarp = kWarps + 1;    // warp 9 (sampling): combines and decides rows
+constexpr int kThreads = kConsumers + 64;  // + the producer warp and the decision warp
 constexpr int kMaxSlots = 16;
 constexpr int kMaxSlotBytes = 32768;
 constexpr int kMaxCluster = 16;
@@ -85,11 +86,24 @@ struct Params {
   int tail_off;  // byte offset of SmemTail
 };
 
+// A row's outcome, from the decision warp to the consumer warps.
+struct Dec {
+  int act;
+  uint32_t st;   // status bits so far
+  float mp, mq;  // row maxima (logits: the weights' m)
+  float u_draw;  // the draw's uniform (ACT_DRAW)
+};
+
 struct __align__(16) SmemTail {
   uint32_t recs[2][kMaxCluster][kRecWords];  // records pushed by the cluster's CTAs
   uint32_t myrec[kRecWords];                 // this CTA's outgoing record
-  float wf[kWarps][8];                       // per-warp partial results
+  float wf[kWarps][8];                       // per-warp partial results (greedy)
   int wi[kWarps][4];
+  float wf2[2][kWarps][8];  // per-warp partials of rows i, i + 1 (sampling)
+  int wi2[2][kWarps][4];
+  Dec dec[2];               // outcomes of rows i, i + 1
+  uint32_t lp[kLimbs], lq[kLimbs], infl;  // exact masses of the row (limbs) and +Inf flags
+  int xc;                   // exchanges done (slot and parity of the next one)
   unsigned long long wu[kWarps];
   double bd[8];  // broadcast of decision values from thread 0
   int bi[8];
@@ -104,6 +118,9 @@ struct __align__(16) SmemTail {
   volatile int go_row;         // consumers -> producer: rows decided so far
   volatile int producer_done;  // producer -> consumers: no copy in flight
   uint64_t redo_bar;           // completion of the draw pass's bulk copies
+  uint64_t pfull[2];           // consumers -> decision warp: partials of row i ready
+  uint64_t dfull[2];           // decision warp -> consumers: outcome of row i ready
+  uint64_t xfull, xdec;        // exact pass: limbs ready / final outcome ready
 };
 
 // ------------------------------------------------------------------ element types

@@ -305,6 +305,13 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     mbar_init(&sm.xbar[0], C);
     mbar_init(&sm.xbar[1], C);
     mbar_init(&sm.redo_bar, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&sm.pfull[q], kWarps);
+      mbar_init(&sm.dfull[q], 1);
+    }
+    mbar_init(&sm.xfull, 1);
+    mbar_init(&sm.xdec, 1);
+    sm.xc = 0;
     sm.stop = 0;
     sm.go_row = 0;
     sm.producer_done = 0;
@@ -391,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     return;
   }
 
-  // ================================================================ consumers
+  if (warp == kDecideWarp && !sampling) return;  // greedy rows are decided by consumer warp 0
+
+  // ================================================================ consumers (and the decision warp)
   // The last consumer warp fetches every row's decision inputs (draft token,
   // uniform, p(t), q(t)) now, while the first chunks are still in flight.
   if (warp == kWarps - 1 && lane < kMaxGather && lane <= kb) {
@@ -442,12 +451,16 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
   // Exchange of sm.myrec with every CTA of the cluster: a collective of
   // warp 0 (lane c pushes the record into CTA c, then every lane waits until
   // all C records have arrived here).
-  int xc = 0, last_slot = 0;
+  // (The count of exchanges lives in shared memory: the decision warp and
+  // consumer warp 0 take turns, handing over through mbarriers.)
+  int last_slot = 0;
   auto send_recv = [&](int words) -> bool {
     warp_converged();
-    const int slot = xc & 1;
-    const uint32_t par = static_cast<uint32_t>((xc >> 1) & 1);
-    ++xc;
+    const int x = sm.xc;
+    __syncwarp();
+    if (lane == 0) sm.xc = x + 1;
+    const int slot = x & 1;
+    const uint32_t par = static_cast<uint32_t>((x >> 1) & 1);
     last_slot = slot;
     if (lane < static_cast<int>(C)) {
       const uint32_t dst = dsmem_addr(&sm.recs[slot][rank][0], static_cast<uint32_t>(lane));
@@ -582,14 +595,10 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
     }
     nadd += (VEC == 8 ? 3 : 2);
 
-    // thread 0's state: status, exact limbs, the next row's draft token
-    uint32_t st = 0;
-    uint32_t lp[kLimbs], lq[kLimbs];
-
-    // Exact masses of row i (collective; reads the row slices from global
-    // memory).  Thread 0 receives the summed limbs and the +Inf flags.
-    auto exact_pass = [&](int i, bool with_q, const WarpT& wfp, const WarpT& wfq,
-                          uint32_t& infl) -> bool {
+    // ---- exact masses of row i (consumer collective; reads the row slices
+    // from global memory).  Thread 0 leaves the summed limbs and the +Inf
+    // flags in shared memory for the decision warp.
+    auto exact_pass = [&](int i, bool with_q, const WarpT& wfp, const WarpT& wfq) -> bool {
       for (int k = tid; k < 2 * kBuckets; k += kConsumers) buckets[k] = 0ull;
       bar_consumers<kConsumers>();
       uint32_t bp = 0, bq = 0;
@@ -619,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
         if (ok) {
           unsigned long long ap[kLimbs], aq[kLimbs];
           for (int k = 0; k < kLimbs; ++k) ap[k] = aq[k] = 0ull;
-          infl = 0;
+          uint32_t infl = 0;
           for (uint32_t c = 0; c < C; ++c) {
             for (int k = 0; k < kLimbs; ++k) {
               ap[k] += rec(c, k);
@@ -631,11 +640,12 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           for (int k = 0; k < kLimbs; ++k) {
             cp += ap[k];
             cq += aq[k];
-            lp[k] = static_cast<uint32_t>(cp);
-            lq[k] = static_cast<uint32_t>(cq);
+            sm.lp[k] = static_cast<uint32_t>(cp);
+            sm.lq[k] = static_cast<uint32_t>(cq);
             cp >>= 32;
             cq >>= 32;
           }
+          sm.infl = infl;
         }
         sm.bi[5] = ok ? 1 : 0;
       }
@@ -794,118 +804,34 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
       return 0;
     };
 
-    for (int i = 0;; ++i) {
-      const bool bonus = i == kb;
-
-      // decision inputs: rows below kMaxGather were fetched at the start; later
-      // rows are loaded now by thread 0 (their latency overlaps the pass)
-      int t = -1;
-      float u = 0.f, gp = 0.f, gq = 0.f;
-      if (tid == 0 && i >= kMaxGather) {
-        u = ld_issue_f32(P.uni + t0 + i);
-        if (!bonus) {
-          t = ld_issue_s32(P.tok + d0 + i);
-          if (t >= 0 && t < P.V) {
-            gp = TR::to_f(tgt[(t0 + i) * P.stride + t]);
-            gq = TR::to_f(drf[(d0 + i) * P.stride + t]);
-          }
-        }
-      }
-
-      // ---- the pass over this row's chunks as they stream in
-      Acc ap, aq;
-      Online op, oq;
-      ap.init();
-      aq.init();
-      op.init();
-      oq.init();
-      float ep = MODE == MODE_PROBS ? kInfF : -kInfF;  // probs: min; logits: max (validity)
-      float eq = ep;
-      for (int part = 0; part < (bonus ? 1 : 2); ++part) {
-        for (int j = 0; j < nck; ++j) {
-          const T* s = acquire();
-          const int n = j == nck - 1 ? last_n : ck_el;
-          if constexpr (MODE == MODE_PROBS)
-            chunk_mass_f32(reinterpret_cast<const float*>(s), n, part ? aq : ap, part ? eq : ep);
-          else
-            chunk_online<T>(s, n, khi, part ? oq : op, part ? eq : ep);
-          release();  // the slot takes the next row's chunks while this row is decided
-        }
-      }
-
-      // ---- warp partials -> shared memory
-      warp_converged();
-      const uint32_t tm = __reduce_or_sync(0xFFFFFFFFu, tmo);
-      if constexpr (MODE == MODE_PROBS) {
-        const float s0 = warp_sum_f(ap.f), s1 = warp_sum_f(aq.f);
-        const float m0 = warp_min_nan_f(ep), m1 = warp_min_nan_f(eq);
-        if (lane == 0) {
-          sm.wf[warp][0] = s0;
-          sm.wf[warp][1] = s1;
-          sm.wf[warp][2] = m0;
-          sm.wf[warp][3] = m1;
-          sm.wi[warp][0] = static_cast<int>(tm);
-        }
-      } else {
-        // rescale each lane's sums to the warp maximum (one more rescale step)
-        const float wmp = warp_max_f(op.m), wmq = warp_max_f(oq.m);
-        float sp = 0.f, wp = 0.f, sq = 0.f, wq = 0.f;
-        if (op.m > -kInfF) {
-          const float d = __fmul_rn(__fsub_rn(wmp, op.m), khi);
-          const float f = ex2_ftz(-d);
-          sp = __fmul_rn(op.s, f);
-          wp = __fmul_rn(__fmaf_rn(d, op.s, op.w), f);
-        }
-        if (oq.m > -kInfF) {
-          const float d = __fmul_rn(__fsub_rn(wmq, oq.m), khi);
-          const float f = ex2_ftz(-d);
-          sq = __fmul_rn(oq.s, f);
-          wq = __fmul_rn(__fmaf_rn(d, oq.s, oq.w), f);
-        }
-        sp = warp_sum_f(sp);
-        wp = warp_sum_f(wp);
-        sq = warp_sum_f(sq);
-        wq = warp_sum_f(wq);
-        const float vmp = warp_max_nan_f(ep), vmq = warp_max_nan_f(eq);
-        const int rr = warp_max_i(max(op.r, oq.r));
-        if (lane == 0) {
-          sm.wf[warp][0] = wmp;
-          sm.wf[warp][1] = sp;
-          sm.wf[warp][2] = wp;
-          sm.wf[warp][3] = wmq;
-          sm.wf[warp][4] = sq;
-          sm.wf[warp][5] = wq;
-          sm.wf[warp][6] = vmp;
-          sm.wf[warp][7] = vmq;
-          sm.wi[warp][0] = static_cast<int>(tm);
-          sm.wi[warp][1] = rr;
-        }
-      }
-      bar_consumers<kConsumers>();
-
-      // ---- thread 0: CTA record, exchange, combine (fp32 pairs), decide
-      if (tid == 0 && i < kMaxGather) {
-        u = sm.g_u[i];
-        t = bonus ? -1 : sm.g_t[i];
-        gp = sm.g_p[i];
-        gq = sm.g_q[i];
-      }
-      if (warp == 0) {
+    // ---- the pipelined row loop.  The consumer warps reduce row i + 1
+    // while the decision warp combines, exchanges and decides row i; a
+    // rejection of row i cuts the speculative pass short.
+    if (warp == kDecideWarp) {
+      // ================================================ decision warp
+      uint32_t st = 0;
+      int xr = 0;  // exact passes so far
+      for (int i = 0;; ++i) {
+        const bool bonus = i == kb;
+        const int pb = i & 1;
+        const bool okp = mbar_wait_bounded(&sm.pfull[pb], static_cast<uint32_t>((i >> 1) & 1));
         warp_converged();
         // lane w < 8 holds warp w's partials, lane c < C will hold CTA c's record
         const bool wl = lane < kWarps;
         const bool cl = lane < static_cast<int>(C);
-        int act = ACT_CONTINUE;
         DF Zp = {0.f, 0.f}, Zq = {0.f, 0.f};
         float Bp = 0.f, Bq = 0.f;
         float mp = 0.f, mq = 0.f, vp, vq;
-        uint32_t anytmo = 0;
+        uint32_t anytmo = okp ? 0u : 1u;
+        const float4 fa = *reinterpret_cast<const float4*>(&sm.wf2[pb][lane & 7][0]);
+        const float4 fb = *reinterpret_cast<const float4*>(&sm.wf2[pb][lane & 7][4]);
+        const int2 ia = *reinterpret_cast<const int2*>(&sm.wi2[pb][lane & 7][0]);
+        const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(ia.x) : 0u) | anytmo;
         if constexpr (MODE == MODE_PROBS) {
-          const DF s0 = warp_sum_df({wl ? sm.wf[lane][0] : 0.f, 0.f});
-          const DF s1 = warp_sum_df({wl ? sm.wf[lane][1] : 0.f, 0.f});
-          const float m0 = warp_min_nan_f(wl ? sm.wf[lane][2] : kInfF);
-          const float m1 = warp_min_nan_f(wl ? sm.wf[lane][3] : kInfF);
-          const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(sm.wi[lane][0]) : 0u);
+          const DF s0 = warp_sum_df({wl ? fa.x : 0.f, 0.f});
+          const DF s1 = warp_sum_df({wl ? fa.y : 0.f, 0.f});
+          const float m0 = warp_min_nan_f(wl ? fa.z : kInfF);
+          const float m1 = warp_min_nan_f(wl ? fa.w : kInfF);
           if (lane == 0) {
             putf(0, s0.hi);
             putf(1, s0.lo);
@@ -930,25 +856,24 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
           Bq = sum_bound(Zq.hi, nadd);
         } else {
           // warps -> CTA (one more rescale step)
-          const float wmp = wl ? sm.wf[lane][0] : -kInfF, wmq = wl ? sm.wf[lane][3] : -kInfF;
+          const float wmp = wl ? fa.x : -kInfF, wmq = wl ? fa.w : -kInfF;
           const float cmp = warp_max_f(wmp), cmq = warp_max_f(wmq);
-          const float c6 = warp_max_nan_f(wl ? sm.wf[lane][6] : -kInfF);
-          const float c7 = warp_max_nan_f(wl ? sm.wf[lane][7] : -kInfF);
-          const int rr = warp_max_i(wl ? sm.wi[lane][1] : 0);
-          const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(sm.wi[lane][0]) : 0u);
+          const float c6 = warp_max_nan_f(wl ? fb.z : -kInfF);
+          const float c7 = warp_max_nan_f(wl ? fb.w : -kInfF);
+          const int rr = warp_max_i(wl ? ia.y : 0);
           DF sp = {0.f, 0.f}, sq = {0.f, 0.f};
           float wp = 0.f, wq = 0.f;
           if (wmp > -kInfF) {
             const float d = __fmul_rn(__fsub_rn(cmp, wmp), khi);
             const float f = ex2_ftz(-d);
-            sp = two_prod(sm.wf[lane][1], f);
-            wp = __fmul_rn(__fmaf_rn(d, sm.wf[lane][1], sm.wf[lane][2]), f);
+            sp = two_prod(fa.y, f);
+            wp = __fmul_rn(__fmaf_rn(d, fa.y, fa.z), f);
           }
           if (wmq > -kInfF) {
             const float d = __fmul_rn(__fsub_rn(cmq, wmq), khi);
             const float f = ex2_ftz(-d);
-            sq = two_prod(sm.wf[lane][4], f);
-            wq = __fmul_rn(__fmaf_rn(d, sm.wf[lane][4], sm.wf[lane][5]), f);
+            sq = two_prod(fb.x, f);
+            wq = __fmul_rn(__fmaf_rn(d, fb.x, fb.y), f);
           }
           warp_converged();
           sp = warp_sum_df(sp);
@@ -1004,8 +929,48 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
             Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
           }
         }
-        // lane 0: input errors seen so far and the next action
+        // ---- lane 0: the decision (input errors in the oracle's order, then
+        // the accept test; the exact masses when the filter cannot decide)
+        int act = ACT_CONTINUE;
         if (lane == 0) {
+          int t = -1;
+          float u = 0.f, gp = 0.f, gq = 0.f;
+          if (i < kMaxGather) {
+            u = sm.g_u[i];
+            t = bonus ? -1 : sm.g_t[i];
+            gp = sm.g_p[i];
+            gq = sm.g_q[i];
+          } else {
+            u = P.uni[t0 + i];
+            if (!bonus) {
+              t = P.tok[d0 + i];
+              if (t >= 0 && t < P.V) {
+                gp = TR::to_f(tgt[(t0 + i) * P.stride + t]);
+                gq = TR::to_f(drf[(d0 + i) * P.stride + t]);
+              }
+            }
+          }
+          const WarpT wfp = make_warp(mp), wfq = make_warp(mq);
+          bool posted = false;  // dec[pb] handed over already (an exact pass followed)
+          bool have_exact = false;
+          double Zp_ex = 0.0, Zq_ex = 0.0;
+          // hands the exact pass to the consumers and waits for its limbs
+          auto run_exact = [&]() -> bool {
+            Dec& dd = sm.dec[pb];
+            dd.act = ACT_EXACT;
+            dd.mp = mp;
+            dd.mq = mq;
+            if (!posted) mbar_arrive_local(&sm.dfull[pb]);
+            posted = true;
+            const bool okx = mbar_wait_bounded(&sm.xfull, static_cast<uint32_t>(xr & 1)) && sm.bi[5] != 0;
+            ++xr;
+            if (okx) {
+              Zp_ex = limbs_to_double(sm.lp);
+              Zq_ex = bonus ? 0.0 : limbs_to_double(sm.lq);
+              have_exact = true;
+            }
+            return okx;
+          };
           uint32_t err = 0;
           bool p_bad = false, q_bad = false, need_x = false;
           if (anytmo) {
@@ -1022,144 +987,212 @@ __global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_con
               p_bad = !(vp < kInfF);  // NaN or +Inf logit
               q_bad = !bonus && !(vq < kInfF);
             }
-            if (need_x) act = ACT_EXACT;
+            if (need_x) {
+              if (run_exact()) {
+                p_bad = p_bad || (sm.infl & 1u);
+                q_bad = q_bad || (sm.infl & 2u);
+              } else {
+                act = ACT_ABORT;
+              }
+            }
           }
-          sm.bi[0] = act;
-          sm.bi[1] = static_cast<int>(err);
-          sm.bi[2] = (p_bad ? 1 : 0) | (q_bad ? 2 : 0);
-          sm.wf[0][0] = Zp.hi;
-          sm.wf[0][1] = Zp.lo;
-          sm.wf[0][2] = Zq.hi;
-          sm.wf[0][3] = Zq.lo;
-          sm.wf[0][4] = Bp;
-          sm.wf[0][5] = Bq;
-          sm.wf[0][6] = mp;
-          sm.wf[0][7] = mq;
-        }
-      }
-      bar_consumers<kConsumers>();
-      if (sm.bi[0] == ACT_ABORT) {
-        abort = true;
-        break;
-      }
-      const float mp = sm.wf[0][6], mq = sm.wf[0][7];
-      const WarpT wfp = make_warp(mp), wfq = make_warp(mq);
-      bool have_exact = false;
-      double Zp_ex = 0.0, Zq_ex = 0.0;  // thread 0: exact masses when known
-      if (sm.bi[0] == ACT_EXACT) {  // +Inf check / overflow: exact masses now
-        uint32_t infl = 0;
-        if (!exact_pass(i, !bonus, wfp, wfq, infl)) {
-          abort = true;
-          break;
-        }
-        if (tid == 0) {
-          sm.bi[2] |= (infl & 1u ? 1 : 0) | (infl & 2u ? 2 : 0);
-          Zp_ex = limbs_to_double(lp);
-          Zq_ex = bonus ? 0.0 : limbs_to_double(lq);
-        }
-        have_exact = true;
-      }
-      // ---- input errors in the oracle's order, then the accept test (thread 0)
-      if (tid == 0) {
-        const DF Zp = {sm.wf[0][0], sm.wf[0][1]}, Zq = {sm.wf[0][2], sm.wf[0][3]};
-        uint32_t err = static_cast<uint32_t>(sm.bi[1]);
-        const bool p_bad = sm.bi[2] & 1, q_bad = (sm.bi[2] >> 1) & 1;
-        if (!err && p_bad) err = ST_BAD_VALUE;
-        if (!err && q_bad) err = ST_BAD_VALUE;
-        if (!err && !(u >= 0.f && u < 1.f)) err = ST_BAD_VALUE;
-        const bool p_zero = MODE == MODE_PROBS ? (have_exact ? Zp_ex == 0.0 : Zp.hi == 0.f) : mp == -kInfF;
-        const bool q_zero = MODE == MODE_PROBS ? (have_exact ? Zq_ex == 0.0 : Zq.hi == 0.f) : mq == -kInfF;
-        int act;
-        if (err) {
-          if (rank == 0) finish(i, -1, st | err);
-          act = ACT_STOP;
-        } else if (p_zero) {
-          if (rank == 0) finish(i, -1, st | ST_ZERO_MASS);
-          act = ACT_STOP;
-        } else if (bonus) {
-          act = ACT_DRAW;  // all K_b drafts accepted: the bonus comes from p_K
-        } else if (q_zero) {
-          if (rank == 0) finish(i, -1, st | ST_ZERO_MASS);
-          act = ACT_STOP;
-        } else {
-          const float pt = wfp(gp), qt = wfq(gq);
-          sm.wf[1][0] = pt;
-          sm.wf[1][1] = qt;
-          if (have_exact) {
-            act = exact_accept(u, pt, qt, lp, lq) ? ACT_CONTINUE : ACT_DRAW;
-            st |= ST_EXACT;
-          } else {
-            const int dec = filter_decide(u, pt, qt, Zp, sm.wf[0][4], Zq, sm.wf[0][5]);
-            act = (force_exact || dec < 0) ? ACT_EXACT : (dec ? ACT_CONTINUE : ACT_DRAW);
+          if (act != ACT_ABORT) {
+            if (!err && p_bad) err = ST_BAD_VALUE;
+            if (!err && q_bad) err = ST_BAD_VALUE;
+            if (!err && !(u >= 0.f && u < 1.f)) err = ST_BAD_VALUE;
+            const bool p_zero = MODE == MODE_PROBS ? (have_exact ? Zp_ex == 0.0 : Zp.hi == 0.f) : mp == -kInfF;
+            const bool q_zero = MODE == MODE_PROBS ? (have_exact ? Zq_ex == 0.0 : Zq.hi == 0.f) : mq == -kInfF;
+            if (err) {
+              if (rank == 0) finish(i, -1, st | err);
+              act = ACT_STOP;
+            } else if (p_zero) {
+              if (rank == 0) finish(i, -1, st | ST_ZERO_MASS);
+              act = ACT_STOP;
+            } else if (bonus) {
+              act = ACT_DRAW;  // all K_b drafts accepted: the bonus comes from p_K
+            } else if (q_zero) {
+              if (rank == 0) finish(i, -1, st | ST_ZERO_MASS);
+              act = ACT_STOP;
+            } else {
+              const float pt = wfp(gp), qt = wfq(gq);
+              int dec = have_exact ? -1 : filter_decide(u, pt, qt, Zp, Bp, Zq, Bq);
+              if (!have_exact && (force_exact || dec < 0) && !run_exact()) {
+                act = ACT_ABORT;
+              } else {
+                if (have_exact) {
+                  dec = exact_accept(u, pt, qt, sm.lp, sm.lq) ? 1 : 0;
+                  st |= ST_EXACT;
+                }
+                act = dec ? ACT_CONTINUE : ACT_DRAW;
+              }
+            }
           }
-        }
-        if (act == ACT_CONTINUE) sm.go_row = i + 1;
-        if (act == ACT_STOP || act == ACT_DRAW) sm.stop = 1;
-        sm.bi[0] = act;
-      }
-      bar_consumers<kConsumers>();
-      int act = sm.bi[0];
-      if (act == ACT_EXACT) {
-        uint32_t infl = 0;
-        if (!exact_pass(i, true, wfp, wfq, infl)) {
-          abort = true;
-          break;
-        }
-        if (tid == 0) {
-          act = exact_accept(u, sm.wf[1][0], sm.wf[1][1], lp, lq) ? ACT_CONTINUE : ACT_DRAW;
-          st |= ST_EXACT;
-          Zp_ex = limbs_to_double(lp);
-          Zq_ex = limbs_to_double(lq);
-          have_exact = true;
+          // ---- the outcome for the consumers
+          Dec& dd = sm.dec[pb];
+          dd.mp = mp;
+          dd.mq = mq;
+          if (act == ACT_DRAW) {
+            const float ud = kb < kMaxGather ? sm.g_u[kb] : P.uni[t0 + kb];
+            const float zp = have_exact ? static_cast<float>(Zp_ex) : __fadd_rn(Zp.hi, Zp.lo);
+            const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : __fadd_rn(Zq.hi, Zq.lo));
+            if constexpr (MODE == MODE_LOGITS) {
+              const DF mk = two_prod(mp, khi), qk = two_prod(mq, khi);
+              sm.dpar[0] = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
+              sm.dpar[1] = bonus ? 0.f : -__fadd_rn(qk.hi, __fadd_rn(qk.lo, log2f(zq)));
+            } else {
+              const double zpd = have_exact ? Zp_ex : static_cast<double>(zp);
+              const double zqd = have_exact && !bonus ? Zq_ex : static_cast<double>(zq);
+              norm_factors(zpd, sm.dpar[0], sm.dpar[1]);
+              norm_factors(zqd, sm.dpar[2], sm.dpar[3]);
+            }
+            dd.u_draw = ud;
+          }
+          dd.st = st;
+          dd.act = act;
           if (act == ACT_CONTINUE) sm.go_row = i + 1;
-          if (act == ACT_DRAW) sm.stop = 1;
-          sm.bi[0] = act;
+          else sm.stop = 1;  // the producer issues nothing more
+          if (posted) {
+            mbar_arrive_local(&sm.xdec);  // after an exact pass the consumers wait here
+          } else {
+            mbar_arrive_local(&sm.dfull[pb]);
+          }
         }
-        bar_consumers<kConsumers>();
-        act = sm.bi[0];
+        act = __shfl_sync(0xFFFFFFFFu, act, 0);
+        xr = __shfl_sync(0xFFFFFFFFu, xr, 0);
+        if (act != ACT_CONTINUE) break;
       }
-      // warped weights of this row for the caller (testing aid)
-      if (MODE == MODE_LOGITS && (P.wt_out || P.wd_out) && act != ACT_STOP) {
-        const T* p = row_slice(false, i);
-        const T* q = row_slice(true, i);
-        for (int e = tid; e < n_el; e += kConsumers) {
-          if (P.wt_out) P.wt_out[(t0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfp(gload<T>(p, e));
-          if (P.wd_out && !bonus)
-            P.wd_out[(d0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfq(gload<T>(q, e));
+    } else {
+      // ================================================ consumer warps
+      // pass over row i's chunks as they stream in; its partials go to the
+      // decision warp.  With `watch` >= 0 the pass stops early once row
+      // `watch` is decided against continuing.  Returns false if it stopped.
+      auto pass_row = [&](int i, int watch) -> bool {
+        const bool bonus = i == kb;
+        Acc ap, aq;
+        Online op, oq;
+        ap.init();
+        aq.init();
+        op.init();
+        oq.init();
+        float ep = MODE == MODE_PROBS ? kInfF : -kInfF;  // probs: min; logits: max (validity)
+        float eq = ep;
+        for (int part = 0; part < (bonus ? 1 : 2); ++part) {
+          for (int j = 0; j < nck; ++j) {
+            if (watch >= 0) {
+              int stop = 0;
+              if (lane == 0 && mbar_test(&sm.dfull[watch & 1], static_cast<uint32_t>((watch >> 1) & 1))) {
+                const int a = sm.dec[watch & 1].act;
+                stop = (a == ACT_DRAW || a == ACT_STOP || a == ACT_ABORT) ? 1 : 0;
+              }
+              if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+            }
+            const T* s = acquire();
+            const int n = j == nck - 1 ? last_n : ck_el;
+            if constexpr (MODE == MODE_PROBS)
+              chunk_mass_f32(reinterpret_cast<const float*>(s), n, part ? aq : ap, part ? eq : ep);
+            else
+              chunk_online<T>(s, n, khi, part ? oq : op, part ? eq : ep);
+            release();  // the slot takes later chunks while rows are decided
+          }
         }
-      }
-      if (act == ACT_STOP) break;
-      if (act == ACT_CONTINUE) continue;
-      // ---- ACT_DRAW: the bonus from p_K, or the residual after the first rejection
-      if (tid == 0) {
-        sm.bi[3] = static_cast<int>(st);
-        const float ud = kb < kMaxGather ? sm.g_u[kb] : ld_issue_f32(P.uni + t0 + kb);
-        sm.wf[1][2] = ud;
-        // draw parameters (normalisations) in fp32, once
-        const float zp = have_exact ? static_cast<float>(Zp_ex) : __fadd_rn(sm.wf[0][0], sm.wf[0][1]);
-        const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : __fadd_rn(sm.wf[0][2], sm.wf[0][3]));
-        if constexpr (MODE == MODE_LOGITS) {
-          const DF mk = two_prod(mp, khi), qk = two_prod(mq, khi);
-          sm.dpar[0] = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
-          sm.dpar[1] = bonus ? 0.f : -__fadd_rn(qk.hi, __fadd_rn(qk.lo, log2f(zq)));
+        // ---- warp partials -> shared memory, then to the decision warp
+        const int pb = i & 1;
+        warp_converged();
+        const uint32_t tm = __reduce_or_sync(0xFFFFFFFFu, tmo);
+        if constexpr (MODE == MODE_PROBS) {
+          const float s0 = warp_sum_f(ap.f), s1 = warp_sum_f(aq.f);
+          const float m0 = warp_min_nan_f(ep), m1 = warp_min_nan_f(eq);
+          if (lane == 0) {
+            sm.wf2[pb][warp][0] = s0;
+            sm.wf2[pb][warp][1] = s1;
+            sm.wf2[pb][warp][2] = m0;
+            sm.wf2[pb][warp][3] = m1;
+            sm.wi2[pb][warp][0] = static_cast<int>(tm);
+          }
         } else {
-          const double zpd = have_exact ? Zp_ex : static_cast<double>(zp);
-          const double zqd = have_exact && !bonus ? Zq_ex : static_cast<double>(zq);
-          norm_factors(zpd, sm.dpar[0], sm.dpar[1]);
-          norm_factors(zqd, sm.dpar[2], sm.dpar[3]);
+          // rescale each lane's sums to the warp maximum (one more rescale step)
+          const float wmp = warp_max_f(op.m), wmq = warp_max_f(oq.m);
+          float sp = 0.f, wp = 0.f, sq = 0.f, wq = 0.f;
+          if (op.m > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(wmp, op.m), khi);
+            const float f = ex2_ftz(-d);
+            sp = __fmul_rn(op.s, f);
+            wp = __fmul_rn(__fmaf_rn(d, op.s, op.w), f);
+          }
+          if (oq.m > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(wmq, oq.m), khi);
+            const float f = ex2_ftz(-d);
+            sq = __fmul_rn(oq.s, f);
+            wq = __fmul_rn(__fmaf_rn(d, oq.s, oq.w), f);
+          }
+          sp = warp_sum_f(sp);
+          wp = warp_sum_f(wp);
+          sq = warp_sum_f(sq);
+          wq = warp_sum_f(wq);
+          const float vmp = warp_max_nan_f(ep), vmq = warp_max_nan_f(eq);
+          const int rr = warp_max_i(max(op.r, oq.r));
+          if (lane == 0) {
+            sm.wf2[pb][warp][0] = wmp;
+            sm.wf2[pb][warp][1] = sp;
+            sm.wf2[pb][warp][2] = wp;
+            sm.wf2[pb][warp][3] = wmq;
+            sm.wf2[pb][warp][4] = sq;
+            sm.wf2[pb][warp][5] = wq;
+            sm.wf2[pb][warp][6] = vmp;
+            sm.wf2[pb][warp][7] = vmq;
+            sm.wi2[pb][warp][0] = static_cast<int>(tm);
+            sm.wi2[pb][warp][1] = rr;
+          }
         }
-      }
-      bar_consumers<kConsumers>();
-      const uint32_t st_now = static_cast<uint32_t>(sm.bi[3]);
-      const float u_draw = sm.wf[1][2];
-      if (!bonus && !(u_draw >= 0.f && u_draw < 1.f)) {
-        if (tid == 0 && rank == 0) finish(i, -1, st_now | ST_BAD_VALUE);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(&sm.pfull[pb]);
+        return true;
+      };
+
+      int xr = 0;  // exact passes so far
+      pass_row(0, -1);
+      for (int i = 0;; ++i) {
+        const bool bonus = i == kb;
+        const int pb = i & 1;
+        if (!bonus) pass_row(i + 1, i);  // speculative: row i + 1 while row i is decided
+        int act = mbar_wait_bounded(&sm.dfull[pb], static_cast<uint32_t>((i >> 1) & 1)) ? sm.dec[pb].act
+                                                                                        : ACT_ABORT;
+        if (act == ACT_EXACT) {  // exact masses of row i, then the final outcome
+          const WarpT wfp = make_warp(sm.dec[pb].mp), wfq = make_warp(sm.dec[pb].mq);
+          exact_pass(i, !bonus, wfp, wfq);
+          if (tid == 0) mbar_arrive_local(&sm.xfull);
+          act = mbar_wait_bounded(&sm.xdec, static_cast<uint32_t>(xr & 1)) ? sm.dec[pb].act : ACT_ABORT;
+          ++xr;
+        }
+        if (act == ACT_ABORT) {
+          abort = true;
+          break;
+        }
+        // warped weights of this row for the caller (testing aid)
+        if (MODE == MODE_LOGITS && (P.wt_out || P.wd_out) && act != ACT_STOP) {
+          const WarpT wfp = make_warp(sm.dec[pb].mp), wfq = make_warp(sm.dec[pb].mq);
+          const T* p = row_slice(false, i);
+          const T* q = row_slice(true, i);
+          for (int e = tid; e < n_el; e += kConsumers) {
+            if (P.wt_out) P.wt_out[(t0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfp(gload<T>(p, e));
+            if (P.wd_out && !bonus)
+              P.wd_out[(d0 + i) * static_cast<long long>(P.V) + v_lo + e] = wfq(gload<T>(q, e));
+          }
+        }
+        if (act == ACT_CONTINUE) continue;
+        if (act == ACT_STOP) break;
+        // ---- ACT_DRAW: the bonus from p_K, or the residual after the first rejection
+        const uint32_t st_now = sm.dec[pb].st;
+        const float u_draw = sm.dec[pb].u_draw;
+        if (!bonus && !(u_draw >= 0.f && u_draw < 1.f)) {
+          if (tid == 0 && rank == 0) finish(i, -1, st_now | ST_BAD_VALUE);
+          break;
+        }
+        int code = draw(i, !bonus, bonus ? kb : i, st_now, u_draw);
+        if (code == 1) code = draw(i, false, i, st_now | ST_ZERO_MASS, u_draw);
+        if (code < 0) abort = true;
         break;
       }
-      int code = draw(i, !bonus, bonus ? kb : i, st_now, u_draw);
-      if (code == 1) code = draw(i, false, i, st_now | ST_ZERO_MASS, u_draw);
-      if (code < 0) abort = true;
-      break;
     }
   }
 
