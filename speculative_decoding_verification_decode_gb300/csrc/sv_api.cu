@@ -123,7 +123,7 @@ sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
   const unsigned gz = static_cast<unsigned>((prm.B + gy - 1) / gy);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.C), gy, gz);
-  cfg.blockDim = dim3(svk::kThreads, 1, 1);
+  cfg.blockDim = dim3(svk::threads_of(MODE), 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -49,6 +49,9 @@ constexpr int kMaxGather = 32;  // rows whose decision inputs are prefetched at 
 
 enum : int { MODE_GREEDY = 0, MODE_PROBS = 1, MODE_LOGITS = 2 };
 
+// Threads of a CTA: greedy verification has no decision warp.
+constexpr int threads_of(int mode) { return mode == MODE_GREEDY ? kThreads - 32 : kThreads; }
+
 #define kInfF (__uint_as_float(0x7F800000u))
 
 constexpr uint32_t ST_BAD_TOKEN = 1u, ST_BAD_VALUE = 2u, ST_ZERO_MASS = 4u, ST_NEAR = 8u,

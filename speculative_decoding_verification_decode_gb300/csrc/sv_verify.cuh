@@ -15,29 +15,18 @@ template <typename T>
 __device__ __forceinline__ void chunk_argmax(const T* s, int n, int e0, float& bv, int& bi,
                                              uint32_t& nanf) {
   constexpr int VEC = ElemTraits<T>::kVec;
-  constexpr int U = 4;  // vectors a thread tests at once
   const int nv = n / VEC;
-  for (int base = threadIdx.x; base < nv; base += U * kConsumers) {
-    float x[U][VEC];
-    float m = -kInfF;
+  for (int vi = threadIdx.x; vi < nv; vi += kConsumers) {
+    float x[VEC];
+    const float m = load_vec_max(s, vi, x);
+    if (!(m <= bv)) {  // a new maximum, a NaN, or no candidate yet
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = base + u * kConsumers;
-      if (vi < nv) m = fmax_nan(m, load_vec_max(s, vi, x[u]));
-    }
-    if (!(m <= bv)) {  // a new maximum, a NaN, or no candidate yet (rare)
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int vi = base + u * kConsumers;
-        if (vi >= nv) break;
-#pragma unroll
-        for (int k = 0; k < VEC; ++k) {
-          if (x[u][k] != x[u][k]) {
-            nanf = 1u;
-          } else if (bv != bv || x[u][k] > bv) {
-            bv = x[u][k];
-            bi = e0 + vi * VEC + k;
-          }
+      for (int k = 0; k < VEC; ++k) {
+        if (x[k] != x[k]) {
+          nanf = 1u;
+        } else if (bv != bv || x[k] > bv) {
+          bv = x[k];
+          bi = e0 + vi * VEC + k;
         }
       }
     }
@@ -233,7 +222,7 @@ __device__ __forceinline__ float seq_sum(const float* r) {
 enum : int { ACT_CONTINUE = 0, ACT_STOP = 1, ACT_EXACT = 2, ACT_DRAW = 3, ACT_ABORT = 4 };
 
 template <int MODE, typename T>
-__global__ void __launch_bounds__(kThreads, 2) sv_verify_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __grid_constant__ Params P) {
   using TR = ElemTraits<T>;
   constexpr int VEC = TR::kVec;
   constexpr int ELEM = static_cast<int>(sizeof(T));
