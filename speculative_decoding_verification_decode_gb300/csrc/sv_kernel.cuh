@@ -119,6 +119,7 @@ struct __align__(16) SmemTail {
   uint64_t empty[kMaxSlots];
   volatile int stop;           // consumers -> producer: issue nothing more
   volatile int go_row;         // consumers -> producer: rows decided so far
+  volatile int cut_row;        // consumers -> producer: the row they cut short (-1: none)
   volatile int producer_done;  // producer -> consumers: no copy in flight
   uint64_t redo_bar;           // completion of the draw pass's bulk copies
   uint64_t pfull[2];           // consumers -> decision warp: partials of row i ready

@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     mbar_init(&sm.xfull, 1);
     mbar_init(&sm.xdec, 1);
     sm.xc = 0;
+    sm.cut_row = -1;
     sm.stop = 0;
     sm.go_row = 0;
     sm.producer_done = 0;
@@ -326,27 +327,34 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         for (int j = 0; j < nck; ++j) {
           int go = 1;
           if (lane == 0) {
+            // Sampling: the consumers reduce every row up to one past the
+            // last accepted row (row i + 1 while row i is decided) unless they
+            // cut that row short together (sm.cut_row), so exactly those rows
+            // are issued; the stop flag is not consulted inside them.  Greedy:
+            // the consumers stop at once, so may the producer.
+            const bool may_stop = !sampling;
             if (round > 0) {
               uint32_t polls = 0;  // poll (not suspend): the stop flag must be seen at once
               while (!mbar_test(&sm.empty[slot], (round - 1) & 1u)) {
-                if (sm.stop || ++polls == kWaitPolls * 64u) {
+                if ((may_stop && sm.stop) || sm.cut_row == r || ++polls == kWaitPolls * 64u) {
                   go = 0;
                   break;
                 }
                 __nanosleep(64);
               }
             }
+            if (sm.cut_row == r) go = 0;
             // sampling: at most P.look rows past the last accepted one (the
-            // next row streams in while this one is decided; a rejection
-            // wastes what was fetched of it)
-            if (go && sampling) {
+            // next row streams in while this one is decided)
+            if (go && sampling && j == 0 && part == 0) {
               uint32_t polls = 0;
               while (r > sm.go_row + P.look && !sm.stop) {
                 __nanosleep(256);
                 if (++polls == kWaitPolls * 16u) break;
               }
+              if (r > sm.go_row + P.look) go = 0;  // stopped, or the wait gave up
             }
-            if (sm.stop) go = 0;
+            if (may_stop && sm.stop) go = 0;
           }
           go = __shfl_sync(0xFFFFFFFFu, go, 0);
           if (!go) {
@@ -795,7 +803,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
 
     // ---- the pipelined row loop.  The consumer warps reduce row i + 1
     // while the decision warp combines, exchanges and decides row i; a
-    // rejection of row i cuts the speculative pass short.
+    // rejection of row i cuts that pass short.
     if (warp == kDecideWarp) {
       // ================================================ decision warp
       uint32_t st = 0;
@@ -1053,8 +1061,11 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     } else {
       // ================================================ consumer warps
       // pass over row i's chunks as they stream in; its partials go to the
-      // decision warp.  With `watch` >= 0 the pass stops early once row
-      // `watch` is decided against continuing.  Returns false if it stopped.
+      // decision warp.  With watch >= 0 the consumers cut the pass short,
+      // all together (a barrier reduction at each chunk), once row `watch` is
+      // decided against continuing, and tell the producer (sm.cut_row); every
+      // warp consumes the same chunks, as the ring's slots are shared.
+      // Returns false if the pass was cut.
       auto pass_row = [&](int i, int watch) -> bool {
         const bool bonus = i == kb;
         Acc ap, aq;
@@ -1068,12 +1079,15 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         for (int part = 0; part < (bonus ? 1 : 2); ++part) {
           for (int j = 0; j < nck; ++j) {
             if (watch >= 0) {
-              int stop = 0;
-              if (lane == 0 && mbar_test(&sm.dfull[watch & 1], static_cast<uint32_t>((watch >> 1) & 1))) {
+              int cut = 0;
+              if (tid == 0 && mbar_test(&sm.dfull[watch & 1], static_cast<uint32_t>((watch >> 1) & 1))) {
                 const int a = sm.dec[watch & 1].act;
-                stop = (a == ACT_DRAW || a == ACT_STOP || a == ACT_ABORT) ? 1 : 0;
+                cut = (a == ACT_DRAW || a == ACT_STOP || a == ACT_ABORT) ? 1 : 0;
               }
-              if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+              if (bar_consumers_or<kConsumers>(cut)) {
+                if (tid == 0) sm.cut_row = i;
+                return false;
+              }
             }
             const T* s = acquire();
             const int n = j == nck - 1 ? last_n : ck_el;
