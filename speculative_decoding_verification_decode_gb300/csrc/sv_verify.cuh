@@ -327,26 +327,16 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         for (int j = 0; j < nck; ++j) {
           int go = 1;
           if (lane == 0) {
-            // Sampling: the consumers reduce every row up to one past the
+            // Sampling: the consumers reduce every row up to P.look past the
             // last accepted row (row i + 1 while row i is decided) unless they
-            // cut that row short together (sm.cut_row), so exactly those rows
-            // are issued; the stop flag is not consulted inside them.  Greedy:
-            // the consumers stop at once, so may the producer.
+            // cut a row short together (sm.cut_row: that row and every later
+            // one are never consumed), so exactly those rows are issued; the
+            // stop flag is not consulted inside them.  Greedy: the consumers
+            // stop at once, so may the producer.
             const bool may_stop = !sampling;
-            if (round > 0) {
-              uint32_t polls = 0;  // poll (not suspend): the stop flag must be seen at once
-              while (!mbar_test(&sm.empty[slot], (round - 1) & 1u)) {
-                if ((may_stop && sm.stop) || sm.cut_row == r || ++polls == kWaitPolls * 64u) {
-                  go = 0;
-                  break;
-                }
-                __nanosleep(64);
-              }
-            }
-            if (sm.cut_row == r) go = 0;
-            // sampling: at most P.look rows past the last accepted one (the
-            // next row streams in while this one is decided)
-            if (go && sampling && j == 0 && part == 0) {
+            // sampling: the row gate comes before the wait for a free slot, as
+            // that slot may hold a chunk of a cut row that is never released
+            if (sampling && j == 0 && part == 0) {
               uint32_t polls = 0;
               while (r > sm.go_row + P.look && !sm.stop) {
                 __nanosleep(256);
@@ -354,6 +344,19 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
               }
               if (r > sm.go_row + P.look) go = 0;  // stopped, or the wait gave up
             }
+            if (go && round > 0) {
+              uint32_t polls = 0;  // poll (not suspend): the flags must be seen at once
+              while (!mbar_test(&sm.empty[slot], (round - 1) & 1u)) {
+                const int cr = sm.cut_row;
+                if ((may_stop && sm.stop) || (cr >= 0 && r >= cr) || ++polls == kWaitPolls * 64u) {
+                  go = 0;
+                  break;
+                }
+                __nanosleep(64);
+              }
+            }
+            const int cr = sm.cut_row;
+            if (cr >= 0 && r >= cr) go = 0;
             if (may_stop && sm.stop) go = 0;
           }
           go = __shfl_sync(0xFFFFFFFFu, go, 0);
