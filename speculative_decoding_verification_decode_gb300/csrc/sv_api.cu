@@ -56,7 +56,7 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr int kSampleSlots = 6;  // ring depth cap in sampling mode
 
 // Layout of one CTA's dynamic shared memory for a given cluster size C and
-// ring depth S: [ring S x slot][per-vector draw sums][SmemTail].
+// ring depth S: [ring S x slot][draw group sums / exact buckets][SmemTail].
 void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
   const int vec = 16 / elem;
   long long slice = (V + C - 1) / C;
@@ -74,8 +74,9 @@ void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
     // most kSampleSlots chunks (the next row streams in as slots free up)
     p.S = 2 * p.nck + 1 < kSampleSlots ? 2 * p.nck + 1 : kSampleSlots;
     ring = static_cast<size_t>(p.S) * p.slot_bytes;
-    // one u64 per 16-byte vector of the slice, or the exact-sum buckets
-    vs = static_cast<size_t>((slice + vec - 1) / vec) * 8;
+    // one u64 per group of kGroupVecs 16-byte vectors, or the exact-sum buckets
+    const long long nvt = (slice + vec - 1) / vec;
+    vs = static_cast<size_t>((nvt + svk::kGroupVecs - 1) / svk::kGroupVecs) * 8;
     if (vs < 2 * svk::kBuckets * 8) vs = 2 * svk::kBuckets * 8;
   }
   p.vsum_off = static_cast<int>(round_up(ring, 128));
@@ -83,8 +84,14 @@ void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
   p.smem = p.tail_off + sizeof(svk::SmemTail);
 }
 
-// One cluster of C CTAs per sequence; the smallest C that gives the batch at
-// least two CTAs per SM while two CTAs still fit on an SM.
+// One cluster of C CTAs per sequence: the smallest C (two CTAs still fitting
+// on an SM) that gives the batch at least two CTAs per SM or, when sampling,
+// brings the slice down to kSampleSliceEl elements.  A sampling sequence is a
+// chain of dependent row passes, so slices past that length lengthen every
+// link; smaller ones add cluster exchanges and launch more CTAs than fit at
+// once (measured on GB300 at V = 32000 and V = 128256).
+constexpr long long kSampleSliceEl = 16384;
+
 bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
   const int vec = 16 / elem;
   const long long nvec = (V + vec - 1) / vec;
@@ -97,7 +104,9 @@ bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
     if (p.smem > kSmemPerSM || p.S > svk::kMaxSlots) continue;
     out = p;
     found = true;
-    if (p.smem <= kSmemTwoCtas && static_cast<long long>(B) * p.C >= want) break;
+    if (p.smem <= kSmemTwoCtas &&
+        (static_cast<long long>(B) * p.C >= want || (sampling && p.slice <= kSampleSliceEl)))
+      break;
   }
   return found;
 }

@@ -46,6 +46,7 @@ constexpr int kBuckets = 254;
 constexpr int kLimbs = 12;
 constexpr int kBigLimbs = 32;
 constexpr int kMaxGather = 32;  // rows whose decision inputs are prefetched at start
+constexpr int kGroupVecs = 32;  // 16-byte vectors per fixed-point group sum of the draw
 
 enum : int { MODE_GREEDY = 0, MODE_PROBS = 1, MODE_LOGITS = 2 };
 
@@ -84,7 +85,7 @@ struct Params {
   int S;           // ring slots
   int use_tma;
   int fixed_shift;
-  int vsum_off;  // byte offset of the per-vector draw sums (sampling)
+  int vsum_off;  // byte offset of the draw's group sums / exact buckets (sampling)
   int look;      // rows the producer may stream past the last accepted row
   int tail_off;  // byte offset of SmemTail
 };
@@ -108,7 +109,6 @@ struct __align__(16) SmemTail {
   uint32_t lp[kLimbs], lq[kLimbs], infl;  // exact masses of the row (limbs) and +Inf flags
   int xc;                   // exchanges done (slot and parity of the next one)
   unsigned long long wu[kWarps];
-  double bd[8];  // broadcast of decision values from thread 0
   int bi[8];
   float dpar[4];  // draw weight parameters (computed once by thread 0)
   // decision inputs of rows 0..kMaxGather-1, loaded at the start
@@ -120,8 +120,6 @@ struct __align__(16) SmemTail {
   volatile int stop;           // consumers -> producer: issue nothing more
   volatile int go_row;         // consumers -> producer: rows decided so far
   volatile int cut_row;        // consumers -> producer: the row they cut short (-1: none)
-  volatile int producer_done;  // producer -> consumers: no copy in flight
-  uint64_t redo_bar;           // completion of the draw pass's bulk copies
   uint64_t pfull[2];           // consumers -> decision warp: partials of row i ready
   uint64_t dfull[2];           // decision warp -> consumers: outcome of row i ready
   uint64_t xfull, xdec;        // exact pass: limbs ready / final outcome ready
@@ -159,49 +157,6 @@ __device__ __forceinline__ float h_lo(uint32_t w) {
 }
 __device__ __forceinline__ float h_hi(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
-}
-
-// Load vector `vi` (16 bytes) of a shared-memory chunk as floats.
-template <typename T>
-__device__ __forceinline__ void load_vec(const T* s, int vi, float* x) {
-  if constexpr (sizeof(T) == 4) {
-    const float4 v = reinterpret_cast<const float4*>(s)[vi];
-    x[0] = v.x;
-    x[1] = v.y;
-    x[2] = v.z;
-    x[3] = v.w;
-  } else {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        x[2 * k] = bf_lo(w[k]);
-        x[2 * k + 1] = bf_hi(w[k]);
-      } else {
-        x[2 * k] = h_lo(w[k]);
-        x[2 * k + 1] = h_hi(w[k]);
-      }
-    }
-  }
-}
-
-// NaN-propagating max of vector `vi` (packed for 16-bit types).
-template <typename T>
-__device__ __forceinline__ float vec_max_nan(const T* s, int vi) {
-  if constexpr (sizeof(T) == 4) {
-    const float4 v = reinterpret_cast<const float4*>(s)[vi];
-    return fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w));
-  } else {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-      const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
-      return fmax_nan(bf_lo(m), bf_hi(m));
-    } else {
-      const uint32_t m = f16x2_max_nan(f16x2_max_nan(v.x, v.y), f16x2_max_nan(v.z, v.w));
-      return fmax_nan(h_lo(m), h_hi(m));
-    }
-  }
 }
 
 // One 16-byte vector of a shared-memory chunk: unpacked floats and their

@@ -137,25 +137,7 @@ __device__ __forceinline__ void unpack_vec(const uint4 v, float* x) {
 // Vector vi (16 bytes) of a 16-byte aligned row slice in global memory.
 template <typename T>
 __device__ __forceinline__ void gload_vec(const T* p, int vi, float* x) {
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + vi);
-  if constexpr (sizeof(T) == 4) {
-    x[0] = __uint_as_float(v.x);
-    x[1] = __uint_as_float(v.y);
-    x[2] = __uint_as_float(v.z);
-    x[3] = __uint_as_float(v.w);
-  } else {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        x[2 * k] = bf_lo(w[k]);
-        x[2 * k + 1] = bf_hi(w[k]);
-      } else {
-        x[2 * k] = h_lo(w[k]);
-        x[2 * k + 1] = h_hi(w[k]);
-      }
-    }
-  }
+  unpack_vec<T>(__ldg(reinterpret_cast<const uint4*>(p) + vi), x);
 }
 
 // Draw weights of vector vi of a row slice pair in global memory (`q` may be
@@ -177,30 +159,6 @@ __device__ __forceinline__ int vec_draw_weights(const T* p, const T* q, int n, i
     for (int k = 0; k < VEC; ++k) {
       xp[k] = k < cnt ? gload<T>(p, e0 + k) : 0.f;
       xq[k] = (q && k < cnt) ? gload<T>(q, e0 + k) : 0.f;
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < VEC; ++k) r[k] = k < cnt ? dw(xp[k], q ? xq[k] : 0.f) : 0.f;
-  return cnt;
-}
-
-// Draw weights of vector vi of a row slice pair staged in shared memory.
-template <typename T, typename D>
-__device__ __forceinline__ int svec_draw_weights(const T* p, const T* q, int n, int vi, const D& dw,
-                                                 float* r) {
-  constexpr int VEC = ElemTraits<T>::kVec;
-  const int e0 = vi * VEC;
-  float xp[VEC], xq[VEC];
-  int cnt = VEC;
-  if (e0 + VEC <= n) {
-    load_vec(p, vi, xp);
-    if (q) load_vec(q, vi, xq);
-  } else {
-    cnt = n - e0;
-#pragma unroll
-    for (int k = 0; k < VEC; ++k) {
-      xp[k] = k < cnt ? ElemTraits<T>::to_f(p[e0 + k]) : 0.f;
-      xq[k] = (q && k < cnt) ? ElemTraits<T>::to_f(q[e0 + k]) : 0.f;
     }
   }
 #pragma unroll
@@ -293,7 +251,6 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     }
     mbar_init(&sm.xbar[0], C);
     mbar_init(&sm.xbar[1], C);
-    mbar_init(&sm.redo_bar, 1);
     for (int q = 0; q < 2; ++q) {
       mbar_init(&sm.pfull[q], kWarps);
       mbar_init(&sm.dfull[q], 1);
@@ -304,7 +261,6 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     sm.cut_row = -1;
     sm.stop = 0;
     sm.go_row = 0;
-    sm.producer_done = 0;
     fence_mbar_init_cluster();
   }
   __syncthreads();
@@ -392,8 +348,6 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         if (s < slot) mbar_wait_bounded(&sm.full[s], round & 1u);
         else if (round > 0) mbar_wait_bounded(&sm.full[s], (round - 1) & 1u);
       }
-      __threadfence_block();
-      sm.producer_done = 1;
     }
     return;
   }
@@ -676,22 +630,30 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
       const T* gq = resid ? row_slice(true, n_acc_row) : nullptr;
       const bool vec_ok = P.use_tma != 0;  // 16-byte aligned rows (slices start on vectors)
       const int nvt = (n_el + VEC - 1) / VEC;
+      const int ng = (nvt + kGroupVecs - 1) / kGroupVecs;
       unsigned long long mine = 0;
-      constexpr int U = 4;  // vectors whose loads are in flight together
+      // Each thread takes U consecutive vectors, so kGroupVecs / U neighbouring
+      // lanes cover one group of vectors, whose fixed-point sum goes to
+      // shared memory (the owner's walk re-reads only the crossing group).
+      constexpr int U = 4;
+      constexpr int LG = kGroupVecs / U;  // lanes per group
+      static_assert(LG == 8, "group sums reduce over 8 lanes");
       const int nfull = vec_ok ? n_el / VEC : 0;  // whole vectors read as 16-byte loads
-      for (int base = tid; base < nvt; base += U * kConsumers) {
+      for (int it = 0; it * kConsumers * U < nvt; ++it) {  // same trip count for every thread
+        const int v0 = (it * kConsumers + tid) * U;
         uint4 rp[U], rq[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int vi = base + u * kConsumers;
+          const int vi = v0 + u;
           if (vi < nfull) {
             rp[u] = __ldg(reinterpret_cast<const uint4*>(gp) + vi);
             rq[u] = gq ? __ldg(reinterpret_cast<const uint4*>(gq) + vi) : make_uint4(0u, 0u, 0u, 0u);
           }
         }
+        unsigned long long fs = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int vi = base + u * kConsumers;
+          const int vi = v0 + u;
           if (vi >= nvt) break;
           float r[VEC];
           if (vi < nfull) {
@@ -703,10 +665,14 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
           } else {
             vec_draw_weights<T>(gp, gq, n_el, vi, vec_ok, dw, r);
           }
-          const unsigned long long f = dw.fix(seq_sum<VEC>(r));
-          vsum[vi] = f;
-          mine += f;
+          fs += dw.fix(seq_sum<VEC>(r));
         }
+        mine += fs;
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 1);
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 2);
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 4);
+        const int g = v0 / kGroupVecs;
+        if ((lane & (LG - 1)) == 0 && g < ng) vsum[g] = fs;
       }
       warp_converged();
       mine = warp_sum_u64(mine);
@@ -757,42 +723,70 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
       bar_consumers<kConsumers>();
       const int code = sm.bi[0];
       if (code != 2) return code;
-      // ---- the owner: a scan of its per-vector sums, then one vector's elements
+      // ---- the owner: a scan of its group sums, then the crossing group's
+      // vectors (one warp), then one vector's elements
       const unsigned long long tloc = sm.wu[0];
       const double Rd = static_cast<double>(sm.wu[1]);
       bar_consumers<kConsumers>();  // sm.wu is reused by the scan
-      const int seg = (nvt + kConsumers - 1) / kConsumers;
-      const int lo = min(nvt, tid * seg), hi = min(nvt, lo + seg);
+      const int seg = (ng + kConsumers - 1) / kConsumers;
+      const int lo = min(ng, tid * seg), hi = min(ng, lo + seg);
       unsigned long long s = 0;
-      for (int v = lo; v < hi; ++v) s += vsum[v];
+      for (int g = lo; g < hi; ++g) s += vsum[g];
       unsigned long long tot;
       warp_converged();
       const unsigned long long ex = block_excl_scan_u64(s, sm.wu, tot);
-      if (tid == 0) sm.bi[1] = -1;
+      if (tid == 0) {
+        sm.bi[1] = -1;
+        sm.bi[3] = -1;
+      }
       bar_consumers<kConsumers>();
       if (tloc >= ex && tloc < ex + s) {
         unsigned long long c0 = ex;
-        int v = lo;
-        for (; v < hi - 1; ++v) {
-          if (tloc < c0 + vsum[v]) break;
-          c0 += vsum[v];
+        int g = lo;
+        for (; g < hi - 1; ++g) {
+          if (tloc < c0 + vsum[g]) break;
+          c0 += vsum[g];
         }
+        sm.bi[3] = g;
+        sm.wu[2] = c0;
+      }
+      bar_consumers<kConsumers>();
+      if (warp == 0 && sm.bi[3] >= 0) {
+        warp_converged();
+        const int g = sm.bi[3];
+        const unsigned long long c0 = sm.wu[2];
+        const int v = g * kGroupVecs + lane;
         float r[VEC];
-        const int cnt = vec_draw_weights<T>(gp, gq, n_el, v, vec_ok, dw, r);
-        float acc = r[0];
-        unsigned long long prev = c0;
+        int cnt = 0;
+        unsigned long long f = 0;
+        if (v < nvt) {
+          cnt = vec_draw_weights<T>(gp, gq, n_el, v, vec_ok, dw, r);
+          f = dw.fix(seq_sum<VEC>(r));
+        }
+        unsigned long long inc = f;
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) {
-          if (k > 0) acc = __fadd_rn(acc, r[k]);
-          const unsigned long long cur = c0 + dw.fix(acc);
-          if (k < cnt && (tloc < cur || k == cnt - 1)) {
-            const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
-            const unsigned long long dmin = dlo < dhi ? dlo : dhi;
-            sm.bi[1] = v_lo + v * VEC + k;
-            sm.bi[2] = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
-            break;
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+          if (lane >= o) inc += n;
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, v < nvt && tloc < c0 + inc);
+        if (hit && lane == __ffs(hit) - 1) {
+          const unsigned long long cv = c0 + inc - f;  // the CDF before this vector
+          float acc = r[0];
+          unsigned long long prev = cv;
+#pragma unroll
+          for (int k = 0; k < VEC; ++k) {
+            if (k > 0) acc = __fadd_rn(acc, r[k]);
+            const unsigned long long cur = cv + dw.fix(acc);
+            if (k < cnt && (tloc < cur || k == cnt - 1)) {
+              const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
+              const unsigned long long dmin = dlo < dhi ? dlo : dhi;
+              sm.bi[1] = v_lo + v * VEC + k;
+              sm.bi[2] = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
+              break;
+            }
+            prev = cur;
           }
-          prev = cur;
         }
       }
       bar_consumers<kConsumers>();
