@@ -53,7 +53,14 @@ constexpr size_t kSmemPerSM = 227 * 1024;  // usable shared memory per SM (bytes
 constexpr size_t kSmemTwoCtas = kSmemPerSM / 2 - 1024;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-constexpr int kSampleSlots = 6;  // ring depth cap in sampling mode
+// Ring slots hold 32 KB: a CTA's bulk copies complete roughly one after
+// another (about 0.3-0.4 us each whatever their size, measured on GB300), so
+// the per-CTA streaming rate grows with the copy size; 16 KB copies held a
+// CTA near 50 GB/s, 32 KB ones near 80 GB/s.
+constexpr int kSlotBytes = 32768;
+constexpr int kSampleSlots = 3;  // ring depth in sampling mode (two CTAs per SM)
+constexpr int kGreedySlots = 2;  // ring depth in greedy mode
+static_assert(kSlotBytes <= svk::kMaxSlotBytes, "ring slot larger than the kernel allows");
 
 // Layout of one CTA's dynamic shared memory for a given cluster size C and
 // ring depth S: [ring S x slot][draw group sums / exact buckets][SmemTail].
@@ -64,14 +71,13 @@ void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
   p.C = static_cast<int>((V + slice - 1) / slice);
   p.slice = static_cast<int>(slice);
   const long long slice_bytes = slice * elem;
-  p.slot_bytes = static_cast<int>(slice_bytes < 16384 ? round_up(slice_bytes, 16) : 16384);
+  p.slot_bytes = static_cast<int>(slice_bytes < kSlotBytes ? round_up(slice_bytes, 16) : kSlotBytes);
   p.nck = static_cast<int>((slice_bytes + p.slot_bytes - 1) / p.slot_bytes);
   p.S = ring_slots;
   size_t ring = static_cast<size_t>(p.S) * p.slot_bytes;
   size_t vs = 0;
   if (sampling) {
-    // room for the current row pair and the first chunk of the next row, at
-    // most kSampleSlots chunks (the next row streams in as slots free up)
+    // the next row streams in as the consumers free slots of the current one
     p.S = 2 * p.nck + 1 < kSampleSlots ? 2 * p.nck + 1 : kSampleSlots;
     ring = static_cast<size_t>(p.S) * p.slot_bytes;
     // one u64 per group of kGroupVecs 16-byte vectors, or the exact-sum buckets
@@ -100,7 +106,7 @@ bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
   for (int C = 1; C <= svk::kMaxCluster; C *= 2) {
     if (C > 1 && C > nvec) break;
     Plan p;
-    layout(sampling, V, elem, C, 4, p);
+    layout(sampling, V, elem, C, kGreedySlots, p);
     if (p.smem > kSmemPerSM || p.S > svk::kMaxSlots) continue;
     out = p;
     found = true;
