@@ -255,8 +255,8 @@ __device__ __forceinline__ DF warp_sum_df(DF v) {
 
 // Per-thread fp32 sum of vector sums.  A thread that adds n_v vector sums
 // (each a pairwise tree of VEC elements) is within (n_v + log2 VEC) * 2^-24 of
-// its exact sum; the block and cluster levels add 6 more roundings (a 5-level
-// warp tree in fp32, then fp32 pairs).  sum_bound() states the total bound.
+// its exact sum; the warp, CTA and cluster levels add 12 more roundings (fp32
+// trees of 5, 3 and 4 levels).  sum_bound() states the total bound.
 struct Acc {
   float f;
   __device__ __forceinline__ void init() { f = 0.f; }
@@ -264,7 +264,7 @@ struct Acc {
 };
 
 __device__ __forceinline__ float sum_bound(float Z, int nadd) {
-  return 2.02f * Z * (static_cast<float>(nadd + 8) * 0x1p-24f);
+  return 2.02f * Z * (static_cast<float>(nadd + 12) * 0x1p-24f);
 }
 
 // ------------------------------------------------------------------ logits -> weights
@@ -312,9 +312,10 @@ struct NoWarp {
 //   s = sum 2^(-nx),  w = sum 2^(-nx) * nx,   nx = (m - l) * k >= 0,
 // rescaled when m grows (all in fp32).  It approximates the row mass
 // Z = sum w_v of the defined weights within
-//   |S - Z| <= 2 * (S * ((R + 3)(e + u) + 2e + (n + 8) u) + W * 4 ln2 u)
+//   |S - Z| <= 2 * (S * ((R + 3)(e + u) + 2e + (n + 12) u) + W * 4 ln2 u)
 // with e the ex2 bound, u = 2^-24, R the rescale steps of any element and n
-// the fp32 additions of any element inside its thread.
+// the fp32 additions of any element inside its thread (the 12 are the
+// warp, CTA and cluster trees).
 struct Online {
   float m, s, w;
   int r;
@@ -389,9 +390,9 @@ struct Online {
 };
 
 __device__ __forceinline__ float online_bound(float S, float W, int R, int nadd) {
-  // (R + 3)(e + u) + 2e + (nadd + 8)u with e = 8u: an integer times u, exact
+  // (R + 3)(e + u) + 2e + (nadd + 12)u with e = 8u: an integer times u, exact
   // in fp32 (no fp64 on this path)
-  const float cs = static_cast<float>(9 * (R + 3) + 16 + nadd + 8) * 0x1p-24f;
+  const float cs = static_cast<float>(9 * (R + 3) + 16 + nadd + 12) * 0x1p-24f;
   constexpr float cw = 2.7725888f * 0x1p-24f;  // 4 ln2 u, rounded up
   return 2.02f * (S * cs + W * cw);
 }
@@ -416,36 +417,43 @@ __device__ __forceinline__ void log2e_over(float T, float& khi, float& klo) {
 }
 
 // ------------------------------------------------------------------ warp reductions
-// Per-warp results go to shared memory and thread 0 combines the eight warps
-// (one named barrier instead of a full block reduction).
+// Butterflies over groups of W lanes (W a power of two, at most 32): every
+// lane ends with the result of its own group.  The decision warp combines 8
+// warp partials (W = 8) and at most 16 CTA records (W = 16), so it takes 3 and
+// 4 levels where a whole-warp butterfly would take 5.
 
+template <int W = 32>
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = W / 2; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
+template <int W = 32>
 __device__ __forceinline__ float warp_max_nan_f(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = W / 2; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
+template <int W = 32>
 __device__ __forceinline__ float warp_min_nan_f(float v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmin_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = W / 2; o; o >>= 1) v = fmin_nan(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
+template <int W = 32>
 __device__ __forceinline__ float warp_max_f(float v) {  // inputs never NaN
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = W / 2; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 
+template <int W = 32>
 __device__ __forceinline__ int warp_max_i(int v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = W / 2; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 

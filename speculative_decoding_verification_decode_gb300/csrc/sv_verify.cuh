@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
             if (sampling && j == 0 && part == 0) {
               uint32_t polls = 0;
               while (r > sm.go_row + P.look && !sm.stop) {
-                __nanosleep(256);
-                if (++polls == kWaitPolls * 16u) break;
+                __nanosleep(32);  // the next row is issued within a fraction of a microsecond
+                if (++polls == kWaitPolls * 64u) break;
               }
               if (r > sm.go_row + P.look) go = 0;  // stopped, or the wait gave up
             }
@@ -304,11 +304,11 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
               uint32_t polls = 0;  // poll (not suspend): the flags must be seen at once
               while (!mbar_test(&sm.empty[slot], (round - 1) & 1u)) {
                 const int cr = sm.cut_row;
-                if ((may_stop && sm.stop) || (cr >= 0 && r >= cr) || ++polls == kWaitPolls * 64u) {
+                if ((may_stop && sm.stop) || (cr >= 0 && r >= cr) || ++polls == kWaitPolls * 128u) {
                   go = 0;
                   break;
                 }
-                __nanosleep(64);
+                __nanosleep(32);
               }
             }
             const int cr = sm.cut_row;
@@ -810,115 +810,107 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         const int pb = i & 1;
         const bool okp = mbar_wait_bounded(&sm.pfull[pb], static_cast<uint32_t>((i >> 1) & 1));
         warp_converged();
-        // lane w < 8 holds warp w's partials, lane c < C will hold CTA c's record
+        // lane w < 8 holds warp w's partials, lane c < C will hold CTA c's
+        // record; sums are fp32 trees over those lanes (3 and 4 levels).
+        // Record flags: bit 0 a wait gave up, bit 1 / 2 a bad target / draft
+        // value (probabilities: NaN or negative; logits: NaN or +Inf).
+        static_assert(kWarps == 8 && kMaxCluster <= 16, "combine widths");
         const bool wl = lane < kWarps;
         const bool cl = lane < static_cast<int>(C);
         DF Zp = {0.f, 0.f}, Zq = {0.f, 0.f};
         float Bp = 0.f, Bq = 0.f;
-        float mp = 0.f, mq = 0.f, vp, vq;
-        uint32_t anytmo = okp ? 0u : 1u;
+        float mp = 0.f, mq = 0.f;
+        uint32_t anytmo = okp ? 0u : 1u, badf = 0u;
         const float4 fa = *reinterpret_cast<const float4*>(&sm.wf2[pb][lane & 7][0]);
         const float4 fb = *reinterpret_cast<const float4*>(&sm.wf2[pb][lane & 7][4]);
         const int2 ia = *reinterpret_cast<const int2*>(&sm.wi2[pb][lane & 7][0]);
         const uint32_t tf = __reduce_or_sync(0xFFFFFFFFu, wl ? static_cast<uint32_t>(ia.x) : 0u) | anytmo;
         if constexpr (MODE == MODE_PROBS) {
-          const DF s0 = warp_sum_df({wl ? fa.x : 0.f, 0.f});
-          const DF s1 = warp_sum_df({wl ? fa.y : 0.f, 0.f});
-          const float m0 = warp_min_nan_f(wl ? fa.z : kInfF);
-          const float m1 = warp_min_nan_f(wl ? fa.w : kInfF);
+          const float s0 = warp_sum_f<8>(wl ? fa.x : 0.f);
+          const float s1 = warp_sum_f<8>(wl ? fa.y : 0.f);
+          const float m0 = warp_min_nan_f<8>(wl ? fa.z : kInfF);
+          const float m1 = warp_min_nan_f<8>(wl ? fa.w : kInfF);
           if (lane == 0) {
-            putf(0, s0.hi);
-            putf(1, s0.lo);
-            putf(2, s1.hi);
-            putf(3, s1.lo);
-            putf(4, m0);
-            putf(5, m1);
-            sm.myrec[6] = tf;
-            sm.myrec[7] = 0u;
+            putf(0, s0);
+            putf(1, s1);
+            sm.myrec[2] = (tf ? 1u : 0u) | (m0 >= 0.f ? 0u : 2u) | (m1 >= 0.f ? 0u : 4u);
+            sm.myrec[3] = 0u;
           }
-          if (!send_recv(8)) anytmo = 1;
-          vp = vq = kInfF;
+          if (!send_recv(4)) anytmo = 1;
           if (!anytmo) {
             warp_converged();
-            Zp = warp_sum_df({cl ? recf(lane, 0) : 0.f, cl ? recf(lane, 1) : 0.f});
-            Zq = warp_sum_df({cl ? recf(lane, 2) : 0.f, cl ? recf(lane, 3) : 0.f});
-            vp = warp_min_nan_f(cl ? recf(lane, 4) : kInfF);
-            vq = warp_min_nan_f(cl ? recf(lane, 5) : kInfF);
-            anytmo = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 6) : 0u);
+            Zp.hi = warp_sum_f<16>(cl ? recf(lane, 0) : 0.f);
+            Zq.hi = warp_sum_f<16>(cl ? recf(lane, 1) : 0.f);
+            const uint32_t f = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 2) : 0u);
+            anytmo = f & 1u;
+            badf = f;
           }
           Bp = sum_bound(Zp.hi, nadd);
           Bq = sum_bound(Zq.hi, nadd);
         } else {
           // warps -> CTA (one more rescale step)
           const float wmp = wl ? fa.x : -kInfF, wmq = wl ? fa.w : -kInfF;
-          const float cmp = warp_max_f(wmp), cmq = warp_max_f(wmq);
-          const float c6 = warp_max_nan_f(wl ? fb.z : -kInfF);
-          const float c7 = warp_max_nan_f(wl ? fb.w : -kInfF);
-          const int rr = warp_max_i(wl ? ia.y : 0);
-          DF sp = {0.f, 0.f}, sq = {0.f, 0.f};
-          float wp = 0.f, wq = 0.f;
+          const float cmp = warp_max_f<8>(wmp), cmq = warp_max_f<8>(wmq);
+          const float c6 = warp_max_nan_f<8>(wl ? fb.z : -kInfF);
+          const float c7 = warp_max_nan_f<8>(wl ? fb.w : -kInfF);
+          const int rr = warp_max_i<8>(wl ? ia.y : 0);
+          float sp = 0.f, sq = 0.f, wp = 0.f, wq = 0.f;
           if (wmp > -kInfF) {
             const float d = __fmul_rn(__fsub_rn(cmp, wmp), khi);
             const float f = ex2_ftz(-d);
-            sp = two_prod(fa.y, f);
+            sp = __fmul_rn(fa.y, f);
             wp = __fmul_rn(__fmaf_rn(d, fa.y, fa.z), f);
           }
           if (wmq > -kInfF) {
             const float d = __fmul_rn(__fsub_rn(cmq, wmq), khi);
             const float f = ex2_ftz(-d);
-            sq = two_prod(fb.x, f);
+            sq = __fmul_rn(fb.x, f);
             wq = __fmul_rn(__fmaf_rn(d, fb.x, fb.y), f);
           }
           warp_converged();
-          sp = warp_sum_df(sp);
-          sq = warp_sum_df(sq);
-          wp = warp_sum_f(wp);
-          wq = warp_sum_f(wq);
+          sp = warp_sum_f<8>(sp);
+          sq = warp_sum_f<8>(sq);
+          wp = warp_sum_f<8>(wp);
+          wq = warp_sum_f<8>(wq);
           if (lane == 0) {
             putf(0, cmp);
             putf(1, cmq);
-            putf(2, c6);
-            putf(3, c7);
-            putf(4, sp.hi);
-            putf(5, sp.lo);
-            putf(6, wp);
-            putf(7, sq.hi);
-            putf(8, sq.lo);
-            putf(9, wq);
-            sm.myrec[10] = static_cast<uint32_t>(rr);
-            sm.myrec[11] = tf;
+            putf(2, sp);
+            putf(3, wp);
+            putf(4, sq);
+            putf(5, wq);
+            sm.myrec[6] = static_cast<uint32_t>(rr);
+            sm.myrec[7] = (tf ? 1u : 0u) | (c6 < kInfF ? 0u : 2u) | (c7 < kInfF ? 0u : 4u);
           }
-          if (!send_recv(12)) anytmo = 1;
+          if (!send_recv(8)) anytmo = 1;
           mp = mq = -kInfF;
-          vp = vq = -kInfF;
           if (!anytmo) {
             warp_converged();
             const float rmp = cl ? recf(lane, 0) : -kInfF, rmq = cl ? recf(lane, 1) : -kInfF;
-            mp = warp_max_f(rmp);
-            mq = warp_max_f(rmq);
-            vp = warp_max_nan_f(cl ? recf(lane, 2) : -kInfF);
-            vq = warp_max_nan_f(cl ? recf(lane, 3) : -kInfF);
-            const int R = warp_max_i(cl ? static_cast<int>(rec(lane, 10)) : 0);
-            anytmo = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 11) : 0u);
+            mp = warp_max_f<16>(rmp);
+            mq = warp_max_f<16>(rmq);
+            const int R = warp_max_i<16>(cl ? static_cast<int>(rec(lane, 6)) : 0);
+            const uint32_t fl = __reduce_or_sync(0xFFFFFFFFu, cl ? rec(lane, 7) : 0u);
+            anytmo = fl & 1u;
+            badf = fl;
             // CTAs -> cluster (one more rescale step)
-            DF zp = {0.f, 0.f}, zq = {0.f, 0.f};
-            float w1 = 0.f, w2 = 0.f;
+            float zp = 0.f, zq = 0.f, w1 = 0.f, w2 = 0.f;
             if (rmp > -kInfF) {
               const float d = __fmul_rn(__fsub_rn(mp, rmp), khi);
               const float f = ex2_ftz(-d);
-              zp = df_mul_f({recf(lane, 4), recf(lane, 5)}, f);
-              w1 = __fmul_rn(__fmaf_rn(d, recf(lane, 4), recf(lane, 6)), f);
+              zp = __fmul_rn(recf(lane, 2), f);
+              w1 = __fmul_rn(__fmaf_rn(d, recf(lane, 2), recf(lane, 3)), f);
             }
             if (rmq > -kInfF) {
               const float d = __fmul_rn(__fsub_rn(mq, rmq), khi);
               const float f = ex2_ftz(-d);
-              zq = df_mul_f({recf(lane, 7), recf(lane, 8)}, f);
-              w2 = __fmul_rn(__fmaf_rn(d, recf(lane, 7), recf(lane, 9)), f);
+              zq = __fmul_rn(recf(lane, 4), f);
+              w2 = __fmul_rn(__fmaf_rn(d, recf(lane, 4), recf(lane, 5)), f);
             }
             warp_converged();
-            Zp = warp_sum_df(zp);
-            Zq = warp_sum_df(zq);
-            const float Wp = warp_sum_f(w1), Wq = warp_sum_f(w2);
+            Zp.hi = warp_sum_f<16>(zp);
+            Zq.hi = warp_sum_f<16>(zq);
+            const float Wp = warp_sum_f<16>(w1), Wq = warp_sum_f<16>(w2);
             Bp = online_bound(Zp.hi, Wp, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
             Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
           }
@@ -972,14 +964,14 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
           } else {
             if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
             if constexpr (MODE == MODE_PROBS) {
-              p_bad = !(vp >= 0.f);  // NaN or a negative value
-              q_bad = !bonus && !(vq >= 0.f);
+              p_bad = (badf & 2u) != 0u;  // NaN or a negative value
+              q_bad = !bonus && (badf & 4u) != 0u;
               // a non-finite approximate mass means a +Inf element or an fp32
               // overflow of the partial sums: the exact pass tells them apart
               need_x = !err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (!bonus && !(Zq.hi <= FLT_MAX)));
             } else {
-              p_bad = !(vp < kInfF);  // NaN or +Inf logit
-              q_bad = !bonus && !(vq < kInfF);
+              p_bad = (badf & 2u) != 0u;  // NaN or +Inf logit
+              q_bad = !bonus && (badf & 4u) != 0u;
             }
             if (need_x) {
               if (run_exact()) {
@@ -1027,8 +1019,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
           dd.mq = mq;
           if (act == ACT_DRAW) {
             const float ud = kb < kMaxGather ? sm.g_u[kb] : P.uni[t0 + kb];
-            const float zp = have_exact ? static_cast<float>(Zp_ex) : __fadd_rn(Zp.hi, Zp.lo);
-            const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : __fadd_rn(Zq.hi, Zq.lo));
+            const float zp = have_exact ? static_cast<float>(Zp_ex) : Zp.hi;
+            const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : Zq.hi);
             if constexpr (MODE == MODE_LOGITS) {
               const DF mk = two_prod(mp, khi), qk = two_prod(mq, khi);
               sm.dpar[0] = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
