@@ -193,6 +193,64 @@ __device__ __forceinline__ float load_vec_max(const T* s, int vi, float* x) {
   }
 }
 
+// U vectors of a shared-memory chunk, vectors base + u * kConsumers (those
+// at or past nv are absent and read as -Inf): unpacked floats, their
+// NaN-propagating maximum, and their minimum over the present vectors (a
+// lower bound for every present element), each from one packed tree.
+template <typename T, int U, int VEC>
+__device__ __forceinline__ void load_block(const T* s, int base, int nv, float (&x)[U][VEC], bool (&have)[U],
+                                           float& vmax, float& vmin) {
+  if constexpr (sizeof(T) == 4) {
+    float hi = -kInfF, lo = kInfF;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = base + u * kConsumers;
+      have[u] = vi < nv;
+      const float4 v = have[u] ? reinterpret_cast<const float4*>(s)[vi] : make_float4(-kInfF, -kInfF, -kInfF, -kInfF);
+      x[u][0] = v.x;
+      x[u][1] = v.y;
+      x[u][2] = v.z;
+      x[u][3] = v.w;
+      hi = fmax_nan(hi, fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w)));
+      if (have[u]) lo = fminf(lo, fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+    }
+    vmax = hi;
+    vmin = lo;
+  } else {
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kNegInf2 = kBf ? 0xFF80FF80u : 0xFC00FC00u;
+    constexpr uint32_t kPosInf2 = kBf ? 0x7F807F80u : 0x7C007C00u;
+    uint32_t w[U][4];
+    uint32_t hi2 = kNegInf2, lo2 = kPosInf2;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = base + u * kConsumers;
+      have[u] = vi < nv;
+      const uint4 v = have[u] ? reinterpret_cast<const uint4*>(s)[vi] : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+      w[u][0] = v.x;
+      w[u][1] = v.y;
+      w[u][2] = v.z;
+      w[u][3] = v.w;
+      if constexpr (kBf) {
+        hi2 = bf16x2_max_nan(hi2, bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w)));
+        if (have[u]) lo2 = bf16x2_min(lo2, bf16x2_min(bf16x2_min(v.x, v.y), bf16x2_min(v.z, v.w)));
+      } else {
+        hi2 = f16x2_max_nan(hi2, f16x2_max_nan(f16x2_max_nan(v.x, v.y), f16x2_max_nan(v.z, v.w)));
+        if (have[u]) lo2 = f16x2_min(lo2, f16x2_min(f16x2_min(v.x, v.y), f16x2_min(v.z, v.w)));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        x[u][2 * q] = kBf ? bf_lo(w[u][q]) : h_lo(w[u][q]);
+        x[u][2 * q + 1] = kBf ? bf_hi(w[u][q]) : h_hi(w[u][q]);
+      }
+    vmax = kBf ? fmax_nan(bf_lo(hi2), bf_hi(hi2)) : fmax_nan(h_lo(hi2), h_hi(hi2));
+    vmin = kBf ? fminf(bf_lo(lo2), bf_hi(lo2)) : fminf(h_lo(lo2), h_hi(lo2));
+  }
+}
+
 // Pairwise sum of N floats (depth log2 N).
 template <int N>
 __device__ __forceinline__ float tree_sum(const float* x) {
@@ -352,40 +410,39 @@ struct Online {
     s = __fadd_rn(s, tree_sum<VEC>(e));
     w = __fadd_rn(w, __fadd_rn(wa, wb));
   }
-  // U vectors at once (vectors u with have[u] false are absent): one max
-  // test and rescale for the block, then U * VEC independent exps.  Each
-  // element still goes through one vector tree and one addition into s.
+  // U vectors at once (vectors u with have[u] false are absent, their
+  // elements -Inf): one max test and rescale for the block, then U * VEC
+  // independent exps.  Each element still goes through one vector tree and
+  // one addition into s.  w takes an upper bound of the block's share: every
+  // element has nx <= (m - vmin) k, and ex2 flushes to 0 past nx = 126, so
+  // sum(e nx) <= sum(e) * min((m - vmin) k, 128).
   template <int U, int VEC>
   __device__ __forceinline__ void add_block(const float (&x)[U][VEC], const bool (&have)[U], float vm,
-                                            float k) {
+                                            float vmin, float k) {
     if (!(vm <= m)) {
       if (!(vm > -kInfF)) return;  // NaN (flagged by the caller) or all -Inf
       if (m == -kInfF) m = vm;
       else rescale_to(vm, k);
     }
     if (m == -kInfF) return;
-    float t[U], wv[U];
+    float t[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       float e[VEC];
-      float wa = 0.f, wb = 0.f;
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const float nx = fminf(__fmul_rn(__fsub_rn(m, x[u][j]), k), 3.0e38f);
-        e[j] = ex2_ftz(-nx);
-        if (j & 1) wb = __fmaf_rn(e[j], nx, wb);
-        else wa = __fmaf_rn(e[j], nx, wa);
-      }
+      for (int j = 0; j < VEC; ++j) e[j] = ex2_ftz(-__fmul_rn(__fsub_rn(m, x[u][j]), k));
       t[u] = tree_sum<VEC>(e);
-      wv[u] = __fadd_rn(wa, wb);
     }
+    float tb = 0.f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (have[u]) {
         s = __fadd_rn(s, t[u]);
-        w = __fadd_rn(w, wv[u]);
+        tb = __fadd_rn(tb, t[u]);
       }
     }
+    const float nxm = fminf(__fmul_rn(__fsub_rn(m, vmin), k), 128.f);
+    w = __fmaf_rn(tb, nxm, w);
   }
 };
 

@@ -53,8 +53,6 @@ __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
       : "memory");
 }
 
-// One poll of phase `parity`; acquire at cluster scope so that data written by
-// peer CTAs before their release-arrive is visible afterwards.
 // One wait on phase `parity` that may suspend the thread in hardware for up
 // to `kSuspendNs` (so waiting warps do not take issue slots); acquire at
 // cluster scope so that data written by peer CTAs before their release-arrive
@@ -166,6 +164,18 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t f16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_min(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 

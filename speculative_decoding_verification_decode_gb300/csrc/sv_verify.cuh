@@ -77,20 +77,10 @@ __device__ __forceinline__ void chunk_online(const T* s, int n, float k, Online&
   for (int base = threadIdx.x; base < nv; base += U * kConsumers) {
     float x[U][VEC];
     bool have[U];
-    float vm = -kInfF;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = base + u * kConsumers;
-      have[u] = vi < nv;
-      if (have[u]) {
-        vm = fmax_nan(vm, load_vec_max(s, vi, x[u]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) x[u][j] = -kInfF;
-      }
-    }
+    float vm, vmin;
+    load_block<T, U, VEC>(s, base, nv, x, have, vm, vmin);
     mx = fmax_nan(mx, vm);
-    o.add_block<U, VEC>(x, have, vm, k);
+    o.add_block<U, VEC>(x, have, vm, vmin, k);
   }
   for (int e = nv * VEC + threadIdx.x; e < n; e += kConsumers) {
     const float x = ElemTraits<T>::to_f(s[e]);
