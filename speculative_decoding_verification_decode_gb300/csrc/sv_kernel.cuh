@@ -370,7 +370,7 @@ struct NoWarp {
 //   s = sum 2^(-nx),  w = sum 2^(-nx) * nx,   nx = (m - l) * k >= 0,
 // rescaled when m grows (all in fp32).  It approximates the row mass
 // Z = sum w_v of the defined weights within
-//   |S - Z| <= 2 * (S * ((R + 3)(e + u) + 2e + (n + 12) u) + W * 4 ln2 u)
+//   |S - Z| <= 2 * (S * ((R + 3)(e + u) + 2e + (n + 12) u + ln2 |m k| u) + W * 5 ln2 u)
 // with e the ex2 bound, u = 2^-24, R the rescale steps of any element and n
 // the fp32 additions of any element inside its thread (the 12 are the
 // warp, CTA and cluster trees).
@@ -426,11 +426,12 @@ struct Online {
     }
     if (m == -kInfF) return;
     float t[U];
+    const float mk = __fmul_rn(m, k);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       float e[VEC];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) e[j] = ex2_ftz(-__fmul_rn(__fsub_rn(m, x[u][j]), k));
+      for (int j = 0; j < VEC; ++j) e[j] = ex2_ftz(__fmaf_rn(x[u][j], k, -mk));
       t[u] = tree_sum<VEC>(e);
     }
     float tb = 0.f;
@@ -446,11 +447,15 @@ struct Online {
   }
 };
 
-__device__ __forceinline__ float online_bound(float S, float W, int R, int nadd) {
+// The pass forms each exponent as x k - m k with one FMA (m k rounded once
+// per block), which moves every argument by at most (|m k| + nx) u / 2 from
+// (x - m) k: a relative weight error of ln2 (|m k| + nx) u / 2, which adds
+// ln2 |m k| u to the S coefficient and ln2 u to the W one.
+__device__ __forceinline__ float online_bound(float S, float W, int R, int nadd, float mk_abs) {
   // (R + 3)(e + u) + 2e + (nadd + 12)u with e = 8u: an integer times u, exact
   // in fp32 (no fp64 on this path)
-  const float cs = static_cast<float>(9 * (R + 3) + 16 + nadd + 12) * 0x1p-24f;
-  constexpr float cw = 2.7725888f * 0x1p-24f;  // 4 ln2 u, rounded up
+  const float cs = static_cast<float>(9 * (R + 3) + 16 + nadd + 12) * 0x1p-24f + 0.6932f * 0x1p-24f * mk_abs;
+  constexpr float cw = 3.4657360f * 0x1p-24f;  // 5 ln2 u, rounded up
   return 2.02f * (S * cs + W * cw);
 }
 

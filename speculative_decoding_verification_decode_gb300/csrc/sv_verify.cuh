@@ -901,8 +901,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
             Zp.hi = warp_sum_f<16>(zp);
             Zq.hi = warp_sum_f<16>(zq);
             const float Wp = warp_sum_f<16>(w1), Wq = warp_sum_f<16>(w2);
-            Bp = online_bound(Zp.hi, Wp, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
-            Bq = online_bound(Zq.hi, Wq, R + 1, nadd) + static_cast<float>(P.V) * 1.2e-38f;
+            Bp = online_bound(Zp.hi, Wp, R + 1, nadd, fabsf(__fmul_rn(mp, khi))) + static_cast<float>(P.V) * 1.2e-38f;
+            Bq = online_bound(Zq.hi, Wq, R + 1, nadd, fabsf(__fmul_rn(mq, khi))) + static_cast<float>(P.V) * 1.2e-38f;
           }
         }
         // ---- lane 0: the decision (input errors in the oracle's order, then
