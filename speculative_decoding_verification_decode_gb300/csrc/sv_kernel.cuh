@@ -545,30 +545,6 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-// Exclusive scan of one u64 per consumer thread (all consumers call it).
-__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
-                                                                  unsigned long long* red,
-                                                                  unsigned long long& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  unsigned long long inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) red[w] = inc;
-  bar_consumers<kConsumers>();
-  unsigned long long before = 0, tot = 0;
-#pragma unroll
-  for (int k = 0; k < kWarps; ++k) {
-    if (k < w) before += red[k];
-    tot += red[k];
-  }
-  bar_consumers<kConsumers>();
-  total = tot;
-  return before + inc - v;
-}
-
 // ------------------------------------------------------------------ exact arithmetic
 
 __device__ __forceinline__ void f32_parts(float x, uint32_t& M, int& s) {

@@ -713,39 +713,44 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
       bar_consumers<kConsumers>();
       const int code = sm.bi[0];
       if (code != 2) return code;
-      // ---- the owner: a scan of its group sums, then the crossing group's
-      // vectors (one warp), then one vector's elements
+      // ---- the owner, warp 0 alone: a scan of the group sums (lane l takes
+      // a run of consecutive groups), then the crossing group's vectors, then
+      // one vector's elements; the other warps are done.
+      if (warp != 0) return 0;
+      warp_converged();
       const unsigned long long tloc = sm.wu[0];
       const double Rd = static_cast<double>(sm.wu[1]);
-      bar_consumers<kConsumers>();  // sm.wu is reused by the scan
-      const int seg = (ng + kConsumers - 1) / kConsumers;
-      const int lo = min(ng, tid * seg), hi = min(ng, lo + seg);
+      const int seg = (ng + 31) / 32;
+      const int lo = min(ng, lane * seg), hi = min(ng, lo + seg);
       unsigned long long s = 0;
       for (int g = lo; g < hi; ++g) s += vsum[g];
-      unsigned long long tot;
-      warp_converged();
-      const unsigned long long ex = block_excl_scan_u64(s, sm.wu, tot);
-      if (tid == 0) {
-        sm.bi[1] = -1;
-        sm.bi[3] = -1;
+      unsigned long long inc = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += n;
       }
-      bar_consumers<kConsumers>();
-      if (tloc >= ex && tloc < ex + s) {
-        unsigned long long c0 = ex;
-        int g = lo;
-        for (; g < hi - 1; ++g) {
-          if (tloc < c0 + vsum[g]) break;
-          c0 += vsum[g];
+      const unsigned long long ex = inc - s;
+      const uint32_t seg_hit = __ballot_sync(0xFFFFFFFFu, tloc >= ex && tloc < inc);
+      int g_hit = -1;
+      unsigned long long c0 = 0;
+      if (seg_hit) {
+        const int L = __ffs(seg_hit) - 1;
+        if (lane == L) {
+          c0 = ex;
+          int g = lo;
+          for (; g < hi - 1; ++g) {
+            if (tloc < c0 + vsum[g]) break;
+            c0 += vsum[g];
+          }
+          g_hit = g;
         }
-        sm.bi[3] = g;
-        sm.wu[2] = c0;
+        g_hit = __shfl_sync(0xFFFFFFFFu, g_hit, L);
+        c0 = __shfl_sync(0xFFFFFFFFu, c0, L);
       }
-      bar_consumers<kConsumers>();
-      if (warp == 0 && sm.bi[3] >= 0) {
-        warp_converged();
-        const int g = sm.bi[3];
-        const unsigned long long c0 = sm.wu[2];
-        const int v = g * kGroupVecs + lane;
+      int found = -1, near_b = 0;
+      if (g_hit >= 0) {
+        const int v = g_hit * kGroupVecs + lane;
         float r[VEC];
         int cnt = 0;
         unsigned long long f = 0;
@@ -753,36 +758,39 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
           cnt = vec_draw_weights<T>(gp, gq, n_el, v, vec_ok, dw, r);
           f = dw.fix(seq_sum<VEC>(r));
         }
-        unsigned long long inc = f;
+        unsigned long long vinc = f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-          if (lane >= o) inc += n;
+          const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, vinc, o);
+          if (lane >= o) vinc += n;
         }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, v < nvt && tloc < c0 + inc);
-        if (hit && lane == __ffs(hit) - 1) {
-          const unsigned long long cv = c0 + inc - f;  // the CDF before this vector
-          float acc = r[0];
-          unsigned long long prev = cv;
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, v < nvt && tloc < c0 + vinc);
+        if (hit) {
+          const int L = __ffs(hit) - 1;
+          if (lane == L) {
+            const unsigned long long cv = c0 + vinc - f;  // the CDF before this vector
+            float acc = r[0];
+            unsigned long long prev = cv;
 #pragma unroll
-          for (int k = 0; k < VEC; ++k) {
-            if (k > 0) acc = __fadd_rn(acc, r[k]);
-            const unsigned long long cur = cv + dw.fix(acc);
-            if (k < cnt && (tloc < cur || k == cnt - 1)) {
-              const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
-              const unsigned long long dmin = dlo < dhi ? dlo : dhi;
-              sm.bi[1] = v_lo + v * VEC + k;
-              sm.bi[2] = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
-              break;
+            for (int k = 0; k < VEC; ++k) {
+              if (k > 0) acc = __fadd_rn(acc, r[k]);
+              const unsigned long long cur = cv + dw.fix(acc);
+              if (k < cnt && (tloc < cur || k == cnt - 1)) {
+                const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
+                const unsigned long long dmin = dlo < dhi ? dlo : dhi;
+                found = v_lo + v * VEC + k;
+                near_b = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
+                break;
+              }
+              prev = cur;
             }
-            prev = cur;
           }
+          found = __shfl_sync(0xFFFFFFFFu, found, L);
+          near_b = __shfl_sync(0xFFFFFFFFu, near_b, L);
         }
       }
-      bar_consumers<kConsumers>();
-      if (tid == 0) {
-        const int found = sm.bi[1];
-        const uint32_t near = (found >= 0 && sm.bi[2]) ? ST_NEAR : 0u;
+      if (lane == 0) {
+        const uint32_t near = (found >= 0 && near_b) ? ST_NEAR : 0u;
         finish(n_acc, found, found >= 0 ? (st_in | near) : (st_in | ST_TIMEOUT));
       }
       return 0;
