@@ -7,6 +7,9 @@ or links anything here, and this package imports nothing from it: the two
 share no code, constants or helpers.  Inputs come from ``workloads`` (data
 only) or from the tests themselves.
 
+``draft_gate`` is the draft-length gate that produces the ragged ``cu_k``
+(PocketLLM docs/dspark.md, the draft-length gate section).
+
 What it computes follows the spec-verify model card (sections "Method",
 "Correctness", "Requirements and limits") and the llmstudio.ru explainer
 "Как работает speculative decoding и MTP при инференсе LLM" (sections 13,
@@ -34,4 +37,14 @@ from .spec_verify import (  # noqa: F401
     accept_from_logits,
     softmax_fp64,
     warped_rows_f32,
+)
+from .draft_gate import (  # noqa: F401
+    GateParams,
+    bucket_of,
+    match_prob,
+    round_cost,
+    expected_tokens,
+    gate_length,
+    gate_batch,
+    update_table,
 )
