@@ -17,5 +17,14 @@ from ._lib import (  # noqa: F401
     SEQ_ZERO_MASS,
     load as load_library,
 )
-from .api import SVError, VerifyResult, accept, accept_from_logits, verify_greedy  # noqa: F401
+from .api import (  # noqa: F401
+    GateResult,
+    SVError,
+    VerifyResult,
+    accept,
+    accept_from_logits,
+    gate_draft_lengths,
+    gate_update,
+    verify_greedy,
+)
 from ._build import build  # noqa: F401

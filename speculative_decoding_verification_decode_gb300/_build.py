@@ -1,4 +1,4 @@
-"""Build libsv.so in-tree with nvcc for sm_103a (no cmake, one translation unit)."""
+"""Build libsv.so in-tree with nvcc for sm_103a (no cmake; the verify and gate translation units)."""
 
 import os
 import shutil
@@ -8,9 +8,9 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsv.so")
-SOURCES = [os.path.join(CSRC, "sv_api.cu")]
-HEADERS = [os.path.join(CSRC, f) for f in ("sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh")] + [
-    os.path.join(os.path.dirname(PKG_DIR), "include", "sv.h")]
+SOURCES = [os.path.join(CSRC, "sv_api.cu"), os.path.join(CSRC, "sv_gate.cu")]
+HEADERS = [os.path.join(CSRC, f) for f in ("sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh", "sv_host.h")] + [
+    os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -1,4 +1,4 @@
-"""ctypes declarations of the C ABI in include/sv.h (loads lib/libsv.so)."""
+"""ctypes declarations of the C ABI in include/sv.h and include/sv_gate.h (loads lib/libsv.so)."""
 
 import ctypes
 import os
@@ -6,7 +6,7 @@ import re
 
 from ._build import LIB_PATH, PKG_DIR
 
-HEADER = os.path.join(os.path.dirname(PKG_DIR), "include", "sv.h")
+HEADERS = [os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h")]
 
 SV_F32, SV_BF16, SV_F16 = 0, 1, 2
 SV_OK, SV_ERR_ARG, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -16,6 +16,16 @@ FLAG_FORCE_EXACT = 1
 
 _vp = ctypes.c_void_p
 _i32, _i64, _u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+_f64 = ctypes.c_double
+
+
+class GateParams(ctypes.Structure):
+    """sv_gate_params (include/sv_gate.h)."""
+    _fields_ = [("margin", ctypes.c_double), ("draft_ms", ctypes.c_double),
+                ("verify_base_ms", ctypes.c_double), ("verify_slope_ms", ctypes.c_double),
+                ("plain_ms", ctypes.c_double), ("margin_threshold", ctypes.c_float),
+                ("min_draft", ctypes.c_int32)]
+
 
 SIGNATURES = {
     "sv_verify_greedy": (_i32, [_vp, _i32, _i64, _vp, _vp, _i32, _i32, _i32, _i32,
@@ -24,6 +34,9 @@ SIGNATURES = {
                          _vp, _vp, _vp, _u32, _vp]),
     "sv_accept_from_logits": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
                                      _i32, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "sv_gate_draft_lengths": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                     ctypes.POINTER(GateParams), _vp, _vp, _vp]),
+    "sv_gate_update": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f64, _vp]),
     "sv_status_string": (ctypes.c_char_p, [_i32]),
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (_i32, []),
@@ -33,8 +46,8 @@ _lib = None
 
 
 def header_symbols():
-    """Function names declared in include/sv.h."""
-    text = open(HEADER).read()
+    """Function names declared in include/sv.h and include/sv_gate.h."""
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"\b(sv_[a-z_]+)\s*\(", text)))
 
 

@@ -9,6 +9,7 @@ results back, which is how an end-to-end caller with host buffers uses it.
 
 from __future__ import annotations
 
+import ctypes
 from typing import NamedTuple, Optional
 
 import torch
@@ -170,3 +171,67 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                                          _p(tok), _p(u), _p(cu), B, K, sum_k, tg.shape[1], _p(n),
                                          _p(nxt), _p(st), _p(wt), _p(wd), flags, m.stream()))
     return m.finish(VerifyResult(n, nxt, st))
+
+
+# ---------------------------------------------------------------- draft-length gate
+
+class GateResult(NamedTuple):
+    n_submit: torch.Tensor  # int32 [B]: drafts each sequence submits
+    cu_k: torch.Tensor  # int32 [B+1]: their exclusive prefix sum (the verify calls' cu_k)
+
+
+def gate_draft_lengths(confidence: torch.Tensor, edges: torch.Tensor, hits: torch.Tensor,
+                       total: torch.Tensor, k_drafted: Optional[torch.Tensor] = None,
+                       logit_margin: Optional[torch.Tensor] = None, margin: float = 1.15,
+                       draft_ms: float = 196.0, verify_base_ms: float = 300.0,
+                       verify_slope_ms: float = 109.0, plain_ms: float = 303.0,
+                       margin_threshold: float = 0.0, min_draft: int = 0) -> GateResult:
+    """Draft-length gate (include/sv_gate.h; PocketLLM dspark.md): ``confidence``
+    is ``[B, K]`` f32; ``edges`` ``[n_buckets - 1]`` f32; ``hits`` / ``total``
+    ``[n_buckets]`` f64 calibration counts.  Defaults are the page's."""
+    if confidence.dim() != 2:
+        raise ValueError("confidence must be [B, K]")
+    dev = confidence.device
+    if dev.type != "cuda":
+        raise ValueError("gate inputs must be CUDA tensors")
+    conf = confidence.to(torch.float32).contiguous()
+    B, K = conf.shape
+    e = edges.to(device=dev, dtype=torch.float32).contiguous()
+    h = hits.to(device=dev, dtype=torch.float64).contiguous()
+    t = total.to(device=dev, dtype=torch.float64).contiguous()
+    kd = None if k_drafted is None else k_drafted.to(device=dev, dtype=torch.int32).contiguous()
+    lm = None if logit_margin is None else logit_margin.to(device=dev, dtype=torch.float32).contiguous()
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    prm = _lib.GateParams(margin, draft_ms, verify_base_ms, verify_slope_ms, plain_ms,
+                          margin_threshold, min_draft)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        _check(lib.sv_gate_draft_lengths(_p(conf), _p(kd), _p(lm), _p(e), _p(h), _p(t), h.numel(), B, K,
+                                         ctypes.byref(prm), _p(n), _p(cu), stream))
+    return GateResult(n, cu)
+
+
+def gate_update(confidence: torch.Tensor, n_submitted: torch.Tensor, n_accepted: torch.Tensor,
+                edges: torch.Tensor, hits: torch.Tensor, total: torch.Tensor, decay: float = 0.9) -> None:
+    """One round of calibration, in place on ``hits`` / ``total`` (f64 CUDA
+    tensors, contiguous): positions before the accepted length are hits, the
+    first rejected position is a miss, later ones are not recorded."""
+    if confidence.dim() != 2:
+        raise ValueError("confidence must be [B, K]")
+    dev = confidence.device
+    for x in (hits, total):
+        if x.device != dev or x.dtype != torch.float64 or not x.is_contiguous():
+            raise ValueError("hits / total must be contiguous f64 tensors on the confidence's device")
+    conf = confidence.to(torch.float32).contiguous()
+    B, K = conf.shape
+    e = edges.to(device=dev, dtype=torch.float32).contiguous()
+    ns = n_submitted.to(device=dev, dtype=torch.int32).contiguous()
+    na = n_accepted.to(device=dev, dtype=torch.int32).contiguous()
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        _check(lib.sv_gate_update(_p(conf), _p(ns), _p(na), _p(e), _p(hits), _p(total), hits.numel(), B, K,
+                                  float(decay), stream))
+

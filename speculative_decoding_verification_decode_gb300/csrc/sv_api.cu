@@ -7,9 +7,10 @@
 #include <mutex>
 
 #include "../../include/sv.h"
+#include "sv_host.h"
 #include "sv_verify.cuh"
 
-namespace {
+namespace svh {
 
 thread_local char g_err[512] = "";
 
@@ -20,6 +21,15 @@ sv_status fail(sv_status s, const char* fmt, ...) {
   va_end(ap);
   return s;
 }
+
+void clear_error() { g_err[0] = '\0'; }
+
+}  // namespace svh
+
+namespace {
+
+using svh::fail;
+using svh::g_err;
 
 int sm_count() {
   static int cached[64] = {0};

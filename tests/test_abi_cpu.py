@@ -80,3 +80,54 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _lib.load()
+
+
+# ---------------------------------------------------------------- draft-length gate (host checks)
+
+def gate(lib, params=True, **kw):
+    prm = _lib.GateParams(1.15, 196.0, 300.0, 109.0, 303.0, 0.0, 0)
+    for k in ("margin", "plain_ms", "min_draft", "verify_slope_ms"):
+        if k in kw:
+            setattr(prm, k, kw.pop(k))
+    args = dict(conf=1 << 12, kd=NULL, lm=NULL, edges=1 << 12, hits=1 << 12, total=1 << 12, nb=6, B=4, K=5,
+                prm=ctypes.byref(prm) if params else NULL, n=1 << 12, cu=1 << 12, stream=NULL)
+    args.update(kw)
+    return lib.sv_gate_draft_lengths(*args.values())
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(B=-1), b"batch"),
+    (dict(K=65), b"k must"),
+    (dict(nb=0), b"n_buckets"),
+    (dict(nb=33), b"n_buckets"),
+    (dict(conf=NULL), b"confidence"),
+    (dict(edges=NULL), b"edges"),
+    (dict(hits=NULL), b"hits"),
+    (dict(cu=NULL), b"output"),
+    (dict(plain_ms=0.0), b"gate params"),
+    (dict(margin=-1.0), b"gate params"),
+    (dict(min_draft=-1), b"gate params"),
+    (dict(verify_slope_ms=float("nan")), b"gate params"),
+])
+def test_gate_argument_errors(lib, kw, frag):
+    assert gate(lib, **kw) == _lib.SV_ERR_ARG
+    assert frag in lib.sv_last_error()
+
+
+def test_gate_params_pointer_required(lib):
+    assert gate(lib, params=False) == _lib.SV_ERR_ARG
+    assert b"params" in lib.sv_last_error()
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(decay=1.5), b"decay"),
+    (dict(decay=float("nan")), b"decay"),
+    (dict(ns=NULL), b"length"),
+    (dict(K=-1), b"k must"),
+])
+def test_gate_update_argument_errors(lib, kw, frag):
+    args = dict(conf=1 << 12, ns=1 << 12, na=1 << 12, edges=1 << 12, hits=1 << 12, total=1 << 12, nb=6, B=4,
+                K=5, decay=0.9, stream=NULL)
+    args.update(kw)
+    assert lib.sv_gate_update(*args.values()) == _lib.SV_ERR_ARG
+    assert frag in lib.sv_last_error()
