@@ -391,6 +391,152 @@ def run_gpu(args):
     return result
 
 
+# ------------------------------------------------------------------ the draft-length gate
+
+GATE_TEXT = ("draft-length gate + calibration update, B=1024 sequences x 5 drafted positions, "
+             "6 confidence buckets seeded with the page's match table")
+# the page's calibration table (PocketLLM dspark.md): bucket edges and the
+# pooled match counts per confidence bucket
+GATE_EDGES = [-0.5, 0.5, 1.5, 3.0, 6.0]
+GATE_TOTAL = [5.0, 17.0, 19.0, 19.0, 14.0, 36.0]
+GATE_HITS = [1.0, 11.0, 15.0, 17.0, 14.0, 36.0]
+
+
+def gate_inputs(B=1024, K=5, seed=0x5eed0006):
+    """Seeded confidences and the accepted lengths their match law implies."""
+    rng = np.random.default_rng(seed)
+    conf = rng.normal(2.0, 3.0, size=(B, K)).astype(np.float32)
+    p = np.array(GATE_HITS) / np.array(GATE_TOTAL)
+    edges = np.array(GATE_EDGES, dtype=np.float32)
+    bucket = (conf[..., None] >= edges).sum(-1)
+    match = rng.random((B, K)) < p[bucket]
+    n_acc = np.where(match.all(1), K, match.argmin(1)).astype(np.int32)
+    return conf, edges, n_acc
+
+
+def run_gate(args):
+    """One step = the gate for a batch, then one calibration update (two
+    one-CTA launches); latency-bound, reported against HBM for the record."""
+    import torch
+
+    import oracle
+    import speculative_decoding_verification_decode_gb300 as sv
+    from speculative_decoding_verification_decode_gb300._build import build
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    build()
+    sv.load_library()
+    conf_h, edges_h, nacc_h = gate_inputs(seed=0x5eed0006 + 1000 * rank)
+    B, K = conf_h.shape
+    conf = torch.from_numpy(conf_h).to(dev)
+    edges = torch.from_numpy(edges_h).to(dev)
+    nacc = torch.from_numpy(nacc_h).to(dev)
+    hits = torch.tensor(GATE_HITS, dtype=torch.float64, device=dev)
+    total = torch.tensor(GATE_TOTAL, dtype=torch.float64, device=dev)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush():  # as for the verification workloads: L2 left holding clean lines
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    def step(c, e, na, h, t):
+        # the update clamps each accepted length to the submitted one
+        g = sv.gate_draft_lengths(c, e, h, t)
+        sv.gate_update(c, g.n_submit, na, e, h, t, decay=1.0)
+        return g
+
+    for _ in range(args.warmup):
+        flush()
+        step(conf, edges, nacc, hits, total)
+    torch.cuda.synchronize(dev)
+    # the step is two tiny launches: capture it in a CUDA graph so the timed
+    # region holds the GPU work, not the host's launch overhead
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(conf, edges, nacc, hits, total)
+        with torch.cuda.graph(graph, stream=side):
+            g = step(conf, edges, nacc, hits, total)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    ms = max_over_ranks(ms_local, dist, dev)
+    # end to end: confidences and lengths from pinned host memory, lengths back
+    conf_p, nacc_p = torch.from_numpy(conf_h).pin_memory(), torch.from_numpy(nacc_h).pin_memory()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        c = conf_p.to(dev, non_blocking=True)
+        na = nacc_p.to(dev, non_blocking=True)
+        out = step(c, edges, na, hits, total).cu_k.to("cpu", non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+    result = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_gbs()
+        nb = len(GATE_TOTAL)
+        moved = 2 * B * K * 4 + 4 * B * 4 + 4 * nb * 8 + (nb - 1) * 8  # conf twice, lengths, table
+        t0 = time.perf_counter()
+        prm = oracle.GateParams()
+        n_o, _ = oracle.gate_batch(conf_h, None, None, edges_h, np.array(GATE_HITS), np.array(GATE_TOTAL), prm)
+        oracle.update_table(conf_h, n_o, np.minimum(nacc_h, n_o), edges_h, np.array(GATE_HITS),
+                            np.array(GATE_TOTAL), 1.0)  # (the kernel clamps the same way)
+        cpu_dt = time.perf_counter() - t0
+        result = {
+            "metric": "gated sequences/s (draft-length gate and calibration update)",
+            "value": world * B / (ms * 1e-3),
+            "unit": "sequences/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f64",
+            "data": "synthetic (seeded; the page's calibration table)",
+            "config": {"workload": f"gate: {GATE_TEXT}", "B": B, "K": K, "launch": "CUDA graph per step",
+                       "l2": "flushed between timed steps (512 MB write, then a 512 MB read)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "gate_kernel + update_kernel (one CTA each)",
+                         "achieved": moved / (ms_local * 1e-3) / 1e9, "peak": peak,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst)", "unit": "GB/s",
+                         "frac": moved / (ms_local * 1e-3) / 1e9 / peak, "traffic": None,
+                         "note": "launch-latency bound: a few KB per step"},
+            "cpu_baseline": {"value": B / cpu_dt, "unit": "sequences/s", "cores": 1, "kind": "oracle",
+                             "sample": f"the whole batch of {B} sequences ({cpu_dt:.2f} s, single thread Python)"},
+            "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "sequences/s",
+                    "h2d_bytes_per_step": B * K * 4 + B * 4, "d2h_bytes_per_step": (B + 1) * 4,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,  # one graph of two kernels per step
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
 def run_reference(args):
     """The CPU oracle timed on the host cores (the reference arm of this repo)."""
     import workloads
@@ -438,7 +584,8 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT))
+    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT) + ["gate"],
+                    help="a verification workload, or 'gate' for the draft-length gate")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline field")
@@ -447,6 +594,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.config == "gate":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the gate's reference is the oracle; "
+                              "its time is the gate line's cpu_baseline"}), flush=True)
+            return None
+        return run_gate(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

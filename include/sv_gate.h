@@ -29,10 +29,12 @@
  *   confidence falls in bucket 0.  hits[k] / total[k] (f64) are bucket k's
  *   decayed counts; a bucket with total 0 has p = 1 (a cold gate keeps the
  *   full draft).
- * Arithmetic.  fp64 with one rounding per operation, in the order written
- *   above (p = hits / total; E by running product and sum; cost as
- *   (draft_ms + verify_base_ms) + verify_slope_ms * n; ratio E / cost; margin
- *   test margin * ratio(K_b)); ties go to the smaller n.
+ * Arithmetic.  The decision is taken in fp32 (it only picks an integer),
+ *   one rounding per operation, in the order written above: p = hits / total
+ *   as an fp64 quotient rounded to fp32; the parameters rounded to fp32 once;
+ *   E by running product and sum; cost as (draft_ms + verify_base_ms) +
+ *   verify_slope_ms * n; ratio E / cost; margin test against margin *
+ *   ratio(K_b); ties go to the smaller n.  The counts stay fp64.
  */
 #ifndef SV_GATE_H
 #define SV_GATE_H

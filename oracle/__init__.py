@@ -44,6 +44,7 @@ from .draft_gate import (  # noqa: F401
     match_prob,
     round_cost,
     expected_tokens,
+    ratios_f32,
     gate_length,
     gate_batch,
     update_table,

@@ -33,9 +33,11 @@ Readings where the page is silent (stated in the design doc as well):
 * ``min_draft`` floors the post-draft choice (capped at K_b); the pre-draft
   margin skip overrides it.
 
-Everything is computed in fp64 with one rounding per operation, in the order
-written here (the GPU kernels follow the same order, so results compare bit
-for bit).
+The decision (E, cost, their ratio, the margin test) is taken in fp32, the
+kernel's precision, since it only decides an integer; p = hits / total is an
+fp64 quotient rounded to fp32, and the calibration counts stay fp64.  Each
+operation rounds once, in the order written here (the GPU kernels follow the
+same order, so results compare bit for bit).
 """
 
 from dataclasses import dataclass
@@ -90,24 +92,36 @@ def expected_tokens(p, n):
     return e
 
 
-def gate_length(conf_row, k_b, logit_margin, edges, hits, total, prm):
-    """Number of drafts (0..k_b) one sequence submits."""
-    if prm.margin_threshold > 0.0 and logit_margin is not None and float(logit_margin) < float(prm.margin_threshold):
-        return 0
-    p = [match_prob(hits[bucket_of(c, edges)], total[bucket_of(c, edges)]) for c in conf_row[:k_b]]
-    n_lo = min(int(prm.min_draft), k_b)
-    best_n, best_r, full_r = -1, 0.0, 0.0
-    e, prod = 1.0, 1.0
+def ratios_f32(p, k_b, prm):
+    """E(n) / cost(n) for n = 0..k_b as the gate decides them: in fp32 (the
+    kernel's precision), one rounding per operation, E by running product
+    and sum, cost as (draft_ms + verify_base_ms) + verify_slope_ms * n."""
+    f = np.float32
+    fixed = f(f(prm.draft_ms) + f(prm.verify_base_ms))
+    e, prod = f(1.0), f(1.0)
+    out = []
     for n in range(0, k_b + 1):
         if n > 0:
-            prod = prod * p[n - 1]
-            e = e + prod
-        r = e / round_cost(n, prm)
-        if n >= n_lo and (best_n < 0 or r > best_r):
-            best_n, best_r = n, r
-        if n == k_b:
-            full_r = r
-    if best_n < k_b and best_r >= float(prm.margin) * full_r:
+            prod = f(prod * f(p[n - 1]))
+            e = f(e + prod)
+        cost = f(prm.plain_ms) if n == 0 else f(fixed + f(f(prm.verify_slope_ms) * f(n)))
+        out.append(f(e / cost))
+    return out
+
+
+def gate_length(conf_row, k_b, logit_margin, edges, hits, total, prm):
+    """Number of drafts (0..k_b) one sequence submits."""
+    if prm.margin_threshold > 0.0 and logit_margin is not None and \
+            np.float32(logit_margin) < np.float32(prm.margin_threshold):
+        return 0
+    p = [np.float32(match_prob(hits[bucket_of(c, edges)], total[bucket_of(c, edges)])) for c in conf_row[:k_b]]
+    r = ratios_f32(p, k_b, prm)
+    n_lo = min(int(prm.min_draft), k_b)
+    best_n = n_lo
+    for n in range(n_lo + 1, k_b + 1):
+        if r[n] > r[best_n]:
+            best_n = n
+    if best_n < k_b and r[best_n] >= np.float32(np.float32(prm.margin) * r[k_b]):
         return best_n
     return k_b
 
@@ -151,5 +165,5 @@ def update_table(conf, n_submitted, n_accepted, edges, hits, total, decay):
     return h2, t2
 
 
-__all__ = ["GateParams", "bucket_of", "match_prob", "round_cost", "expected_tokens", "gate_length",
-           "gate_batch", "update_table"]
+__all__ = ["GateParams", "bucket_of", "match_prob", "round_cost", "expected_tokens", "ratios_f32",
+           "gate_length", "gate_batch", "update_table"]

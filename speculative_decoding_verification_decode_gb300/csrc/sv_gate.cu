@@ -1,15 +1,18 @@
 // The draft-length gate (PocketLLM docs/dspark.md, the draft-length gate
 // section): per sequence, how many drafted tokens to submit to verification,
 // and the online calibration of P(match | confidence bucket).  The formulas
-// and the order of every fp64 operation are those of include/sv_gate.h.
+// and the order of every operation are those of include/sv_gate.h.
 //
 // Both kernels are one CTA: the work is a few dozen flops per drafted
-// position, so the launch and one pass over the small inputs are the cost.
-// The gate walks the batch in tiles of kThreads sequences, one thread per
-// sequence, and scans the tile's lengths into cu_k with a running carry; the
-// update tallies the round's observations with shared-memory integer
-// atomics (exact, so the result does not depend on their order) and then
-// decays and adds them per bucket.
+// position, so the launch and the latency of reading the small inputs are
+// the cost.  Each walks the batch in tiles of kThreads sequences: the CTA
+// first reads the tile's confidences with coalesced loads and keeps their
+// bucket ids in shared memory (one memory latency per tile, not one per
+// position), then one thread handles one sequence.  The gate scans the
+// tile's lengths into cu_k with a running carry; the update tallies the
+// round's observations with shared-memory integer atomics (exact, so the
+// result does not depend on their order) and then decays and adds them per
+// bucket.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -19,7 +22,7 @@
 
 namespace svg {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // sequences per tile; kThreads * K bucket ids in shared memory
 constexpr int kMaxBuckets = SV_GATE_MAX_BUCKETS;
 constexpr int kMaxK = SV_GATE_MAX_K;
 
@@ -32,7 +35,7 @@ struct GateArgs {
   const double* total;
   int32_t* n_out;
   int32_t* cu_out;
-  double margin, draft_ms, verify_base_ms, verify_slope_ms, plain_ms;
+  float margin, draft_ms, verify_base_ms, verify_slope_ms, plain_ms;  // rounded to fp32 once
   float margin_threshold;
   int min_draft;
   int nb, B, K;
@@ -59,46 +62,60 @@ __device__ __forceinline__ int bucket_of(float c, const float* edges, int nb) {
 
 __device__ __forceinline__ int clamp_i(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
-__device__ int gate_one(const GateArgs& a, int b, const float* edges, const double* p) {
-  const int kb = a.k_drafted ? clamp_i(a.k_drafted[b], 0, a.K) : a.K;
-  if (a.margin_threshold > 0.f && a.logit_margin && a.logit_margin[b] < a.margin_threshold) return 0;
+// The decision runs in fp32 (it only picks an integer; fp64 is a small
+// fraction of fp32's rate on this part), one rounding per operation.
+__device__ int gate_one(const GateArgs& a, int kb, float lm, const uint8_t* bk, const float* p) {
+  if (a.margin_threshold > 0.f && a.logit_margin && lm < a.margin_threshold) return 0;
   const int n_lo = a.min_draft < kb ? a.min_draft : kb;
-  const float* conf = a.conf + static_cast<long long>(b) * a.K;
-  const double fixed = __dadd_rn(a.draft_ms, a.verify_base_ms);
-  int best_n = -1;
-  double best_r = 0.0, full_r = 0.0, e = 1.0, prod = 1.0;
+  const float fixed = __fadd_rn(a.draft_ms, a.verify_base_ms);
+  int best_n = n_lo;
+  float best_r = 0.f, full_r = 0.f, e = 1.f, prod = 1.f;
   for (int n = 0; n <= kb; ++n) {
     if (n > 0) {
-      prod = __dmul_rn(prod, p[bucket_of(conf[n - 1], edges, a.nb)]);
-      e = __dadd_rn(e, prod);
+      prod = __fmul_rn(prod, p[bk[n - 1]]);
+      e = __fadd_rn(e, prod);
     }
-    const double cost = n == 0 ? a.plain_ms : __dadd_rn(fixed, __dmul_rn(a.verify_slope_ms, static_cast<double>(n)));
-    const double r = __ddiv_rn(e, cost);
-    if (n >= n_lo && (best_n < 0 || r > best_r)) {
-      best_n = n;
+    const float cost = n == 0 ? a.plain_ms : __fadd_rn(fixed, __fmul_rn(a.verify_slope_ms, static_cast<float>(n)));
+    const float r = __fdiv_rn(e, cost);
+    if (n == n_lo || (n > n_lo && r > best_r)) {
+      if (n > n_lo) best_n = n;
       best_r = r;
     }
     if (n == kb) full_r = r;
   }
-  if (best_n < kb && best_r >= __dmul_rn(a.margin, full_r)) return best_n;
+  if (best_n < kb && best_r >= __fmul_rn(a.margin, full_r)) return best_n;
   return kb;
 }
 
+// Bucket ids of the tile's confidences (positions 0..K-1 of sequences
+// base .. base + kThreads - 1), read with coalesced loads.
+__device__ __forceinline__ void tile_buckets(const float* conf, int base, int B, int K, const float* edges, int nb,
+                                             uint8_t* bk) {
+  const int n = (min(B, base + kThreads) - base) * K;
+  const float* src = conf + static_cast<long long>(base) * K;
+  for (int e = threadIdx.x; e < n; e += kThreads) bk[e] = static_cast<uint8_t>(bucket_of(src[e], edges, nb));
+}
+
 __global__ void __launch_bounds__(kThreads) gate_kernel(const GateArgs a) {
+  extern __shared__ uint8_t s_bk[];  // [kThreads * K] bucket ids of the tile
   __shared__ float s_edges[kMaxBuckets];
-  __shared__ double s_p[kMaxBuckets];
+  __shared__ float s_p[kMaxBuckets];
   __shared__ int s_warp[kThreads / 32];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   if (t < a.nb - 1) s_edges[t] = a.edges[t];
-  if (t < a.nb) {
+  if (t < a.nb) {  // p = hits / total as an fp64 quotient, rounded to fp32
     const double h = a.hits[t], tot = a.total[t];
-    s_p[t] = tot > 0.0 ? __ddiv_rn(h, tot) : 1.0;
+    s_p[t] = tot > 0.0 ? static_cast<float>(__ddiv_rn(h, tot)) : 1.f;
   }
   __syncthreads();
   int carry = 0;  // lengths of the sequences before this tile
   for (int base = 0; base < a.B; base += kThreads) {
     const int b = base + t;
-    const int n = b < a.B ? gate_one(a, b, s_edges, s_p) : 0;
+    const int kb = b < a.B ? (a.k_drafted ? clamp_i(a.k_drafted[b], 0, a.K) : a.K) : 0;
+    const float lm = (b < a.B && a.logit_margin) ? a.logit_margin[b] : 0.f;
+    tile_buckets(a.conf, base, a.B, a.K, s_edges, a.nb, s_bk);
+    __syncthreads();
+    const int n = b < a.B ? gate_one(a, kb, lm, s_bk + t * a.K, s_p) : 0;
     if (b < a.B) a.n_out[b] = n;
     // exclusive scan of n over the tile (warp scans, then the warp totals)
     int inc = n;
@@ -117,30 +134,33 @@ __global__ void __launch_bounds__(kThreads) gate_kernel(const GateArgs a) {
     }
     if (b < a.B) a.cu_out[b] = carry + before + inc - n;
     carry += tile;
-    __syncthreads();  // s_warp is rewritten by the next tile
+    __syncthreads();  // s_warp and s_bk are rewritten by the next tile
   }
   if (t == 0) a.cu_out[a.B] = carry;
 }
 
 __global__ void __launch_bounds__(kThreads) update_kernel(const UpdateArgs a) {
+  extern __shared__ uint8_t s_bk[];  // [kThreads * K] bucket ids of the tile
   __shared__ float s_edges[kMaxBuckets];
   __shared__ unsigned s_h[kMaxBuckets], s_t[kMaxBuckets];
   const int t = threadIdx.x;
   if (t < a.nb - 1) s_edges[t] = a.edges[t];
   if (t < kMaxBuckets) s_h[t] = s_t[t] = 0u;
   __syncthreads();
-  for (int b = t; b < a.B; b += kThreads) {
-    const int ks = clamp_i(a.n_sub[b], 0, a.K);
-    const int na = clamp_i(a.n_acc[b], 0, ks);
-    const float* conf = a.conf + static_cast<long long>(b) * a.K;
+  for (int base = 0; base < a.B; base += kThreads) {
+    const int b = base + t;
+    const int ks = b < a.B ? clamp_i(a.n_sub[b], 0, a.K) : 0;
+    const int na = b < a.B ? clamp_i(a.n_acc[b], 0, ks) : 0;
+    tile_buckets(a.conf, base, a.B, a.K, s_edges, a.nb, s_bk);
+    __syncthreads();
+    const uint8_t* bk = s_bk + t * a.K;
     for (int i = 0; i < na; ++i) {
-      const int k = bucket_of(conf[i], s_edges, a.nb);
-      atomicAdd(&s_h[k], 1u);
-      atomicAdd(&s_t[k], 1u);
+      atomicAdd(&s_h[bk[i]], 1u);
+      atomicAdd(&s_t[bk[i]], 1u);
     }
-    if (na < ks) atomicAdd(&s_t[bucket_of(conf[na], s_edges, a.nb)], 1u);
+    if (na < ks) atomicAdd(&s_t[bk[na]], 1u);
+    __syncthreads();  // s_bk is rewritten by the next tile
   }
-  __syncthreads();
   if (t < a.nb) {
     a.hits[t] = __dadd_rn(__dmul_rn(a.decay, a.hits[t]), static_cast<double>(s_h[t]));
     a.total[t] = __dadd_rn(__dmul_rn(a.decay, a.total[t]), static_cast<double>(s_t[t]));
@@ -190,17 +210,17 @@ extern "C" sv_status sv_gate_draft_lengths(const float* confidence, const int32_
   a.total = total;
   a.n_out = n_out;
   a.cu_out = cu_k_out;
-  a.margin = q.margin;
-  a.draft_ms = q.draft_ms;
-  a.verify_base_ms = q.verify_base_ms;
-  a.verify_slope_ms = q.verify_slope_ms;
-  a.plain_ms = q.plain_ms;
+  a.margin = static_cast<float>(q.margin);
+  a.draft_ms = static_cast<float>(q.draft_ms);
+  a.verify_base_ms = static_cast<float>(q.verify_base_ms);
+  a.verify_slope_ms = static_cast<float>(q.verify_slope_ms);
+  a.plain_ms = static_cast<float>(q.plain_ms);
   a.margin_threshold = q.margin_threshold;
   a.min_draft = q.min_draft;
   a.nb = n_buckets;
   a.B = B;
   a.K = K;
-  svg::gate_kernel<<<1, svg::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  svg::gate_kernel<<<1, svg::kThreads, static_cast<size_t>(svg::kThreads) * K, static_cast<cudaStream_t>(stream)>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return svh::fail(SV_ERR_CUDA, "gate kernel launch: %s", cudaGetErrorString(e));
   return SV_OK;
@@ -225,7 +245,7 @@ extern "C" sv_status sv_gate_update(const float* confidence, const int32_t* n_su
   a.nb = n_buckets;
   a.B = B;
   a.K = K;
-  svg::update_kernel<<<1, svg::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  svg::update_kernel<<<1, svg::kThreads, static_cast<size_t>(svg::kThreads) * K, static_cast<cudaStream_t>(stream)>>>(a);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return svh::fail(SV_ERR_CUDA, "gate update launch: %s", cudaGetErrorString(e));
   return SV_OK;

@@ -29,9 +29,14 @@ def test_cost_matches_the_page():
 
 @pytest.mark.parametrize("p", [0.0, 0.2, 0.5, 0.678, 0.9, 1.0])
 def test_expected_tokens_closed_form(p):
+    prm = GateParams()
+    r32 = oracle.ratios_f32([p] * 8, 8, prm)
     for n in range(0, 9):
         closed = float(n + 1) if p == 1.0 else 1.0 + p * (1.0 - p ** n) / (1.0 - p)
         assert oracle.expected_tokens([p] * n, n) == pytest.approx(closed, rel=1e-14, abs=1e-14)
+        # the gate's fp32 ratio of the same E(n) over cost(n)
+        cost = 303.0 if n == 0 else 196.0 + 300.0 + 109.0 * n
+        assert float(r32[n]) == pytest.approx(closed / cost, rel=3e-6)
 
 
 def _brute(p, k_b, prm, logit_margin=None):
@@ -63,12 +68,12 @@ def test_gate_matches_brute_force():
              for c in conf[:k_b]]
         got = oracle.gate_length(conf, k_b, None, EDGES, hits, total, prm)
         want = _brute(p, k_b, prm)
-        # the brute force's sums round differently; only exact near-ties may differ
+        # the gate decides in fp32: only near-ties (within its rounding) may differ
         if got != want:
             e = lambda n: 1.0 + sum(math.prod(p[:i + 1]) for i in range(n))
             c = lambda n: prm.plain_ms if n == 0 else prm.draft_ms + prm.verify_base_ms + prm.verify_slope_ms * n
-            assert abs(e(got) / c(got) - e(want) / c(want)) < 1e-12 or \
-                abs(e(got) / c(got) - prm.margin * e(k_b) / c(k_b)) < 1e-12
+            rg, rw, rf = e(got) / c(got), e(want) / c(want), prm.margin * e(k_b) / c(k_b)
+            assert abs(rg - rw) <= 1e-5 * rw or abs(rg - rf) <= 1e-5 * rf or abs(rw - rf) <= 1e-5 * rf
 
 
 def test_limits_the_page_states():
@@ -175,18 +180,25 @@ import textwrap  # noqa: E402
 
 import oracle.draft_gate as dg  # noqa: E402
 
+def _closed_form_pin():
+    test_expected_tokens_closed_form(0.678)
+
+
 GATE_MUTATIONS = [
     ("update_table", "if na < ks:\n            new_t[bucket_of(conf[b, na], edges)] += 1",
      "for i in range(na, ks):\n            new_t[bucket_of(conf[b, i], edges)] += 1",
      [test_update_records_only_uncensored_positions, test_online_estimate_is_unbiased_under_censoring]),
     ("update_table", "d * float(hits[k]) + float(new_h[k])", "float(hits[k]) + float(new_h[k])",
      [test_update_records_only_uncensored_positions]),
-    ("gate_length", "r > best_r", "r >= best_r", [test_ties_go_to_smaller_n]),
-    ("gate_length", "best_r >= float(prm.margin) * full_r", "best_r >= full_r",
+    ("gate_length", "if r[n] > r[best_n]:", "if r[n] >= r[best_n]:", [test_ties_go_to_smaller_n]),
+    ("gate_length", "r[best_n] >= np.float32(np.float32(prm.margin) * r[k_b])", "r[best_n] >= r[k_b]",
      [test_margin_between_one_and_its_factor]),
-    ("gate_length", "prod = prod * p[n - 1]", "prod = prod * p[0]", [test_gate_matches_brute_force]),
+    ("ratios_f32", "prod = f(prod * f(p[n - 1]))", "prod = f(prod * f(p[0]))",
+     [test_gate_matches_brute_force, _closed_form_pin]),
     ("round_cost", "float(prm.verify_slope_ms) * float(n)", "float(prm.verify_slope_ms) * float(n + 1)",
      [test_cost_matches_the_page]),
+    ("ratios_f32", "f(f(prm.verify_slope_ms) * f(n))", "f(f(prm.verify_slope_ms) * f(n + 1))",
+     [_closed_form_pin]),
     ("match_prob", "if t > 0.0 else 1.0", "if t > 0.0 else 0.0", [test_limits_the_page_states]),
     ("bucket_of", "if c >= float(e):", "if c > float(e):", [test_buckets_are_half_open_and_nan_is_lowest]),
     ("gate_length", "n_lo = min(int(prm.min_draft), k_b)", "n_lo = 0", [test_min_draft_and_pre_draft_skip]),
