@@ -537,6 +537,118 @@ def run_gate(args):
     return result
 
 
+# ------------------------------------------------------------------ the decoding loop
+
+DECODER_TEXT = ("speculative decoding rounds (draft 5, verify, commit) as one CUDA graph, B=64, "
+                "V=128256 bf16 logits from a synthetic table model, temperature 0.8")
+
+
+class _TableModel:
+    """Synthetic next-token logits: a table row picked by a hash of the last
+    two tokens (no trained weights exist here)."""
+
+    def __init__(self, torch, dev, V, H, seed, dtype):
+        g = torch.Generator().manual_seed(seed)
+        self.table = (torch.randn(H, V, generator=g) * 3.0).to(device=dev, dtype=dtype)
+        self.H, self.torch, self.dev = H, torch, dev
+
+    def next_logits(self, tokens, lengths):
+        torch = self.torch
+        rows = torch.arange(tokens.shape[0], device=self.dev)
+        t1 = tokens[rows, (lengths.long() - 1).clamp(min=0)].long()
+        t2 = tokens[rows, (lengths.long() - 2).clamp(min=0)].long()
+        return self.table[(t1 * 1000003 + t2 * 7919) % self.H]
+
+    def rows(self, tokens, lengths, k):
+        return self.torch.stack([self.next_logits(tokens, lengths + j) for j in range(k + 1)], dim=1)
+
+
+def run_decoder(args):
+    """One step = one speculative decoding round of the whole batch, replayed
+    from a CUDA graph; the metric counts committed tokens."""
+    import torch
+
+    import speculative_decoding_verification_decode_gb300 as sv
+    from speculative_decoding_verification_decode_gb300._build import build
+    from speculative_decoding_verification_decode_gb300.decoder import SpeculativeDecoder
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    build()
+    sv.load_library()
+    B, K, V, H = 64, 5, 128256, 509
+    rounds = args.warmup + args.steps
+    target = _TableModel(torch, dev, V, H, seed=31 + rank, dtype=torch.bfloat16)
+    draft = _TableModel(torch, dev, V, H, seed=31 + rank, dtype=torch.bfloat16)
+    draft.table = (draft.table.float() + torch.randn(draft.table.shape, device=dev) * 1.5).to(torch.bfloat16)
+    L = 3 + (rounds + 2) * (K + 1)
+    tok = torch.zeros(B, L, dtype=torch.int32, device=dev)
+    tok[:, :3] = torch.randint(0, V, (B, 3), device=dev, dtype=torch.int32)
+    lens = torch.full((B,), 3, dtype=torch.int32, device=dev)
+    T = torch.full((B,), 0.8, dtype=torch.float32, device=dev)
+    dec = SpeculativeDecoder(draft.next_logits, target.rows, tok, lens, K, V, temperature=T, seed=rank)
+    dec.capture()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        dec.graph.replay()
+    torch.cuda.synchronize(dev)
+    l0 = int(dec.lengths.sum())
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            dec.graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    committed = int(dec.lengths.sum()) - l0
+    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    ms = max_over_ranks(ms_local, dist, dev)
+    result = None
+    if rank == 0:
+        peak, peak_kind = measured_peak_gbs()
+        tok_per_round = committed / args.steps
+        # bytes of the round's verification inputs: target rows + draft rows, bf16
+        moved = B * ((K + 1) + K) * V * 2
+        result = {
+            "metric": "committed tokens/s (speculative decoding rounds, synthetic table model)",
+            "value": world * tok_per_round / (ms * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded table model; no trained weights)",
+            "config": {"workload": f"decoder: {DECODER_TEXT}", "B": B, "K": K, "V": V,
+                       "tokens_per_round": tok_per_round, "launch": "CUDA graph per round",
+                       "l2": "not flushed: each round's rows are freshly written by the model",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "whole round (model gathers, softmax draws, verify)",
+                         "achieved": moved / (ms_local * 1e-3) / 1e9, "peak": peak,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst)", "unit": "GB/s",
+                         "frac": moved / (ms_local * 1e-3) / 1e9 / peak, "traffic": None,
+                         "note": "bytes = the verification inputs a round produces; the table model's "
+                                 "own gathers and the drafter's softmax draws are extra"},
+            "cpu_baseline": None,
+            "e2e": None,
+            "gpu_launches": None,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
 def run_reference(args):
     """The CPU oracle timed on the host cores (the reference arm of this repo)."""
     import workloads
@@ -584,8 +696,9 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT) + ["gate"],
-                    help="a verification workload, or 'gate' for the draft-length gate")
+    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT) + ["gate", "decoder"],
+                    help="a verification workload, 'gate' for the draft-length gate, or 'decoder' "
+                         "for whole speculative decoding rounds")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline field")
@@ -594,6 +707,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.config == "decoder":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "no reference decoding loop: the "
+                              "oracle verifies single steps"}), flush=True)
+            return None
+        return run_decoder(args)
     if args.config == "gate":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the gate's reference is the oracle; "

@@ -28,3 +28,4 @@ from .api import (  # noqa: F401
     verify_greedy,
 )
 from ._build import build  # noqa: F401
+from .decoder import SpeculativeDecoder  # noqa: F401,E402
