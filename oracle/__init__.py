@@ -7,7 +7,9 @@ or links anything here, and this package imports nothing from it: the two
 share no code, constants or helpers.  Inputs come from ``workloads`` (data
 only) or from the tests themselves.
 
-``draft_gate`` is the draft-length gate that produces the ragged ``cu_k``
+``sampler_filter`` holds the top-k / top-p filters applied to p and q
+before verification (llmstudio.ru section 38).  ``draft_gate`` is the
+draft-length gate that produces the ragged ``cu_k``
 (PocketLLM docs/dspark.md, the draft-length gate section).
 
 What it computes follows the spec-verify model card (sections "Method",
@@ -24,6 +26,7 @@ from .spec_verify import (  # noqa: F401
     ZERO_MASS,
     NEAR_BOUNDARY,
     BAD_LAYOUT,
+    NEAR_FILTER,
     BOUNDARY_REL_TOL,
     Result,
     decode_rows,
@@ -37,6 +40,14 @@ from .spec_verify import (  # noqa: F401
     accept_from_logits,
     softmax_fp64,
     warped_rows_f32,
+)
+from .sampler_filter import (  # noqa: F401
+    FILTER_REL_TOL,
+    top_k_floor,
+    filter_floor,
+    floor_is_valid,
+    apply_floor,
+    floors_batch,
 )
 from .draft_gate import (  # noqa: F401
     GateParams,

@@ -56,6 +56,7 @@ BAD_VALUE = 2
 ZERO_MASS = 4
 NEAR_BOUNDARY = 8
 BAD_LAYOUT = 64
+NEAR_FILTER = 256  # oracle only: a top-p boundary within the filter tolerance
 
 BOUNDARY_REL_TOL = 1e-5
 
@@ -336,19 +337,35 @@ def warped_rows_f32(logits: np.ndarray, dtype: str, temperature: float) -> np.nd
 
 def accept_from_logits(target: np.ndarray, draft: np.ndarray, dtype: str,
                        temperature: np.ndarray, tokens: np.ndarray, u: np.ndarray,
-                       B: int, K: int, cu_k: Optional[np.ndarray] = None) -> Result:
+                       B: int, K: int, cu_k: Optional[np.ndarray] = None,
+                       top_k: Optional[np.ndarray] = None,
+                       top_p: Optional[np.ndarray] = None) -> Result:
     """Mixed greedy / sampled verification from logits with per-sequence T.
 
     ``T_b = 0`` runs greedy on the raw logits; ``T_b > 0`` warps target and
     draft rows identically to ``softmax(l / T_b)`` (fp64, rounded to f32) and
     runs speculative sampling on them (llmstudio.ru sections 13, 37, 38).
+    With ``top_k`` / ``top_p`` (per sequence), every sampled row is first cut
+    to the tokens the filters keep (``sampler_filter``; section 38: the
+    filters come after the temperature and apply to p and q alike).  An
+    invalid top-p is ``BAD_VALUE`` at row 0; a row whose top-p boundary is
+    within the filter tolerance sets the oracle-only ``NEAR_FILTER`` bit.
     """
+    from . import sampler_filter as sf
     V = target.shape[1]
     res = _new_result(B)
+    near_rows = [False]
 
-    def getter(rows, start, T):
+    def getter(rows, start, T, k=None, p=None):
         def get(i):
-            pr, err = softmax_fp64(decode_rows(rows[start + i], dtype), T)
+            x = decode_rows(rows[start + i], dtype)
+            if k is not None or p is not None:
+                floor, near, bad = sf.filter_floor(x, T, k, p)
+                if bad:
+                    return None, BAD_VALUE
+                near_rows[0] = near_rows[0] or near
+                x = sf.apply_floor(x, floor)
+            pr, err = softmax_fp64(x, T)
             if err == ZERO_MASS:
                 # all -Inf: a row of zero weights, reported by the mass check
                 return np.zeros(V, np.float32), 0
@@ -368,7 +385,12 @@ def accept_from_logits(target: np.ndarray, draft: np.ndarray, dtype: str,
             n, nxt, st = _greedy_sequence(lambda i: decode_rows(target[t0 + i], dtype),
                                           tokens[d0:d0 + k], k, V)
         else:
-            n, nxt, st = _accept_sequence(getter(target, t0, T), getter(draft, d0, T),
+            fk = None if top_k is None else int(top_k[b])
+            fp = None if top_p is None else float(np.float32(top_p[b]))
+            near_rows[0] = False
+            n, nxt, st = _accept_sequence(getter(target, t0, T, fk, fp), getter(draft, d0, T, fk, fp),
                                           tokens[d0:d0 + k], u[t0:t0 + k + 1], k, V)
+            if near_rows[0]:
+                st |= NEAR_FILTER
         res.n_accepted[b], res.next_token[b], res.status[b] = n, nxt, st
     return res
