@@ -25,6 +25,7 @@ from .api import (  # noqa: F401
     accept_from_logits,
     gate_draft_lengths,
     gate_update,
+    sampler_floors,
     verify_greedy,
 )
 from ._build import build  # noqa: F401

@@ -1,4 +1,4 @@
-"""Build libsv.so in-tree with nvcc for sm_103a (no cmake; the verify and gate translation units)."""
+"""Build libsv.so in-tree with nvcc for sm_103a (no cmake; the verify, gate and filter translation units)."""
 
 import os
 import shutil
@@ -8,9 +8,9 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsv.so")
-SOURCES = [os.path.join(CSRC, "sv_api.cu"), os.path.join(CSRC, "sv_gate.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("sv_api.cu", "sv_gate.cu", "sv_filter.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh", "sv_host.h")] + [
-    os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h")]
+    os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h", "sv_filter.h")]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -6,7 +6,7 @@ import re
 
 from ._build import LIB_PATH, PKG_DIR
 
-HEADERS = [os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h")]
+HEADERS = [os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h", "sv_filter.h")]
 
 SV_F32, SV_BF16, SV_F16 = 0, 1, 2
 SV_OK, SV_ERR_ARG, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -34,6 +34,11 @@ SIGNATURES = {
                          _vp, _vp, _vp, _u32, _vp]),
     "sv_accept_from_logits": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
                                      _i32, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "sv_sampler_floors": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                 _vp, _vp, _vp]),
+    "sv_accept_from_logits_floored": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
+                                             _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u32,
+                                             _vp]),
     "sv_gate_draft_lengths": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      ctypes.POINTER(GateParams), _vp, _vp, _vp]),
     "sv_gate_update": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f64, _vp]),
@@ -46,7 +51,7 @@ _lib = None
 
 
 def header_symbols():
-    """Function names declared in include/sv.h and include/sv_gate.h."""
+    """Function names declared in the headers under include/."""
     text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"\b(sv_[a-z_]+)\s*\(", text)))
 

@@ -145,13 +145,21 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                        temperature: torch.Tensor, draft_tokens: torch.Tensor,
                        uniforms: torch.Tensor, cu_k: Optional[torch.Tensor] = None,
                        k: Optional[int] = None, warped_out: Optional[tuple] = None,
-                       flags: int = 0) -> VerifyResult:
+                       flags: int = 0, top_k: Optional[torch.Tensor] = None,
+                       top_p: Optional[torch.Tensor] = None,
+                       floors: Optional[tuple] = None) -> VerifyResult:
     """Mixed greedy / sampled verification from logits with a fused
     per-sequence temperature softmax (``temperature[b] == 0`` is greedy).
 
     ``warped_out``: optional pair of f32 device tensors ``[target_rows, V]``
     and ``[draft_rows, V]`` that receive the warped weights of every row the
-    kernel reached (a testing aid)."""
+    kernel reached (a testing aid).
+
+    ``top_k`` (int32 ``[B]``) / ``top_p`` (f32 ``[B]``): the sampler filters of
+    include/sv_filter.h, applied alike to target and draft rows (two launches:
+    the floors, then the floored verification).  ``floors``: a pair of f32
+    device tensors ``[target_rows]``, ``[draft_rows]`` of precomputed floors
+    (used instead of top_k / top_p; either may be None)."""
     m = _Marshal(target_logits)
     tg = _rows(m.dev(target_logits))
     dr = _rows(m.dev(draft_logits, tg.dtype))
@@ -166,11 +174,64 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     wt, wd = (None, None) if warped_out is None else warped_out
     n, nxt, st = m.outputs(B)
     lib = _lib.load()
+    if floors is None and (top_k is not None or top_p is not None):
+        floors = _floors(lib, m, tg, dr, T, m.dev(top_k, torch.int32), m.dev(top_p, torch.float32),
+                         cu, B, K, sum_k)
     with torch.cuda.device(m.device):
-        _check(lib.sv_accept_from_logits(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T),
-                                         _p(tok), _p(u), _p(cu), B, K, sum_k, tg.shape[1], _p(n),
-                                         _p(nxt), _p(st), _p(wt), _p(wd), flags, m.stream()))
+        if floors is None:
+            _check(lib.sv_accept_from_logits(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T),
+                                             _p(tok), _p(u), _p(cu), B, K, sum_k, tg.shape[1], _p(n),
+                                             _p(nxt), _p(st), _p(wt), _p(wd), flags, m.stream()))
+        else:
+            ft, fd = (m.dev(f, torch.float32) for f in floors)
+            _check(lib.sv_accept_from_logits_floored(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0),
+                                                     _p(T), _p(tok), _p(u), _p(cu), B, K, sum_k,
+                                                     tg.shape[1], _p(ft), _p(fd), _p(n), _p(nxt),
+                                                     _p(st), _p(wt), _p(wd), flags, m.stream()))
     return m.finish(VerifyResult(n, nxt, st))
+
+
+def _floors(lib, m, tg, dr, T, tk, tp, cu, B, K, sum_k):
+    ft = torch.full((sum_k + B,), float("-inf"), dtype=torch.float32, device=m.device)
+    fd = torch.full((sum_k,), float("-inf"), dtype=torch.float32, device=m.device)
+    with torch.cuda.device(m.device):
+        _check(lib.sv_sampler_floors(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T), _p(tk),
+                                     _p(tp), _p(cu), B, K, sum_k, tg.shape[1], _p(ft), _p(fd),
+                                     m.stream()))
+    return ft, fd
+
+
+def sampler_floors(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                   temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
+                   top_p: Optional[torch.Tensor] = None, cu_k: Optional[torch.Tensor] = None,
+                   k: Optional[int] = None, sum_k: Optional[int] = None):
+    """Per-row floors of the top-k / top-p filters (include/sv_filter.h):
+    ``(floor_target [target_rows], floor_draft [draft_rows])`` f32; the rows a
+    filter keeps are those with logit >= floor (-inf keeps all, NaN marks an
+    invalid top-p).  Without ``cu_k`` the layout is B*(K+1) target rows and
+    B*K draft rows with ``k`` = K."""
+    m = _Marshal(target_logits)
+    tg = _rows(m.dev(target_logits))
+    dr = _rows(m.dev(draft_logits, tg.dtype))
+    if dr.stride(0) != tg.stride(0):
+        dr = dr.contiguous()
+        tg = tg.contiguous()
+    T = m.dev(temperature.reshape(-1), torch.float32)
+    cu = m.dev(cu_k, torch.int32)
+    if cu is None:
+        B = int(T.numel())
+        K = (tg.shape[0] - B) // B if B else 0
+        sk = B * K
+    else:
+        B = int(cu.numel()) - 1
+        if k is None or sum_k is None:
+            raise ValueError("k and sum_k are required with cu_k")
+        K, sk = int(k), int(sum_k)
+    ft, fd = _floors(_lib.load(), m, tg, dr, T, m.dev(top_k, torch.int32), m.dev(top_p, torch.float32),
+                     cu, B, K, sk)
+    if m.host:
+        return ft.cpu(), fd.cpu()
+    return ft, fd
 
 
 # ---------------------------------------------------------------- draft-length gate

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "../../include/sv.h"
+#include "../../include/sv_filter.h"
 #include "sv_host.h"
 #include "sv_verify.cuh"
 
@@ -129,7 +130,10 @@ bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
 
 template <int MODE, typename T>
 sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
-  auto kern = svk::sv_verify_kernel<MODE, T>;
+  auto kern = svk::sv_verify_kernel<MODE, T, false>;
+  if constexpr (MODE == svk::MODE_LOGITS) {
+    if (prm.flo_t || prm.flo_d) kern = svk::sv_verify_kernel<MODE, T, true>;
+  }
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(smem): %s", cudaGetErrorString(e));
@@ -264,13 +268,15 @@ sv_status sv_accept(const float* target_probs, const float* draft_probs, int64_t
   return launch<svk::MODE_PROBS, float>(p, pl, static_cast<cudaStream_t>(stream));
 }
 
-sv_status sv_accept_from_logits(const void* target_logits, const void* draft_logits,
-                                sv_dtype dtype, int64_t row_stride, const float* temperature,
-                                const int32_t* draft_tokens, const float* uniforms,
-                                const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
-                                int32_t vocab, int32_t* n_accepted, int32_t* next_token,
-                                uint32_t* status, float* warped_target_out,
-                                float* warped_draft_out, uint32_t flags, void* stream) {
+namespace {
+
+sv_status accept_logits(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                        int64_t row_stride, const float* temperature, const int32_t* draft_tokens,
+                        const float* uniforms, const int32_t* cu_k, int32_t batch, int32_t k,
+                        int32_t sum_k, int32_t vocab, const float* floor_target,
+                        const float* floor_draft, int32_t* n_accepted, int32_t* next_token,
+                        uint32_t* status, float* warped_target_out, float* warped_draft_out,
+                        uint32_t flags, void* stream) {
   sv_status s = check_common(target_logits, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
                              n_accepted, next_token, status, flags);
   if (s != SV_OK || batch == 0) return s;
@@ -288,6 +294,8 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
                               flags);
   p.wt_out = warped_target_out;
   p.wd_out = warped_draft_out;
+  p.flo_t = floor_target;
+  p.flo_d = floor_draft;
   p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
               (row_stride * elem) % 16 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -296,6 +304,34 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
     case SV_BF16: return launch<svk::MODE_LOGITS, __nv_bfloat16>(p, pl, st);
     default: return launch<svk::MODE_LOGITS, __half>(p, pl, st);
   }
+}
+
+}  // namespace
+
+sv_status sv_accept_from_logits(const void* target_logits, const void* draft_logits,
+                                sv_dtype dtype, int64_t row_stride, const float* temperature,
+                                const int32_t* draft_tokens, const float* uniforms,
+                                const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
+                                int32_t vocab, int32_t* n_accepted, int32_t* next_token,
+                                uint32_t* status, float* warped_target_out,
+                                float* warped_draft_out, uint32_t flags, void* stream) {
+  return accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
+                       uniforms, cu_k, batch, k, sum_k, vocab, nullptr, nullptr, n_accepted,
+                       next_token, status, warped_target_out, warped_draft_out, flags, stream);
+}
+
+sv_status sv_accept_from_logits_floored(const void* target_logits, const void* draft_logits,
+                                        sv_dtype dtype, int64_t row_stride, const float* temperature,
+                                        const int32_t* draft_tokens, const float* uniforms,
+                                        const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
+                                        int32_t vocab, const float* floor_target,
+                                        const float* floor_draft, int32_t* n_accepted,
+                                        int32_t* next_token, uint32_t* status,
+                                        float* warped_target_out, float* warped_draft_out,
+                                        uint32_t flags, void* stream) {
+  return accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
+                       uniforms, cu_k, batch, k, sum_k, vocab, floor_target, floor_draft, n_accepted,
+                       next_token, status, warped_target_out, warped_draft_out, flags, stream);
 }
 
 const char* sv_status_string(sv_status s) {

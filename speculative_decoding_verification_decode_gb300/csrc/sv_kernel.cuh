@@ -79,6 +79,8 @@ struct Params {
   unsigned* st_out;
   float* wt_out;
   float* wd_out;
+  const float* flo_t;  // per-row floors of the sampler filters (NULL: none)
+  const float* flo_d;
   unsigned flags;
   int slice;       // elements per CTA slice (multiple of the vector width)
   int slot_bytes;  // bytes per ring slot (multiple of 16)
@@ -330,10 +332,12 @@ __device__ __forceinline__ float sum_bound(float Z, int nadd) {
 // The defined weights of a warped row (the values whose exact sum is the
 // row mass): w = 2^((l - m) * k) with m the row maximum and k = log2(e)/T.
 // 16-bit logits: one fp32 subtract and multiply, then ex2.approx.ftz.
+// Both weigh a logit below the row's floor `lo` (the sampler filters' cut;
+// -Inf: none) as 0.
 struct Warp16 {
-  float m, k;
+  float m, k, lo;
   __device__ __forceinline__ float operator()(float l) const {
-    return ex2_ftz(__fmul_rn(__fsub_rn(l, m), k));
+    return l < lo ? 0.f : ex2_ftz(__fmul_rn(__fsub_rn(l, m), k));
   }
 };
 
@@ -341,8 +345,9 @@ struct Warp16 {
 // double-float k = khi + klo kept to about 2^-40, and the low part applied as
 // a first-order correction to 2^hi.
 struct Warp32 {
-  float m, khi, klo;
+  float m, khi, klo, lo;
   __device__ __forceinline__ float operator()(float l) const {
+    if (l < lo) return 0.f;
     const float s = __fsub_rn(l, m);
     const float bb = __fsub_rn(s, l);
     const float err = __fadd_rn(__fsub_rn(l, __fsub_rn(s, bb)), __fsub_rn(-m, bb));
@@ -362,7 +367,9 @@ struct WarpOf<float> {
   using type = Warp32;
 };
 
+// Probability rows are used as they are (`lo` stays -Inf: no floors there).
 struct NoWarp {
+  float lo;
   __device__ __forceinline__ float operator()(float x) const { return x; }
 };
 
@@ -562,7 +569,7 @@ __device__ __forceinline__ void bucket_add(unsigned long long* bk, float x) {
 }
 
 // sum_s bk[s] * 2^s  ->  kLimbs little-endian 32-bit limbs.
-__device__ __noinline__ void buckets_to_limbs(const unsigned long long* bk, uint32_t* limbs) {
+static __device__ __noinline__ void buckets_to_limbs(const unsigned long long* bk, uint32_t* limbs) {
   unsigned long long acc[kLimbs];
   for (int i = 0; i < kLimbs; ++i) acc[i] = 0;
   for (int s = 0; s < kBuckets; ++s) {
@@ -620,7 +627,7 @@ __device__ __forceinline__ int big_cmp(const Big& a, const Big& b) {
 }
 
 // Exact  u * q_t * Sp  <  p_t * Sq  (both sides scaled by 2^447; see f32_parts).
-__device__ __noinline__ bool exact_accept(float u, float pt, float qt, const uint32_t* sp,
+static __device__ __noinline__ bool exact_accept(float u, float pt, float qt, const uint32_t* sp,
                                           const uint32_t* sq) {
   uint32_t Mu, Mq, Mp;
   int su, sq_, sp_;
@@ -706,13 +713,19 @@ struct DrawProbs {
 // exponent, 2^(l k + c) with c = -m k - log2 Z (one FMA and one ex2 per row).
 // Only the draw uses these (they need not equal the defined weights bit for
 // bit; both passes of the draw use the same function).
+// FL: the rows carry sampler-filter floors (logits below weigh 0).
+template <bool FL>
 struct DrawLogits {
   float k, cp, cq, scale;
+  float lo_p, lo_q;  // the rows' floors (FL only)
   int resid;
   __device__ __forceinline__ float operator()(float lp, float lq) const {
-    const float a = ex2_ftz(__fmaf_rn(lp, k, cp));
+    float a = ex2_ftz(__fmaf_rn(lp, k, cp));
+    if constexpr (FL) a = lp < lo_p ? 0.f : a;
     if (!resid) return a;
-    return fmaxf(__fsub_rn(a, ex2_ftz(__fmaf_rn(lq, k, cq))), 0.f);
+    float b = ex2_ftz(__fmaf_rn(lq, k, cq));
+    if constexpr (FL) b = lq < lo_q ? 0.f : b;
+    return fmaxf(__fsub_rn(a, b), 0.f);
   }
   __device__ __forceinline__ unsigned long long fix(float v) const {
     return floor_u64(__fmul_rn(v, scale));

@@ -68,9 +68,12 @@ __device__ __forceinline__ void chunk_mass_f32(const float* s, int n, Acc& a, fl
 }
 
 // Online softmax over a chunk of logits; `mx` tracks the NaN-propagating max
-// (for validity), `o` the running max and sums (for the mass).
-template <typename T>
-__device__ __forceinline__ void chunk_online(const T* s, int n, float k, Online& o, float& mx) {
+// (for validity), `o` the running max and sums (for the mass).  Logits below
+// the row's floor `lo` (the sampler filters; -Inf: none) enter the sums as
+// -Inf, i.e. with weight 0; the maximum and the validity check see them as
+// they are (the floor never exceeds the row maximum).
+template <typename T, bool FL>
+__device__ __forceinline__ void chunk_online(const T* s, int n, float k, float lo, Online& o, float& mx) {
   constexpr int VEC = ElemTraits<T>::kVec;
   constexpr int U = 4;  // vectors a thread holds at once (independent exps)
   const int nv = n / VEC;
@@ -80,12 +83,19 @@ __device__ __forceinline__ void chunk_online(const T* s, int n, float k, Online&
     float vm, vmin;
     load_block<T, U, VEC>(s, base, nv, x, have, vm, vmin);
     mx = fmax_nan(mx, vm);
+    if constexpr (FL) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) x[u][j] = x[u][j] < lo ? -kInfF : x[u][j];
+    }
     o.add_block<U, VEC>(x, have, vm, vmin, k);
   }
   for (int e = nv * VEC + threadIdx.x; e < n; e += kConsumers) {
     const float x = ElemTraits<T>::to_f(s[e]);
     mx = fmax_nan(mx, x);
-    o.add_vec<1>(&x, x, k);
+    const float xm = (FL && x < lo) ? -kInfF : x;
+    o.add_vec<1>(&xm, xm, k);
   }
 }
 
@@ -169,7 +179,9 @@ __device__ __forceinline__ float seq_sum(const float* r) {
 
 enum : int { ACT_CONTINUE = 0, ACT_STOP = 1, ACT_EXACT = 2, ACT_DRAW = 3, ACT_ABORT = 4 };
 
-template <int MODE, typename T>
+// FL: logits rows with sampler-filter floors (P.flo_t / P.flo_d); a separate
+// instantiation, so the unfiltered kernels carry none of its code.
+template <int MODE, typename T, bool FL = false>
 __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __grid_constant__ Params P) {
   using TR = ElemTraits<T>;
   constexpr int VEC = TR::kVec;
@@ -231,6 +243,17 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
   // start of this CTA's slice of target row r (draft row r when q)
   auto row_slice = [&](bool q, int r) -> const T* {
     return q ? drf + (d0 + r) * P.stride + v_lo : tgt + (t0 + r) * P.stride + v_lo;
+  };
+  // the sampler filters' floor of target row r (draft row r when q); -Inf: none
+  auto row_floor = [&](bool q, int r) -> float {
+    if constexpr (!FL) {
+      (void)q;
+      (void)r;
+      return -kInfF;
+    } else {
+      const float* f = q ? P.flo_d : P.flo_t;
+      return f ? __ldg(f + (q ? d0 : t0) + r) : -kInfF;
+    }
   };
 
   // ---------------------------------------------------------------- barriers
@@ -514,7 +537,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     // ============================================================== sampling
     float khi = 0.f, klo = 0.f;
     if (MODE == MODE_LOGITS) log2e_over(temp, khi, klo);
-    auto make_warp = [&](float m) {
+    auto make_warp = [&](float m, float lo) {
       WarpT w;
       if constexpr (MODE == MODE_LOGITS) {
         if constexpr (sizeof(T) == 4) {
@@ -526,8 +549,14 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
           w.k = khi;
         }
       }
+      w.lo = lo;
       (void)m;
       return w;
+    };
+    // the weight functors of row i (target, and draft unless i is the bonus row)
+    auto warp_p = [&](int i, float m) { return make_warp(m, MODE == MODE_LOGITS ? row_floor(false, i) : -kInfF); };
+    auto warp_q = [&](int i, float m, bool bonus) {
+      return make_warp(m, (MODE == MODE_LOGITS && !bonus) ? row_floor(true, i) : -kInfF);
     };
     const bool force_exact = (P.flags & FLAG_FORCE_EXACT) != 0u;
     unsigned long long* buckets = vsum;  // the exact pass and the draw never overlap
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     // streamed, so mostly from L2; collective).  Returns 0 when done (the
     // owning CTA wrote the outputs), 1 when the residual is empty, -1 when a
     // device wait gave up.
-    using DrawT = typename std::conditional<MODE == MODE_LOGITS, DrawLogits, DrawProbs>::type;
+    using DrawT = typename std::conditional<MODE == MODE_LOGITS, DrawLogits<FL>, DrawProbs>::type;
     auto draw = [&](int n_acc_row, bool resid, int n_acc, uint32_t st_in, float u_draw) -> int {
       DrawT dw;
       dw.scale = __uint_as_float(static_cast<uint32_t>(127 + P.fixed_shift) << 23);
@@ -610,6 +639,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         dw.k = khi;  // c = -m k - log2 Z, folded into one FMA per element
         dw.cp = sm.dpar[0];
         dw.cq = sm.dpar[1];
+        dw.lo_p = row_floor(false, n_acc_row);
+        dw.lo_q = resid ? row_floor(true, n_acc_row) : -kInfF;
       } else {
         dw.sp = sm.dpar[0];
         dw.ap = sm.dpar[1];
@@ -934,7 +965,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
               }
             }
           }
-          const WarpT wfp = make_warp(mp), wfq = make_warp(mq);
+          const WarpT wfp = warp_p(i, mp), wfq = warp_q(i, mq, bonus);
           bool posted = false;  // dec[pb] handed over already (an exact pass followed)
           bool have_exact = false;
           double Zp_ex = 0.0, Zq_ex = 0.0;
@@ -968,8 +999,9 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
               // overflow of the partial sums: the exact pass tells them apart
               need_x = !err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (!bonus && !(Zq.hi <= FLT_MAX)));
             } else {
-              p_bad = (badf & 2u) != 0u;  // NaN or +Inf logit
-              q_bad = !bonus && (badf & 4u) != 0u;
+              // NaN or +Inf logit, or a NaN floor (an invalid filter parameter)
+              p_bad = (badf & 2u) != 0u || wfp.lo != wfp.lo;
+              q_bad = !bonus && ((badf & 4u) != 0u || wfq.lo != wfq.lo);
             }
             if (need_x) {
               if (run_exact()) {
@@ -1064,6 +1096,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         float ep = MODE == MODE_PROBS ? kInfF : -kInfF;  // probs: min; logits: max (validity)
         float eq = ep;
         for (int part = 0; part < (bonus ? 1 : 2); ++part) {
+          const float lo = MODE == MODE_LOGITS ? row_floor(part == 1, i) : -kInfF;
           for (int j = 0; j < nck; ++j) {
             if (watch >= 0) {
               int cut = 0;
@@ -1081,7 +1114,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
             if constexpr (MODE == MODE_PROBS)
               chunk_mass_f32(reinterpret_cast<const float*>(s), n, part ? aq : ap, part ? eq : ep);
             else
-              chunk_online<T>(s, n, khi, part ? oq : op, part ? eq : ep);
+              chunk_online<T, FL>(s, n, khi, lo, part ? oq : op, part ? eq : ep);
             release();  // the slot takes later chunks while rows are decided
           }
         }
@@ -1148,7 +1181,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         int act = mbar_wait_bounded(&sm.dfull[pb], static_cast<uint32_t>((i >> 1) & 1)) ? sm.dec[pb].act
                                                                                         : ACT_ABORT;
         if (act == ACT_EXACT) {  // exact masses of row i, then the final outcome
-          const WarpT wfp = make_warp(sm.dec[pb].mp), wfq = make_warp(sm.dec[pb].mq);
+          const WarpT wfp = warp_p(i, sm.dec[pb].mp), wfq = warp_q(i, sm.dec[pb].mq, bonus);
           exact_pass(i, !bonus, wfp, wfq);
           if (tid == 0) mbar_arrive_local(&sm.xfull);
           act = mbar_wait_bounded(&sm.xdec, static_cast<uint32_t>(xr & 1)) ? sm.dec[pb].act : ACT_ABORT;
@@ -1160,7 +1193,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         }
         // warped weights of this row for the caller (testing aid)
         if (MODE == MODE_LOGITS && (P.wt_out || P.wd_out) && act != ACT_STOP) {
-          const WarpT wfp = make_warp(sm.dec[pb].mp), wfq = make_warp(sm.dec[pb].mq);
+          const WarpT wfp = warp_p(i, sm.dec[pb].mp), wfq = warp_q(i, sm.dec[pb].mq, bonus);
           const T* p = row_slice(false, i);
           const T* q = row_slice(true, i);
           for (int e = tid; e < n_el; e += kConsumers) {

@@ -131,3 +131,42 @@ def test_gate_update_argument_errors(lib, kw, frag):
     args.update(kw)
     assert lib.sv_gate_update(*args.values()) == _lib.SV_ERR_ARG
     assert frag in lib.sv_last_error()
+
+
+# ---------------------------------------------------------------- sampler filters (host checks)
+
+def floors(lib, **kw):
+    args = dict(target=1 << 12, draft=1 << 12, dtype=1, stride=16, temp=1 << 12, top_k=1 << 12,
+                top_p=1 << 12, cu=NULL, B=2, K=3, sum_k=6, V=16, ft=1 << 12, fd=1 << 12, stream=NULL)
+    args.update(kw)
+    return lib.sv_sampler_floors(*args.values())
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(B=-1), b"batch"),
+    (dict(K=-1), b"k must"),
+    (dict(V=0), b"vocab"),
+    (dict(stride=8), b"row_stride"),
+    (dict(sum_k=5), b"sum_k"),
+    (dict(dtype=7), b"dtype"),
+    (dict(target=NULL), b"target"),
+    (dict(temp=NULL), b"temperature"),
+    (dict(draft=NULL), b"draft_logits"),
+])
+def test_floors_argument_errors(lib, kw, frag):
+    assert floors(lib, **kw) == _lib.SV_ERR_ARG
+    assert frag in lib.sv_last_error()
+
+
+def test_floors_without_filters_or_rows_launch_nothing(lib):
+    # no CUDA call happens on these paths, so they run without a GPU
+    assert floors(lib, top_k=NULL, top_p=NULL) == _lib.SV_OK
+    assert floors(lib, B=0, sum_k=0) == _lib.SV_OK
+    assert floors(lib, ft=NULL, fd=NULL) == _lib.SV_OK
+
+
+def test_floored_logits_argument_errors(lib):
+    args = [1 << 12, 1 << 12, 9, 16, 1 << 12, 1 << 12, 1 << 12, NULL, 2, 3, 6, 16, NULL, NULL,
+            1 << 12, 1 << 12, 1 << 12, NULL, NULL, 0, NULL]
+    assert lib.sv_accept_from_logits_floored(*args) == _lib.SV_ERR_ARG
+    assert b"dtype" in lib.sv_last_error()
