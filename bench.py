@@ -36,13 +36,17 @@ CONFIG_TEXT = {
     "config3": "B=256 K=4 V=152064 f32 probabilities, greedy",
     "config4": "B=32 ragged K_b~U{0..8} V=129280 f32 probabilities, rejection sampling",
     "config5": "B=1024 K=3 V=32000 f16 logits, half greedy / half sampled",
+    "filter": "config 2 rows (B=64 K=5 V=128256 bf16 logits, T=0.8) with top-k 50 and top-p 0.9 "
+              "on every sequence: floors kernel, then floored verification",
 }
+FILTER_TOP_K, FILTER_TOP_P = 50, 0.9
 KERNEL_NAMES = {
-    "config1": "sv_verify_kernel<1, float>",
-    "config2": "sv_verify_kernel<2, __nv_bfloat16>",
-    "config3": "sv_verify_kernel<0, float>",
-    "config4": "sv_verify_kernel<1, float>",
-    "config5": "sv_verify_kernel<2, __half>",
+    "config1": "sv_verify_kernel<1, float, false>",
+    "config2": "sv_verify_kernel<2, __nv_bfloat16, false>",
+    "config3": "sv_verify_kernel<0, float, false>",
+    "config4": "sv_verify_kernel<1, float, false>",
+    "config5": "sv_verify_kernel<2, __half, false>",
+    "filter": "floors_kernel<__nv_bfloat16>",
 }
 METRIC = "verified rows/s and achieved HBM GB/s vs GB300 peak at B=64 K=5 V=128256"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_config2_traffic.md")
@@ -179,8 +183,13 @@ def device_inputs(wl, torch, dev):
         if dt == "bf16":
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
         return torch.from_numpy(a).to(dev)
-    return dict(target=td(wl.target, wl.dtype), draft=td(wl.draft, wl.dtype), tokens=td(wl.tokens),
-                uniforms=td(wl.uniforms), cu_k=td(wl.cu_k), temperature=td(wl.temperature))
+    x = dict(target=td(wl.target, wl.dtype), draft=td(wl.draft, wl.dtype), tokens=td(wl.tokens),
+             uniforms=td(wl.uniforms), cu_k=td(wl.cu_k), temperature=td(wl.temperature),
+             top_k=td(getattr(wl, "top_k", None)), top_p=td(getattr(wl, "top_p", None)))
+    if x["top_k"] is not None:  # the floors' buffers, reused every step
+        x["floors"] = (torch.empty(wl.target.shape[0], dtype=torch.float32, device=dev),
+                       torch.empty(wl.draft.shape[0], dtype=torch.float32, device=dev))
+    return x
 
 
 def host_inputs(wl, torch):
@@ -191,7 +200,8 @@ def host_inputs(wl, torch):
         t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == "bf16" else torch.from_numpy(a)
         return t.pin_memory()
     return dict(target=th(wl.target, wl.dtype), draft=th(wl.draft, wl.dtype), tokens=th(wl.tokens),
-                uniforms=th(wl.uniforms), cu_k=th(wl.cu_k), temperature=th(wl.temperature))
+                uniforms=th(wl.uniforms), cu_k=th(wl.cu_k), temperature=th(wl.temperature),
+                top_k=th(getattr(wl, "top_k", None)), top_p=th(getattr(wl, "top_p", None)))
 
 
 def call(sv, wl, x):
@@ -200,8 +210,33 @@ def call(sv, wl, x):
         return sv.verify_greedy(x["target"], x["tokens"], x["cu_k"], k)
     if wl.mode in ("accept", "both"):
         return sv.accept(x["target"], x["draft"], x["tokens"], x["uniforms"], x["cu_k"], k)
+    if x.get("top_k") is not None:
+        if "floors" in x:  # device inputs: the floors kernel, then the floored verification
+            floors(sv, wl, x)
+            return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
+                                         x["uniforms"], x["cu_k"], k, floors=x["floors"])
+        return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
+                                     x["uniforms"], x["cu_k"], k, top_k=x["top_k"], top_p=x["top_p"])
     return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
                                  x["uniforms"], x["cu_k"], k)
+
+
+def floors(sv, wl, x):
+    return sv.sampler_floors(x["target"], x["draft"], x["temperature"], x["top_k"], x["top_p"], x["cu_k"],
+                             wl.K, int(wl.tokens.size), out=x["floors"])
+
+
+def make_workload(name, seed_shift=0):
+    """A named workload; 'filter' is config 2 with top-k 50 and top-p 0.9 on
+    every sequence (the sampler filters before verification)."""
+    import workloads
+    base = "config2" if name == "filter" else name
+    base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5}[base]
+    wl = workloads.make_config(base, seed=workloads.configs.SEED_BASE + base_seed + seed_shift)
+    if name == "filter":
+        wl.top_k = np.full(wl.B, FILTER_TOP_K, np.int32)
+        wl.top_p = np.full(wl.B, FILTER_TOP_P, np.float32)
+    return wl
 
 
 def algorithmic_bytes(wl, n_acc):
@@ -240,8 +275,11 @@ def oracle_rows_per_s(wl, budget_s=20.0):
         elif wl.mode in ("accept", "both"):
             oracle.accept(wl.target[tsl], wl.draft[dsl], wl.tokens[dsl], wl.uniforms[tsl], 1, k)
         else:
+            tk, tp = getattr(wl, "top_k", None), getattr(wl, "top_p", None)
             oracle.accept_from_logits(wl.target[tsl], wl.draft[dsl], wl.dtype,
-                                      wl.temperature[b:b + 1], wl.tokens[dsl], wl.uniforms[tsl], 1, k)
+                                      wl.temperature[b:b + 1], wl.tokens[dsl], wl.uniforms[tsl], 1, k,
+                                      top_k=None if tk is None else tk[b:b + 1],
+                                      top_p=None if tp is None else tp[b:b + 1])
         done_rows += k + 1
         done_seq += 1
         tr0 += k + 1
@@ -267,9 +305,7 @@ def run_gpu(args):
     sv.load_library()
 
     # every rank verifies its own batch (independent sequences: weak scaling)
-    seed_shift = rank * 1000
-    base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5}[args.config]
-    wl = workloads.make_config(args.config, seed=workloads.configs.SEED_BASE + base_seed + seed_shift)
+    wl = make_workload(args.config, seed_shift=rank * 1000)
     x = device_inputs(wl, torch, dev)
     rows_per_step = int((wl.k_per_seq + 1).sum())
     stream = torch.cuda.current_stream(dev)
@@ -302,6 +338,15 @@ def run_gpu(args):
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(per_step_ms))
     ms = max_over_ranks(ms_local, dist, dev)
+    floors_ms = None
+    if args.config == "filter":  # the floors kernel alone (the roofline's kernel)
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            floors(sv, wl, x)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        floors_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
 
     # end to end through the public API with pinned host buffers
     hx = host_inputs(wl, torch)
@@ -328,6 +373,8 @@ def run_gpu(args):
         alg = algorithmic_bytes(wl, n_acc)
         formula = wl.formula_bytes()
         achieved = alg / (ms_local * 1e-3) / 1e9
+        if floors_ms is not None:  # the floors read every row once: the formula bytes
+            achieved = formula / (floors_ms * 1e-3) / 1e9
         traffic = profiled_traffic() if args.config == "config2" else None
         value = world * rows_per_step / (ms * 1e-3)
         cpu_val, cpu_seq, cpu_dt = oracle_rows_per_s(wl, budget_s=args.cpu_budget)
@@ -356,6 +403,8 @@ def run_gpu(args):
                 "algorithmic_bytes_per_step": alg,
                 "l2": "flushed between timed steps (512 MB write, then a 512 MB read)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                **({"floors_us": floors_ms * 1e3, "verify_us": (ms_local - floors_ms) * 1e3,
+                    "top_k": FILTER_TOP_K, "top_p": FILTER_TOP_P} if floors_ms is not None else {}),
             },
             "roofline": {
                 "bound": "hbm",
@@ -382,7 +431,7 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
             },
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.config == "filter" else 1),
             "clocks": clocks.summary(),
         }
         print(json.dumps(result), flush=True)
@@ -656,7 +705,7 @@ def run_reference(args):
     rank, world, _ = dist_info()
     if rank != 0:
         return None
-    wl = workloads.make_config(args.config)
+    wl = make_workload(args.config)
     per_step = []
     for i in range(args.warmup + args.steps):
         v, nseq, dt = oracle_rows_per_s(wl, budget_s=args.ref_step_budget)

@@ -191,9 +191,12 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     return m.finish(VerifyResult(n, nxt, st))
 
 
-def _floors(lib, m, tg, dr, T, tk, tp, cu, B, K, sum_k):
-    ft = torch.full((sum_k + B,), float("-inf"), dtype=torch.float32, device=m.device)
-    fd = torch.full((sum_k,), float("-inf"), dtype=torch.float32, device=m.device)
+def _floors(lib, m, tg, dr, T, tk, tp, cu, B, K, sum_k, out=None):
+    if out is not None:
+        ft, fd = out
+    else:
+        ft = torch.full((sum_k + B,), float("-inf"), dtype=torch.float32, device=m.device)
+        fd = torch.full((sum_k,), float("-inf"), dtype=torch.float32, device=m.device)
     with torch.cuda.device(m.device):
         _check(lib.sv_sampler_floors(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T), _p(tk),
                                      _p(tp), _p(cu), B, K, sum_k, tg.shape[1], _p(ft), _p(fd),
@@ -204,12 +207,14 @@ def _floors(lib, m, tg, dr, T, tk, tp, cu, B, K, sum_k):
 def sampler_floors(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                    temperature: torch.Tensor, top_k: Optional[torch.Tensor] = None,
                    top_p: Optional[torch.Tensor] = None, cu_k: Optional[torch.Tensor] = None,
-                   k: Optional[int] = None, sum_k: Optional[int] = None):
+                   k: Optional[int] = None, sum_k: Optional[int] = None, out: Optional[tuple] = None):
     """Per-row floors of the top-k / top-p filters (include/sv_filter.h):
     ``(floor_target [target_rows], floor_draft [draft_rows])`` f32; the rows a
     filter keeps are those with logit >= floor (-inf keeps all, NaN marks an
     invalid top-p).  Without ``cu_k`` the layout is B*(K+1) target rows and
-    B*K draft rows with ``k`` = K."""
+    B*K draft rows with ``k`` = K.  ``out``: optional preallocated f32 device
+    tensors for the two results (device inputs only; rows the kernel does not
+    reach keep their values)."""
     m = _Marshal(target_logits)
     tg = _rows(m.dev(target_logits))
     dr = _rows(m.dev(draft_logits, tg.dtype))
@@ -228,7 +233,7 @@ def sampler_floors(target_logits: torch.Tensor, draft_logits: torch.Tensor,
             raise ValueError("k and sum_k are required with cu_k")
         K, sk = int(k), int(sum_k)
     ft, fd = _floors(_lib.load(), m, tg, dr, T, m.dev(top_k, torch.int32), m.dev(top_p, torch.float32),
-                     cu, B, K, sk)
+                     cu, B, K, sk, None if m.host else out)
     if m.host:
         return ft.cpu(), fd.cpu()
     return ft, fd

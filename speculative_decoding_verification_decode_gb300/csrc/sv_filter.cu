@@ -13,17 +13,22 @@
 // (sign, exponent and two mantissa bits of an f32), so the logits of a row
 // spread over many bins and the shared-memory atomics rarely collide.
 //
-// The first pass over the row also keeps each thread's 8 largest keys in
-// registers (4096 candidates per row, then in shared memory).  A floor among
-// the top few thousand logits (the usual top-k, and top-p of a peaked row) is
-// then selected from the candidates alone, with a check that proves the
-// answer is the row's own; otherwise the select runs over the whole row.  So
-// top-k reads the row once and top-p twice (the second pass sums the kept
-// weight, without atomics).
+// Two passes over the row.  The first takes the row maximum, the non-NaN
+// count and a strided sample of 4096 logits; the sample gives a lower bound L
+// of the floor (for top-k the rank 2k plus a margin, for top-p alone the rank
+// of about 2500 logits), and the second pass appends every logit >= L to a
+// shared-memory list and, for top-p alone, sums the row's weight Z.  The
+// exact selects then run on the list: its counts and weights are complete
+// for every key >= L, so a floor found there is the row's own when (top-k)
+// the list holds at least k keys, or (top-p alone) the test already fails
+// once the chosen key's own group is added.  When a check fails or the list
+// overflows, the same selects run over the whole row instead (a few more
+// passes; correct, only slower).
 //
 // Counts are 32-bit integers and weights 64-bit fixed point (2^-40 units,
-// truncated), so every sum is exact and independent of the order of the
-// atomics: the result is deterministic.
+// truncated, converted on the integer pipe: this part's fp64 pipe, which
+// also serves 64-bit conversions, is slow), so every sum is exact and
+// independent of the order of the atomics: the result is deterministic.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -38,7 +43,7 @@ namespace svf {
 constexpr int kThreads = 512;
 constexpr int kWarpsF = kThreads / 32;
 constexpr int kMaxBins = 2048;
-constexpr int kCand = 8;  // largest keys each thread keeps from the first pass
+constexpr int kCap = 4096;  // sampled keys, then collected keys, in shared memory
 
 struct Args {
   const void* tgt;
@@ -69,6 +74,7 @@ struct KeyOf<float> {
     return true;
   }
   __device__ static float value_raw(uint32_t raw) { return __uint_as_float(raw); }
+  __device__ static uint32_t raw_of(float x) { return __float_as_uint(x); }
   __device__ static float value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
   }
@@ -92,32 +98,23 @@ struct Key16 {
   __device__ static float value(uint32_t k) {
     return value_raw((k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu));
   }
+  // the raw bits of a value of this type (exact: x came from value_raw)
+  __device__ static uint32_t raw_of(float x) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) return __float_as_uint(x) >> 16;
+    else return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
+  }
 };
 template <>
 struct KeyOf<__nv_bfloat16> : Key16<__nv_bfloat16> {};
 template <>
 struct KeyOf<__half> : Key16<__half> {};
 
-// f(raw bits) for every element of a row: 16-byte loads where the row is
-// aligned (kLoads of them in flight per thread), element loads for the rest.
-// The order of the calls is immaterial (every use is an exact integer
-// reduction).
-template <typename T, typename F>
-__device__ __forceinline__ void vec_elems(const uint4 v, F& f) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if constexpr (sizeof(T) == 4) {
-      f(w[j]);
-    } else {
-      f(w[j] & 0xFFFFu);
-      f(w[j] >> 16);
-    }
-  }
-}
-
-template <typename T, typename F>
-__device__ __forceinline__ void for_each_raw(const T* row, int V, F&& f) {
+// Every element of a row: fw(32-bit word) for the 16-byte aligned part (one
+// f32 or two packed 16-bit values per word; kLoads vectors in flight per
+// thread), fe(raw bits) for single elements elsewhere.  The order of the
+// calls is immaterial (every use is an exact integer reduction or a max).
+template <typename T, typename FW, typename FE>
+__device__ __forceinline__ void for_each_word(const T* row, int V, FW&& fw, FE&& fe) {
   constexpr int VEC = 16 / static_cast<int>(sizeof(T));
   constexpr int kLoads = 4;
   int done = 0;
@@ -130,15 +127,42 @@ __device__ __forceinline__ void for_each_raw(const T* row, int V, F&& f) {
 #pragma unroll
       for (int u = 0; u < kLoads; ++u) v[u] = __ldg(r4 + vi + u * kThreads);
 #pragma unroll
-      for (int u = 0; u < kLoads; ++u) vec_elems<T>(v[u], f);
+      for (int u = 0; u < kLoads; ++u) {
+        fw(v[u].x);
+        fw(v[u].y);
+        fw(v[u].z);
+        fw(v[u].w);
+      }
     }
-    for (; vi < nv; vi += kThreads) vec_elems<T>(__ldg(r4 + vi), f);
+    for (; vi < nv; vi += kThreads) {
+      const uint4 v = __ldg(r4 + vi);
+      fw(v.x);
+      fw(v.y);
+      fw(v.z);
+      fw(v.w);
+    }
     done = nv * VEC;
   }
   for (int e = done + static_cast<int>(threadIdx.x); e < V; e += kThreads) {
-    if constexpr (sizeof(T) == 4) f(__ldg(reinterpret_cast<const uint32_t*>(row) + e));
-    else f(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e)));
+    if constexpr (sizeof(T) == 4) fe(__ldg(reinterpret_cast<const uint32_t*>(row) + e));
+    else fe(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e)));
   }
+}
+
+// f(raw bits) for every element of a row.
+template <typename T, typename F>
+__device__ __forceinline__ void for_each_raw(const T* row, int V, F&& f) {
+  for_each_word<T>(
+      row, V,
+      [&](uint32_t w) {
+        if constexpr (sizeof(T) == 4) {
+          f(w);
+        } else {
+          f(w & 0xFFFFu);
+          f(w >> 16);
+        }
+      },
+      f);
 }
 
 // Selection state shared by the CTA: the key prefix chosen so far and the
@@ -186,17 +210,22 @@ __device__ __forceinline__ int warp_pick(unsigned long long c, unsigned long lon
   return l;
 }
 
-// Warp 0: the lowest non-empty bin of hc / hm (nb bins, a multiple of 32)
-// whose keys above pass the test; updates s (prefix extended by `width` bits,
-// the carry by the bins above the chosen one).
-__device__ __forceinline__ void scan_bins(const unsigned* hc, const unsigned long long* hm, int nb, int width,
+// Warp 0: the lowest non-empty bin of hc / hm (32 * PER bins) whose keys
+// above pass the test; updates s (prefix extended by `width` bits, the carry
+// by the bins above the chosen one, the group by the chosen bin).  PER is a
+// compile-time count so each lane's loads are unrolled and overlap.
+template <int PER>
+__device__ __forceinline__ void scan_bins(const unsigned* hc, const unsigned long long* hm, int width,
                                           const Crit& cr, Sel& s) {
   const int lane = threadIdx.x & 31;
-  const int per = nb / 32;
   unsigned long long c = 0, m = 0;
-  for (int j = 0; j < per; ++j) {
-    c += hc[lane * per + j];
-    m += hm[lane * per + j];
+  // each lane sums its own PER bins, starting at a lane-dependent offset so
+  // the 32 lanes read 32 different banks at every step
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int b = lane * PER + ((j + lane) & (PER - 1));
+    c += hc[b];
+    m += hm[b];
   }
   unsigned long long ac, am;
   const int l1 = warp_pick(c, m, s.c_above, s.m_above, cr, ac, am);
@@ -204,14 +233,15 @@ __device__ __forceinline__ void scan_bins(const unsigned* hc, const unsigned lon
     if (lane == 0) s.ok = 0;
     return;
   }
-  // lanes split the chosen range of `per` bins, q bins each
-  const int q = per >= 32 ? per / 32 : 1;
-  const int base = l1 * per;
+  // lanes split the chosen range of PER bins, Q bins each
+  constexpr int Q = PER >= 32 ? PER / 32 : 1;
+  const int base = l1 * PER;
   c = m = 0;
-  if (lane * q < per) {
-    for (int j = 0; j < q; ++j) {
-      c += hc[base + lane * q + j];
-      m += hm[base + lane * q + j];
+  if (lane * Q < PER) {
+#pragma unroll
+    for (int j = 0; j < Q; ++j) {
+      c += hc[base + lane * Q + j];
+      m += hm[base + lane * Q + j];
     }
   }
   const int l2 = warp_pick(c, m, ac, am, cr, ac, am);
@@ -222,8 +252,9 @@ __device__ __forceinline__ void scan_bins(const unsigned* hc, const unsigned lon
   if (lane == l2) {  // at most two bins left: walk them from the top
     int bin = -1;
     unsigned long long bc = 0, bm = 0;
-    for (int j = q - 1; j >= 0; --j) {
-      const int b = base + lane * q + j;
+#pragma unroll
+    for (int j = Q - 1; j >= 0; --j) {
+      const int b = base + lane * Q + j;
       if (hc[b] == 0u) continue;
       if (!cr.within(ac, am)) break;
       bin = b;
@@ -278,7 +309,11 @@ __device__ __forceinline__ void radix_select(const Src& src, const WFn& weight, 
       });
     }
     __syncthreads();
-    if (tid < 32 && ok) scan_bins(h_cnt, h_mass, nb, KT::width(l), cr, sel);
+    if (tid < 32 && ok) {
+      if (nb == 2048) scan_bins<64>(h_cnt, h_mass, KT::width(l), cr, sel);
+      else if (nb == 1024) scan_bins<32>(h_cnt, h_mass, KT::width(l), cr, sel);
+      else scan_bins<1>(h_cnt, h_mass, KT::width(l), cr, sel);
+    }
     __syncthreads();
   }
 }
@@ -289,10 +324,12 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   using WarpT = typename svk::WarpOf<T>::type;
   __shared__ unsigned h_cnt[kMaxBins];
   __shared__ unsigned long long h_mass[kMaxBins];
-  __shared__ uint32_t cand[kThreads * kCand];
-  __shared__ unsigned r_max[kWarpsF], r_cnt[kWarpsF], r_g[kWarpsF];
+  __shared__ uint32_t col[kCap];  // the sample, then the collected keys
+  __shared__ unsigned r_cnt[kWarpsF];
+  __shared__ float r_max[kWarpsF];
   __shared__ unsigned long long r_z[kWarpsF];
   __shared__ Sel sel;
+  __shared__ int n_col;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   const long long b = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
@@ -334,118 +371,188 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     return;
   }
 
-  // ---- pass 1: the row maximum, the non-NaN count, and each thread's kCand
-  // largest keys (candidates; 0 = none).  Every key above G, the largest of
-  // the threads' smallest candidates, is a candidate.
-  uint32_t kmax = 0u, nn = 0u;
-  uint32_t c[kCand];
-#pragma unroll
-  for (int j = 0; j < kCand; ++j) c[j] = 0u;
+  // ---- pass 1: the row maximum and non-NaN count; a strided sample of
+  // kCap keys (0: NaN) into `col`
+  float mx = -kInfF;
+  uint32_t nan_n = 0u;
   for_each_raw<T>(row, a.V, [&](uint32_t raw) {
-    uint32_t k;
-    if (!KT::key(raw, k)) return;
-    kmax = max(kmax, k);
-    ++nn;
-    if (k > c[kCand - 1]) {
-      c[kCand - 1] = k;
-#pragma unroll
-      for (int j = kCand - 1; j > 0; --j) {
-        if (c[j] > c[j - 1]) {
-          const uint32_t t = c[j];
-          c[j] = c[j - 1];
-          c[j - 1] = t;
-        }
-      }
-    }
+    const float x = KT::value_raw(raw);
+    mx = fmaxf(mx, x);  // NaN never wins
+    nan_n += x != x ? 1u : 0u;
   });
+  uint32_t nn = nan_n;  // NaN count here; the non-NaN count after the reduction
 #pragma unroll
-  for (int j = 0; j < kCand; ++j) cand[tid * kCand + j] = c[j];
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  for (int j = 0; j < kCap / kThreads; ++j) {
+    const int e = static_cast<int>((static_cast<long long>(tid * (kCap / kThreads) + j) * a.V) / kCap);
+    uint32_t raw;
+    if constexpr (sizeof(T) == 4) raw = __ldg(reinterpret_cast<const uint32_t*>(row) + e);
+    else raw = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e));
+    uint32_t k;
+    col[tid * (kCap / kThreads) + j] = KT::key(raw, k) ? k : 0u;
+  }
+  mx = svk::warp_max_f(mx);
   nn = __reduce_add_sync(0xFFFFFFFFu, nn);
-  const uint32_t gl = __reduce_max_sync(0xFFFFFFFFu, c[kCand - 1]);
   if (lane == 0) {
-    r_max[warp] = kmax;
+    r_max[warp] = mx;
     r_cnt[warp] = nn;
-    r_g[warp] = gl;
   }
+  if (tid == 0) n_col = 0;
   __syncthreads();
-  kmax = 0u;
+  mx = -kInfF;
   nn = 0u;
-  uint32_t G = 0u;
   for (int w = 0; w < kWarpsF; ++w) {
-    kmax = max(kmax, r_max[w]);
+    mx = fmaxf(mx, r_max[w]);
     nn += r_cnt[w];
-    G = max(G, r_g[w]);
   }
-  const float m = KT::value(kmax);
-  if (nn == 0u || !(m > -kInfF && m < kInfF)) {  // no finite maximum: no filter
+  nn = static_cast<uint32_t>(a.V) - nn;
+  if (nn == 0u || !(mx > -kInfF && mx < kInfF)) {  // no finite maximum: no filter
     if (tid == 0) *out = -kInfF;
     return;
   }
+  uint32_t kmax;
+  KT::key(KT::raw_of(mx), kmax);
+  const float m = KT::value(kmax);
   if (use_k && static_cast<uint32_t>(kk) >= nn) use_k = false;  // k covers the row
 
-  auto cand_src = [&](auto f) {
-    for (int j = tid; j < kThreads * kCand; j += kThreads) {
-      const uint32_t k = cand[j];
+  float khi = 0.f, klo = 0.f;
+  svk::log2e_over(temp, khi, klo);
+  WarpT wf;
+  if constexpr (sizeof(T) == 4) {
+    wf.m = m;
+    wf.khi = khi;
+    wf.klo = klo;
+  } else {
+    wf.m = m;
+    wf.k = khi;
+  }
+  wf.lo = -kInfF;
+  auto weight = [&](uint32_t k) -> unsigned long long {
+    return svk::floor_u64(__fmul_rn(wf(KT::value(k)), 0x1p40f));
+  };
+  auto none = [](uint32_t) { return 0ull; };
+  auto col_src = [&](auto f) {
+    const int n = min(n_col, kCap);
+    for (int j = tid; j < n; j += kThreads) f(col[j]);
+  };
+  auto samp_src = [&](auto f) {
+    for (int j = tid; j < kCap; j += kThreads) {
+      const uint32_t k = col[j];
       if (k) f(k);
     }
   };
-  auto row_src = [&](auto f) {
-    for_each_raw<T>(row, a.V, [&](uint32_t raw) {
-      uint32_t k;
-      if (KT::key(raw, k)) f(k);
-    });
-  };
-  // A selection among the candidates is the row's own when the chosen key is
-  // above G (so every key at or above it is a candidate: the counts and
-  // weights above it and at it are complete) and the test already fails once
-  // its own group is added (so no lower key can pass).
 
-  // ---- top-k: the k-th largest key
-  uint32_t key_k = 0u;  // below every key: keeps all
-  if (use_k) {
-    const Crit cr{true, static_cast<unsigned long long>(kk), 0.0};
-    auto none = [](uint32_t) { return 0ull; };
-    radix_select<KT>(cand_src, none, false, 0u, cr, h_cnt, h_mass, sel);
-    const bool exact = sel.ok && sel.prefix > G && !cr.within(sel.c_above + sel.c_grp, 0ull);
-    if (!exact) radix_select<KT>(row_src, none, false, 0u, cr, h_cnt, h_mass, sel);
-    key_k = sel.ok ? sel.prefix : 0u;
-  }
-
-  // ---- top-p on what top-k kept: the lowest key whose kept weight above is < p Z
-  uint32_t key_p = key_k;
-  if (use_p && key_k < kmax) {
-    float khi, klo;
-    svk::log2e_over(temp, khi, klo);
-    WarpT wf;
-    if constexpr (sizeof(T) == 4) {
-      wf.m = m;
-      wf.khi = khi;
-      wf.klo = klo;
-    } else {
-      wf.m = m;
-      wf.k = khi;
+  // ---- a lower bound L of the floor from the sample: every logit >= L is
+  // collected in pass 2.  Top-k: the sample's rank of 2k logits, plus a
+  // margin.  Top-p alone: the rank of about 0.6 kCap logits (a nucleus of up
+  // to a couple of thousand logits is then complete in the list).  A sample
+  // rank beyond the sample collects every logit.
+  uint32_t L = 1u;  // every key is >= 1
+  {
+    const unsigned long long ns = kCap;  // samples drawn (a short row is sampled repeatedly)
+    const unsigned long long j = use_k ? 2ull * static_cast<unsigned long long>(kk) * ns / nn + 16ull
+                                       : (6ull * kCap / 10ull) * ns / nn;
+    if (j >= 1ull && j < ns) {
+      radix_select<KT>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
+      if (sel.ok) L = sel.prefix;
     }
-    wf.lo = -kInfF;
-    auto weight = [&](uint32_t k) -> unsigned long long {
-      return __float2ull_rz(__fmul_rn(wf(KT::value(k)), 0x1p40f));
-    };
-    // Z: the kept weight (a pass over the row without atomics)
-    unsigned long long z = 0ull;
-    row_src([&](uint32_t k) {
-      if (k >= key_k) z += weight(k);
+  }
+  __syncthreads();  // the sample is no longer read
+
+  // ---- pass 2: collect every key >= L (its count is exact); with top-p alone
+  // also the total weight Z
+  unsigned long long z = 0ull;
+  {
+    const bool need_z = !use_k;
+    // compared as values (NaN never passes; -0 and +0 compare equal, as
+    // their keys are equal); keys only for the logits collected
+    const float Lf = L == 1u ? -kInfF : KT::value(L);
+    for_each_raw<T>(row, a.V, [&](uint32_t raw) {
+      const float x = KT::value_raw(raw);
+      if (need_z && x == x) z += svk::floor_u64(__fmul_rn(wf(x), 0x1p40f));
+      if (x >= Lf) {
+        uint32_t k;
+        KT::key(raw, k);
+        const int at = atomicAdd(&n_col, 1);
+        if (at < kCap) col[at] = k;
+      }
     });
+    if (need_z) {
 #pragma unroll
-    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-    if (lane == 0) r_z[warp] = z;
-    __syncthreads();
+      for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+      if (lane == 0) r_z[warp] = z;
+    }
+  }
+  __syncthreads();
+  if (!use_k) {
     z = 0ull;
     for (int w = 0; w < kWarpsF; ++w) z += r_z[w];
-    const Crit cr{false, 0ull, static_cast<double>(p) * static_cast<double>(z)};
-    radix_select<KT>(cand_src, weight, true, key_k, cr, h_cnt, h_mass, sel);
-    const bool exact = sel.ok && sel.prefix > G && !cr.within(0ull, sel.m_above + sel.m_grp);
-    if (!exact) radix_select<KT>(row_src, weight, true, key_k, cr, h_cnt, h_mass, sel);
-    if (sel.ok) key_p = sel.prefix;
+  }
+  const int nc = n_col;
+  // the collection holds every key >= L unless it overflowed; for top-k it
+  // must also reach k keys (else the k-th largest lies below L)
+  bool fast = nc <= kCap && (!use_k || nc >= kk);
+
+  uint32_t key_k = 0u, key_p = 0u;
+  if (fast) {
+    if (use_k) {
+      radix_select<KT>(col_src, none, false, 0u, Crit{true, static_cast<unsigned long long>(kk), 0.0}, h_cnt,
+                       h_mass, sel);
+      fast = sel.ok != 0;
+      key_k = sel.prefix;
+      key_p = key_k;
+    }
+    if (fast && use_p && key_k < kmax) {
+      if (use_k) {  // Z over the top-k set, all of it collected
+        unsigned long long zk = 0ull;
+        col_src([&](uint32_t k) {
+          if (k >= key_k) zk += weight(k);
+        });
+#pragma unroll
+        for (int o = 16; o; o >>= 1) zk += __shfl_xor_sync(0xFFFFFFFFu, zk, o);
+        __syncthreads();
+        if (lane == 0) r_z[warp] = zk;
+        __syncthreads();
+        z = 0ull;
+        for (int w = 0; w < kWarpsF; ++w) z += r_z[w];
+      }
+      const Crit cr{false, 0ull, static_cast<double>(p) * static_cast<double>(z)};
+      radix_select<KT>(col_src, weight, true, key_k, cr, h_cnt, h_mass, sel);
+      // with top-k every key above the answer is collected; with top-p alone
+      // the answer is the row's own once the test fails with its own group
+      fast = sel.ok && (use_k || !cr.within(0ull, sel.m_above + sel.m_grp));
+      key_p = sel.prefix;
+    }
+  }
+  if (!fast) {  // full-row radix selects
+    auto row_src = [&](auto f) {
+      for_each_raw<T>(row, a.V, [&](uint32_t raw) {
+        uint32_t k;
+        if (KT::key(raw, k)) f(k);
+      });
+    };
+    key_k = 0u;
+    if (use_k) {
+      radix_select<KT>(row_src, none, false, 0u, Crit{true, static_cast<unsigned long long>(kk), 0.0}, h_cnt,
+                       h_mass, sel);
+      key_k = sel.ok ? sel.prefix : 0u;
+    }
+    key_p = key_k;
+    if (use_p && key_k < kmax) {
+      unsigned long long zr = 0ull;
+      row_src([&](uint32_t k) {
+        if (k >= key_k) zr += weight(k);
+      });
+#pragma unroll
+      for (int o = 16; o; o >>= 1) zr += __shfl_xor_sync(0xFFFFFFFFu, zr, o);
+      __syncthreads();
+      if (lane == 0) r_z[warp] = zr;
+      __syncthreads();
+      zr = 0ull;
+      for (int w = 0; w < kWarpsF; ++w) zr += r_z[w];
+      radix_select<KT>(row_src, weight, true, key_k,
+                       Crit{false, 0ull, static_cast<double>(p) * static_cast<double>(zr)}, h_cnt, h_mass, sel);
+      if (sel.ok) key_p = sel.prefix;
+    }
   }
   if (tid == 0) *out = key_p == 0u ? -kInfF : KT::value(key_p);
 }
