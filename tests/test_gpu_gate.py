@@ -1,8 +1,9 @@
 """Draft-length gate on the GPU vs the oracle (PocketLLM dspark.md, the gate).
 
 Lengths, cu_k and the updated calibration counts must be bit-identical:
-both sides evaluate the same fp64 operations in the same order, and the
-update's counts are integers tallied before the one decay-and-add.
+both sides take the length decision with the same fp32 operations in the
+same order, and the update's counts are integers tallied before the one fp64
+decay-and-add.
 """
 
 import numpy as np
