@@ -413,6 +413,10 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   KT::key(KT::raw_of(mx), kmax);
   const float m = KT::value(kmax);
   if (use_k && static_cast<uint32_t>(kk) >= nn) use_k = false;  // k covers the row
+  if (!use_k && !use_p) {
+    if (tid == 0) *out = -kInfF;
+    return;
+  }
 
   float khi = 0.f, klo = 0.f;
   svk::log2e_over(temp, khi, klo);

@@ -8,6 +8,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -56,3 +57,18 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_filter_workload_and_its_reference_arm():
+    """The filter line's workload is config 2 with per-sequence top-k / top-p,
+    and its reference arm runs the oracle with those filters."""
+    import bench
+    wl = bench.make_workload("filter")
+    assert wl.B == 64 and wl.K == 5 and wl.V == 128256 and wl.dtype == "bf16"
+    assert (wl.top_k == bench.FILTER_TOP_K).all() and np.allclose(wl.top_p, bench.FILTER_TOP_P)
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+           "--ref-step-budget", "0.3", "--config", "filter"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    d = json.loads([l for l in res.stdout.splitlines() if l.startswith("{")][-1])
+    assert d["impl"] == "reference" and d["value"] > 0 and "top-k 50" in d["config"]["workload"]
