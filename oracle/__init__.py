@@ -7,7 +7,8 @@ or links anything here, and this package imports nothing from it: the two
 share no code, constants or helpers.  Inputs come from ``workloads`` (data
 only) or from the tests themselves.
 
-``sampler_filter`` holds the top-k / top-p filters applied to p and q
+``lm_head`` puts the LM head (logits = H W^T, llmstudio.ru section 21) in
+front of the verification.  ``sampler_filter`` holds the top-k / top-p filters applied to p and q
 before verification (llmstudio.ru section 38).  ``draft_gate`` is the
 draft-length gate that produces the ragged ``cu_k``
 (PocketLLM docs/dspark.md, the draft-length gate section).
@@ -48,6 +49,11 @@ from .sampler_filter import (  # noqa: F401
     floor_is_valid,
     apply_floor,
     floors_batch,
+)
+from .lm_head import (  # noqa: F401
+    lm_head_logits,
+    accept_lm_head,
+    verify_greedy_lm_head,
 )
 from .draft_gate import (  # noqa: F401
     GateParams,

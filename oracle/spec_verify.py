@@ -73,8 +73,10 @@ class Result:
 # ------------------------------------------------------------------ inputs
 
 def decode_rows(arr: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact conversion of stored rows to float64 ('f32', 'f16', or 'bf16'
-    given as uint16 bit patterns)."""
+    """Exact conversion of stored rows to float64 ('f32', 'f16', 'bf16'
+    given as uint16 bit patterns, or 'f64' as they are)."""
+    if dtype == "f64":
+        return np.asarray(arr, np.float64)
     if dtype == "bf16":
         bits = np.asarray(arr, np.uint16).astype(np.uint32) << 16
         return bits.view(np.float32).astype(np.float64)

@@ -49,3 +49,18 @@ def test_bf16_rounding():
     x = np.array([1.0, 1.00390625, 1.01171875, -2.5, 3.0e38], np.float32)
     bits = w.f32_to_bf16_bits(x)
     assert list(bits[:4]) == [0x3F80, 0x3F80, 0x3F82, 0xC020]
+
+
+def test_lm_head_workload_shapes_and_determinism():
+    import workloads as W
+    a = W.make_lm_head(B=3, K=2, V=50, d=16)
+    b = W.make_lm_head(B=3, K=2, V=50, d=16)
+    assert a.h_target.shape == (9, 16) and a.h_draft.shape == (6, 16) and a.w.shape == (50, 16)
+    assert a.h_target.dtype == np.uint16 and a.w.dtype == np.uint16
+    assert ((a.tokens >= 0) & (a.tokens < 50)).all() and a.uniforms.shape == (9,)
+    for x, y in ((a.h_target, b.h_target), (a.w, b.w), (a.tokens, b.tokens), (a.uniforms, b.uniforms)):
+        assert np.array_equal(x, y)
+    # logits of the projection have about the requested spread
+    h = (a.h_target.astype(np.uint32) << 16).view(np.float32)
+    w = (a.w.astype(np.uint32) << 16).view(np.float32)
+    assert 1.5 < float((h @ w.T).std()) < 5.0

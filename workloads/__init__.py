@@ -21,3 +21,4 @@ from .configs import (  # noqa: F401
     f32_to_bf16_bits,
     uniforms_24bit,
 )
+from .lm_head import LMHeadWorkload, make_lm_head  # noqa: F401,E402
