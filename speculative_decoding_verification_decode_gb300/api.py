@@ -215,6 +215,22 @@ def sampler_floors(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     B*K draft rows with ``k`` = K.  ``out``: optional preallocated f32 device
     tensors for the two results (device inputs only; rows the kernel does not
     reach keep their values)."""
+    n_t = target_logits.reshape(-1, target_logits.shape[-1]).shape[0]
+    n_d = draft_logits.reshape(-1, draft_logits.shape[-1]).shape[0]
+    if cu_k is None:
+        B = int(temperature.numel())
+        K = (n_t - B) // B if B else 0
+        sk = B * K
+        if n_t != B * (K + 1) or n_d != sk:
+            raise ValueError(f"without cu_k the rows must be B*(K+1) target and B*K draft rows for "
+                             f"B = {B} temperatures (got {n_t} and {n_d})")
+    else:
+        B = int(cu_k.numel()) - 1
+        if k is None or sum_k is None:
+            raise ValueError("k and sum_k are required with cu_k")
+        K, sk = int(k), int(sum_k)
+        if n_t < sk + B or n_d < sk:
+            raise ValueError(f"cu_k needs {sk + B} target and {sk} draft rows (got {n_t} and {n_d})")
     m = _Marshal(target_logits)
     tg = _rows(m.dev(target_logits))
     dr = _rows(m.dev(draft_logits, tg.dtype))
@@ -223,15 +239,6 @@ def sampler_floors(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         tg = tg.contiguous()
     T = m.dev(temperature.reshape(-1), torch.float32)
     cu = m.dev(cu_k, torch.int32)
-    if cu is None:
-        B = int(T.numel())
-        K = (tg.shape[0] - B) // B if B else 0
-        sk = B * K
-    else:
-        B = int(cu.numel()) - 1
-        if k is None or sum_k is None:
-            raise ValueError("k and sum_k are required with cu_k")
-        K, sk = int(k), int(sum_k)
     ft, fd = _floors(_lib.load(), m, tg, dr, T, m.dev(top_k, torch.int32), m.dev(top_p, torch.float32),
                      cu, B, K, sk, None if m.host else out)
     if m.host:

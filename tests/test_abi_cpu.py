@@ -170,3 +170,16 @@ def test_floored_logits_argument_errors(lib):
             1 << 12, 1 << 12, 1 << 12, NULL, NULL, 0, NULL]
     assert lib.sv_accept_from_logits_floored(*args) == _lib.SV_ERR_ARG
     assert b"dtype" in lib.sv_last_error()
+
+
+def test_floors_binding_checks_row_counts_before_any_device_work():
+    import torch
+    from speculative_decoding_verification_decode_gb300 import sampler_floors
+    T = torch.full((4,), 0.8)
+    with pytest.raises(ValueError, match="B\\*\\(K\\+1\\)"):
+        sampler_floors(torch.zeros(4 * 3 + 1, 8), torch.zeros(8, 8), T, torch.ones(4, dtype=torch.int32))
+    with pytest.raises(ValueError, match="B\\*\\(K\\+1\\)"):
+        sampler_floors(torch.zeros(12, 8), torch.zeros(7, 8), T, torch.ones(4, dtype=torch.int32))
+    with pytest.raises(ValueError, match="cu_k needs"):
+        sampler_floors(torch.zeros(5, 8), torch.zeros(2, 8), T, None, torch.full((4,), 0.9),
+                       torch.tensor([0, 1, 2, 3, 4], dtype=torch.int32), k=1, sum_k=4)
