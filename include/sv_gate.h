@@ -29,12 +29,16 @@
  *   confidence falls in bucket 0.  hits[k] / total[k] (f64) are bucket k's
  *   decayed counts; a bucket with total 0 has p = 1 (a cold gate keeps the
  *   full draft).
- * Arithmetic.  The decision is taken in fp32 (it only picks an integer),
- *   one rounding per operation, in the order written above: p = hits / total
- *   as an fp64 quotient rounded to fp32; the parameters rounded to fp32 once;
- *   E by running product and sum; cost as (draft_ms + verify_base_ms) +
- *   verify_slope_ms * n; ratio E / cost; margin test against margin *
- *   ratio(K_b); ties go to the smaller n.  The counts stay fp64.
+ * Arithmetic.  The rule above is defined on exact values (p = hits / total,
+ *   the double parameters as given).  The kernel evaluates it in fp32, one
+ *   rounding per operation: p as an fp64 quotient rounded to fp32, the
+ *   parameters rounded to fp32 once, E by running product and sum, cost as
+ *   (draft_ms + verify_base_ms) + verify_slope_ms * n, the ratio E / cost, the
+ *   margin test against margin * ratio(K_b), ties to the smaller n.  Each
+ *   ratio is then within (3n + 6) * 2^-24 of its exact value, so the chosen n
+ *   is the exact rule's except where two compared quantities lie within
+ *   those bounds of each other (near-ties, where either choice is within the
+ *   fp32 evaluation's rounding).  The counts stay fp64.
  */
 #ifndef SV_GATE_H
 #define SV_GATE_H

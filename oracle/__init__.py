@@ -61,7 +61,9 @@ from .draft_gate import (  # noqa: F401
     match_prob,
     round_cost,
     expected_tokens,
-    ratios_f32,
+    gate_ratios,
+    ratio_error_bound,
+    gate_decision,
     gate_length,
     gate_batch,
     update_table,

@@ -22,7 +22,7 @@ a calibration table of P(draft token matches | confidence bucket)
   recorded).  Counts decay by ``decay`` per round before the new ones are
   added.
 
-Readings where the page is silent (stated in the design doc as well):
+Readings where the page is silent:
 
 * Buckets are half-open intervals of the confidence, ``[e_{i-1}, e_i)``, with
   ``e_{-1} = -inf`` and ``e_{NB-1} = +inf``; a NaN confidence falls in bucket 0.
@@ -33,16 +33,23 @@ Readings where the page is silent (stated in the design doc as well):
 * ``min_draft`` floors the post-draft choice (capped at K_b); the pre-draft
   margin skip overrides it.
 
-The decision (E, cost, their ratio, the margin test) is taken in fp32, the
-kernel's precision, since it only decides an integer; p = hits / total is an
-fp64 quotient rounded to fp32, and the calibration counts stay fp64.  Each
-operation rounds once, in the order written here (the GPU kernels follow the
-same order, so results compare bit for bit).
+Arithmetic.  The page fixes no precision, so the decision here is the rule
+itself in exact rational arithmetic: p = hits / total, the costs and the
+margin are the exact values of the (double) parameters, and E, cost and their
+ratio are Fractions.  An implementation that evaluates the ratios in floating
+point can pick another n only where two compared quantities lie within its
+rounding error of each other; ``gate_decision`` reports such near-ties, for
+the fp32 evaluation order of ``ratio_error_bound``.  The calibration counts
+are decayed and added in fp64, one rounding per operation (decay, then add):
+that is the update rule written out in the counts' own type.
 """
 
 from dataclasses import dataclass
+from fractions import Fraction
 
 import numpy as np
+
+F32_UNIT = 2.0 ** -24  # unit roundoff of fp32
 
 
 @dataclass
@@ -72,75 +79,103 @@ def bucket_of(conf, edges):
 
 
 def match_prob(hits, total):
-    """Calibrated P(match) of one bucket; 1 when it has no observations."""
-    h, t = float(hits), float(total)
-    return h / t if t > 0.0 else 1.0
+    """Calibrated P(match) of one bucket, exactly; 1 when it has no observations."""
+    h, t = Fraction(float(hits)), Fraction(float(total))
+    return h / t if t > 0 else Fraction(1)
 
 
 def round_cost(n, prm):
+    """cost(n) in ms, exactly (a Fraction of the double parameters)."""
     if n == 0:
-        return float(prm.plain_ms)
-    return float(prm.draft_ms) + float(prm.verify_base_ms) + float(prm.verify_slope_ms) * float(n)
+        return Fraction(float(prm.plain_ms))
+    return (Fraction(float(prm.draft_ms)) + Fraction(float(prm.verify_base_ms))
+            + Fraction(float(prm.verify_slope_ms)) * n)
 
 
 def expected_tokens(p, n):
-    """E(n) = 1 + sum_{i<n} prod_{j<=i} p_j (running product, running sum)."""
-    e, prod = 1.0, 1.0
+    """E(n) = 1 + sum_{i<n} prod_{j<=i} p_j (running product, running sum);
+    exact when p holds Fractions."""
+    e, prod = Fraction(1), Fraction(1)
     for i in range(n):
-        prod = prod * float(p[i])
+        prod = prod * (p[i] if isinstance(p[i], Fraction) else Fraction(float(p[i])))
         e = e + prod
     return e
 
 
-def ratios_f32(p, k_b, prm):
-    """E(n) / cost(n) for n = 0..k_b as the gate decides them: in fp32 (the
-    kernel's precision), one rounding per operation, E by running product
-    and sum, cost as (draft_ms + verify_base_ms) + verify_slope_ms * n."""
-    f = np.float32
-    fixed = f(f(prm.draft_ms) + f(prm.verify_base_ms))
-    e, prod = f(1.0), f(1.0)
+def gate_ratios(p, k_b, prm):
+    """E(n) / cost(n) for n = 0..k_b, exactly.  A zero cost gives +inf."""
     out = []
-    for n in range(0, k_b + 1):
-        if n > 0:
-            prod = f(prod * f(p[n - 1]))
-            e = f(e + prod)
-        cost = f(prm.plain_ms) if n == 0 else f(fixed + f(f(prm.verify_slope_ms) * f(n)))
-        out.append(f(e / cost))
+    for n in range(k_b + 1):
+        c = round_cost(n, prm)
+        out.append(expected_tokens(p, n) / c if c > 0 else float("inf"))
     return out
 
 
-def gate_length(conf_row, k_b, logit_margin, edges, hits, total, prm):
-    """Number of drafts (0..k_b) one sequence submits."""
+def ratio_error_bound(n):
+    """Relative error bound of E(n)/cost(n) evaluated in fp32 with one rounding
+    per operation: p rounded once (u), n products (2n u over the product of
+    rounded factors), n additions of positive terms into E (n u), cost from
+    fp32-rounded parameters (two inputs and two operations: 4 u), the
+    quotient (u); (3n + 6) u covers the first-order sum with room for the
+    second-order terms."""
+    return (3 * n + 6) * F32_UNIT
+
+
+def _near(a, b, rel):
+    if a == float("inf") or b == float("inf"):
+        return a == b
+    return abs(a - b) <= Fraction(rel) * max(a, b)
+
+
+def gate_decision(conf_row, k_b, logit_margin, edges, hits, total, prm):
+    """(n, near): the number of drafts (0..k_b) one sequence submits, and
+    whether a comparison that decided it was within an fp32 evaluation's error
+    bound (a near-tie, where such an evaluation may pick another n)."""
     if prm.margin_threshold > 0.0 and logit_margin is not None and \
             np.float32(logit_margin) < np.float32(prm.margin_threshold):
-        return 0
-    p = [np.float32(match_prob(hits[bucket_of(c, edges)], total[bucket_of(c, edges)])) for c in conf_row[:k_b]]
-    r = ratios_f32(p, k_b, prm)
+        return 0, False
+    p = [match_prob(hits[bucket_of(c, edges)], total[bucket_of(c, edges)]) for c in conf_row[:k_b]]
+    r = gate_ratios(p, k_b, prm)
     n_lo = min(int(prm.min_draft), k_b)
     best_n = n_lo
     for n in range(n_lo + 1, k_b + 1):
         if r[n] > r[best_n]:
             best_n = n
-    if best_n < k_b and r[best_n] >= np.float32(np.float32(prm.margin) * r[k_b]):
-        return best_n
-    return k_b
+    near = any(_near(r[n], r[best_n], ratio_error_bound(n) + ratio_error_bound(best_n))
+               for n in range(n_lo, k_b + 1) if n != best_n)
+    if best_n == k_b:
+        return k_b, near
+    m = Fraction(float(prm.margin))
+    full = r[k_b] * m if r[k_b] != float("inf") else (float("inf") if m > 0 else float("nan"))
+    near = near or (full == full and _near(r[best_n], full,
+                                           ratio_error_bound(best_n) + ratio_error_bound(k_b) + 2 * F32_UNIT))
+    if full == full and r[best_n] >= full:
+        return best_n, near
+    return k_b, near
 
 
-def gate_batch(conf, k_per_seq, logit_margin, edges, hits, total, prm):
-    """Per-sequence lengths and their exclusive prefix sum ``cu_k[B+1]``.
+def gate_length(conf_row, k_b, logit_margin, edges, hits, total, prm):
+    """Number of drafts (0..k_b) one sequence submits."""
+    return gate_decision(conf_row, k_b, logit_margin, edges, hits, total, prm)[0]
+
+
+def gate_batch(conf, k_per_seq, logit_margin, edges, hits, total, prm, with_near=False):
+    """Per-sequence lengths and their exclusive prefix sum ``cu_k[B+1]``
+    (and, with ``with_near``, the per-sequence near-tie flags).
 
     ``conf`` is ``[B, K]`` (row b holds sequence b's K drafted positions);
     ``k_per_seq[b]`` <= K drafts were made for b (all K when None)."""
     conf = np.asarray(conf)
     B, K = conf.shape
     n = np.zeros(B, dtype=np.int32)
+    near = np.zeros(B, dtype=bool)
     for b in range(B):
         kb = K if k_per_seq is None else int(k_per_seq[b])
         lm = None if logit_margin is None else logit_margin[b]
-        n[b] = gate_length(conf[b], kb, lm, edges, hits, total, prm)
+        n[b], near[b] = gate_decision(conf[b], kb, lm, edges, hits, total, prm)
     cu = np.zeros(B + 1, dtype=np.int32)
     cu[1:] = np.cumsum(n)
-    return n, cu
+    return (n, cu, near) if with_near else (n, cu)
 
 
 def update_table(conf, n_submitted, n_accepted, edges, hits, total, decay):
@@ -165,5 +200,5 @@ def update_table(conf, n_submitted, n_accepted, edges, hits, total, decay):
     return h2, t2
 
 
-__all__ = ["GateParams", "bucket_of", "match_prob", "round_cost", "expected_tokens", "ratios_f32",
-           "gate_length", "gate_batch", "update_table"]
+__all__ = ["GateParams", "bucket_of", "match_prob", "round_cost", "expected_tokens", "gate_ratios",
+           "ratio_error_bound", "gate_decision", "gate_length", "gate_batch", "update_table"]

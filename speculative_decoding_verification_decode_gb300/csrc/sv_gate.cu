@@ -63,7 +63,9 @@ __device__ __forceinline__ int bucket_of(float c, const float* edges, int nb) {
 __device__ __forceinline__ int clamp_i(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
 // The decision runs in fp32 (it only picks an integer; fp64 is a small
-// fraction of fp32's rate on this part), one rounding per operation.
+// fraction of fp32's rate on this part), one rounding per operation: every
+// ratio is within (3n + 6) * 2^-24 of the exact E(n)/cost(n), so the length
+// is the exact rule's wherever no two compared ratios are that close.
 __device__ int gate_one(const GateArgs& a, int kb, float lm, const uint8_t* bk, const float* p) {
   if (a.margin_threshold > 0.f && a.logit_margin && lm < a.margin_threshold) return 0;
   const int n_lo = a.min_draft < kb ? a.min_draft : kb;

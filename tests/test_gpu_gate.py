@@ -1,8 +1,11 @@
 """Draft-length gate on the GPU vs the oracle (PocketLLM dspark.md, the gate).
 
-Lengths, cu_k and the updated calibration counts must be bit-identical:
-both sides take the length decision with the same fp32 operations in the
-same order, and the update's counts are integers tallied before the one fp64
+The oracle takes the length decision in exact rational arithmetic; the
+kernel takes it in fp32.  Lengths must be identical on every sequence the
+oracle does not flag as a near-tie (two compared ratios within the fp32
+evaluation's error bound), and cu_k must be the prefix sum of the kernel's
+lengths (equal to the oracle's when no flagged length differs).  The updated
+calibration counts are bit-identical: integers tallied before the one fp64
 decay-and-add.
 """
 
@@ -67,8 +70,25 @@ def _gpu_gate(conf, hits, total, prm, k_drafted=None, logit_margin=None):
     return g.n_submit.cpu().numpy(), g.cu_k.cpu().numpy()
 
 
+NEAR_SEEN = {"flagged": 0, "differ": 0}
+
+
+def _check_lengths(n_g, cu_g, n_o, cu_o, near, prm=None):
+    """Equal lengths outside the oracle's near-ties; cu_k the kernel's own
+    prefix sum (the oracle's when every length agrees)."""
+    differ = n_g != n_o
+    assert not (differ & ~near).any(), (np.flatnonzero(differ & ~near)[:5], prm)
+    want_cu = np.zeros(n_g.size + 1, dtype=np.int64)
+    want_cu[1:] = np.cumsum(n_g)
+    assert np.array_equal(cu_g, want_cu)
+    if not differ.any():
+        assert np.array_equal(cu_g, cu_o)
+    NEAR_SEEN["flagged"] += int(near.sum())
+    NEAR_SEEN["differ"] += int(differ.sum())
+
+
 @pytest.mark.parametrize("B,K", [(0, 5), (1, 0), (1, 5), (7, 5), (64, 5), (300, 16), (1025, 8), (40, 64)])
-def test_gate_lengths_bit_exact(B, K):
+def test_gate_lengths_match_outside_near_ties(B, K):
     rng = np.random.default_rng(1000 + B * 7 + K)
     for trial in range(3):
         conf, hits, total = _inputs(rng, B, K, cold=(trial == 0))
@@ -76,9 +96,8 @@ def test_gate_lengths_bit_exact(B, K):
         kd = rng.integers(0, K + 1, size=B).astype(np.int32) if trial == 2 else None
         lm = rng.uniform(0, 8, size=B).astype(np.float32) if prm.margin_threshold > 0 else None
         n_g, cu_g = _gpu_gate(conf, hits, total, prm, kd, lm)
-        n_o, cu_o = oracle.gate_batch(conf, kd, lm, EDGES, hits, total, prm)
-        assert np.array_equal(n_g, n_o), (np.flatnonzero(n_g != n_o)[:5], prm)
-        assert np.array_equal(cu_g, cu_o)
+        _check_lengths(n_g, cu_g, *oracle.gate_batch(conf, kd, lm, EDGES, hits, total, prm, with_near=True),
+                       prm)
 
 
 def test_gate_page_defaults():
@@ -89,9 +108,17 @@ def test_gate_page_defaults():
     hits = np.array([4.0, 13.0, 15.8, 17.8, 20.0, 20.0])  # 20 % .. 100 %, the page's table
     conf = np.array([[7.0] * 5, [-1.0] * 5, [2.0, 1.0, 0.0, -1.0, -1.0]], dtype=np.float32)
     n_g, cu_g = _gpu_gate(conf, hits, total, GateParams())
-    n_o, cu_o = oracle.gate_batch(conf, None, None, EDGES, hits, total, GateParams())
+    n_o, cu_o, near = oracle.gate_batch(conf, None, None, EDGES, hits, total, GateParams(), with_near=True)
+    assert not near.any()
     assert np.array_equal(n_g, n_o) and np.array_equal(cu_g, cu_o)
     assert n_g[0] == 5 and n_g[1] == 0
+
+
+def test_gate_near_ties_reported():
+    """How many sequences the oracle flagged as near-ties over the length
+    tests, and how many of them the kernel decided the other way (printed)."""
+    print(f"gate near-ties: {NEAR_SEEN['flagged']} flagged, {NEAR_SEEN['differ']} decided differently")
+    assert NEAR_SEEN["differ"] <= NEAR_SEEN["flagged"]
 
 
 def test_gate_update_bit_exact_over_rounds():

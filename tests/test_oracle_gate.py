@@ -7,6 +7,7 @@ online estimate under censoring.
 """
 
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -30,13 +31,14 @@ def test_cost_matches_the_page():
 @pytest.mark.parametrize("p", [0.0, 0.2, 0.5, 0.678, 0.9, 1.0])
 def test_expected_tokens_closed_form(p):
     prm = GateParams()
-    r32 = oracle.ratios_f32([p] * 8, 8, prm)
+    q = Fraction(p)  # the exact value of the double
+    r = oracle.gate_ratios([q] * 8, 8, prm)
     for n in range(0, 9):
-        closed = float(n + 1) if p == 1.0 else 1.0 + p * (1.0 - p ** n) / (1.0 - p)
-        assert oracle.expected_tokens([p] * n, n) == pytest.approx(closed, rel=1e-14, abs=1e-14)
-        # the gate's fp32 ratio of the same E(n) over cost(n)
-        cost = 303.0 if n == 0 else 196.0 + 300.0 + 109.0 * n
-        assert float(r32[n]) == pytest.approx(closed / cost, rel=3e-6)
+        # geometric series: 1 + q (1 - q^n) / (1 - q), or n + 1 at q = 1
+        closed = Fraction(n + 1) if q == 1 else 1 + q * (1 - q ** n) / (1 - q)
+        assert oracle.expected_tokens([q] * n, n) == closed
+        cost = Fraction(303) if n == 0 else Fraction(196 + 300 + 109 * n)
+        assert r[n] == closed / cost
 
 
 def _brute(p, k_b, prm, logit_margin=None):
@@ -64,16 +66,79 @@ def test_gate_matches_brute_force():
         total = hits + rng.integers(0, 20, size=6)
         conf = rng.normal(1.5, 2.5, size=8).astype(np.float32)
         prm = GateParams(min_draft=int(rng.integers(0, 3)), margin=float(rng.choice([1.0, 1.15, 1.5])))
-        p = [oracle.match_prob(hits[oracle.bucket_of(c, EDGES)], total[oracle.bucket_of(c, EDGES)])
+        p = [float(oracle.match_prob(hits[oracle.bucket_of(c, EDGES)], total[oracle.bucket_of(c, EDGES)]))
              for c in conf[:k_b]]
         got = oracle.gate_length(conf, k_b, None, EDGES, hits, total, prm)
         want = _brute(p, k_b, prm)
-        # the gate decides in fp32: only near-ties (within its rounding) may differ
+        # the brute force's fp64 sums round differently; only exact near-ties may differ
         if got != want:
             e = lambda n: 1.0 + sum(math.prod(p[:i + 1]) for i in range(n))
             c = lambda n: prm.plain_ms if n == 0 else prm.draft_ms + prm.verify_base_ms + prm.verify_slope_ms * n
-            rg, rw, rf = e(got) / c(got), e(want) / c(want), prm.margin * e(k_b) / c(k_b)
-            assert abs(rg - rw) <= 1e-5 * rw or abs(rg - rf) <= 1e-5 * rf or abs(rw - rf) <= 1e-5 * rf
+            assert abs(e(got) / c(got) - e(want) / c(want)) < 1e-12 or \
+                abs(e(got) / c(got) - prm.margin * e(k_b) / c(k_b)) < 1e-12
+
+
+def _fp32_gate(conf_row, k_b, edges, hits, total, prm):
+    """An fp32 evaluation of the gate's rule (one rounding per operation, the
+    order of ratio_error_bound's derivation): a model of a fast evaluation,
+    used to check that the oracle's near-tie flag covers every disagreement."""
+    f = np.float32
+    p = []
+    for c in conf_row[:k_b]:
+        k = oracle.bucket_of(c, edges)
+        p.append(f(hits[k] / total[k]) if total[k] > 0 else f(1.0))
+    fixed = f(f(prm.draft_ms) + f(prm.verify_base_ms))
+    e, prod, r = f(1.0), f(1.0), []
+    for n in range(k_b + 1):
+        if n > 0:
+            prod = f(prod * p[n - 1])
+            e = f(e + prod)
+        cost = f(prm.plain_ms) if n == 0 else f(fixed + f(f(prm.verify_slope_ms) * f(n)))
+        r.append(f(e / cost))
+    n_lo = min(prm.min_draft, k_b)
+    best = n_lo
+    for n in range(n_lo + 1, k_b + 1):
+        if r[n] > r[best]:
+            best = n
+    if best < k_b and r[best] >= f(f(prm.margin) * r[k_b]):
+        return best
+    return k_b
+
+
+def test_near_tie_flag_covers_fp32_disagreements():
+    """Wherever an fp32 evaluation picks another length than the exact rule,
+    the oracle has flagged the sequence as a near-tie; and the flag is rare
+    on random inputs (it marks ties, not ordinary decisions)."""
+    rng = np.random.default_rng(17)
+    flagged = differ = 0
+    n_cases = 3000
+    for trial in range(n_cases):
+        k_b = int(rng.integers(0, 17))
+        total = rng.integers(1, 40, size=6).astype(np.float64)
+        hits = np.minimum(total, rng.integers(0, 40, size=6)).astype(np.float64)
+        if trial % 3 == 0:  # steep tables: near-ties between lengths are common there
+            hits = total.copy()
+            hits[rng.integers(0, 6)] -= 1
+        conf = rng.normal(1.5, 2.5, size=16).astype(np.float32)
+        prm = GateParams(min_draft=int(rng.integers(0, 3)), margin=float(rng.choice([1.0, 1.15, 1.5])),
+                         verify_slope_ms=float(rng.choice([109.0, 0.0, 1e-3])))
+        n, near = oracle.gate_decision(conf, k_b, None, EDGES, hits, total, prm)
+        n32 = _fp32_gate(conf, k_b, EDGES, hits, total, prm)
+        flagged += near
+        if n32 != n:
+            differ += 1
+            assert near, (trial, n, n32)
+    assert differ <= flagged < n_cases // 5, (differ, flagged)
+
+
+def test_exact_ties_are_flagged():
+    # equal costs and no matches: n = 1..5 tie exactly, the rule takes 1
+    prm = GateParams(verify_slope_ms=0.0, plain_ms=1e9, margin=1.0)
+    hits, total = np.zeros(6), np.full(6, 10.0)
+    assert oracle.gate_decision([0.0] * 5, 5, None, EDGES, hits, total, prm) == (1, True)
+    # far from any tie: the page's confident and hopeless drafts
+    assert oracle.gate_decision([7.0] * 5, 5, None, EDGES, hits.copy() + 10, total, GateParams()) == (5, False)
+    assert oracle.gate_decision([0.0] * 5, 5, None, EDGES, hits, total, GateParams()) == (0, False)
 
 
 def test_limits_the_page_states():
@@ -190,18 +255,19 @@ GATE_MUTATIONS = [
      [test_update_records_only_uncensored_positions, test_online_estimate_is_unbiased_under_censoring]),
     ("update_table", "d * float(hits[k]) + float(new_h[k])", "float(hits[k]) + float(new_h[k])",
      [test_update_records_only_uncensored_positions]),
-    ("gate_length", "if r[n] > r[best_n]:", "if r[n] >= r[best_n]:", [test_ties_go_to_smaller_n]),
-    ("gate_length", "r[best_n] >= np.float32(np.float32(prm.margin) * r[k_b])", "r[best_n] >= r[k_b]",
-     [test_margin_between_one_and_its_factor]),
-    ("ratios_f32", "prod = f(prod * f(p[n - 1]))", "prod = f(prod * f(p[0]))",
+    ("gate_decision", "if r[n] > r[best_n]:", "if r[n] >= r[best_n]:", [test_ties_go_to_smaller_n]),
+    ("gate_decision", "full = r[k_b] * m if", "full = r[k_b] if", [test_margin_between_one_and_its_factor]),
+    ("expected_tokens", "prod = prod * (p[i]", "prod = prod * (p[0]",
      [test_gate_matches_brute_force, _closed_form_pin]),
-    ("round_cost", "float(prm.verify_slope_ms) * float(n)", "float(prm.verify_slope_ms) * float(n + 1)",
+    ("round_cost", "Fraction(float(prm.verify_base_ms))", "Fraction(float(prm.verify_slope_ms))",
      [test_cost_matches_the_page]),
-    ("ratios_f32", "f(f(prm.verify_slope_ms) * f(n))", "f(f(prm.verify_slope_ms) * f(n + 1))",
+    ("round_cost", "Fraction(float(prm.verify_slope_ms)) * n", "Fraction(float(prm.verify_slope_ms)) * (n + 1)",
      [_closed_form_pin]),
-    ("match_prob", "if t > 0.0 else 1.0", "if t > 0.0 else 0.0", [test_limits_the_page_states]),
+    ("gate_decision", "ratio_error_bound(n) + ratio_error_bound(best_n))", "0)",
+     [test_exact_ties_are_flagged, test_near_tie_flag_covers_fp32_disagreements]),
+    ("match_prob", "if t > 0 else Fraction(1)", "if t > 0 else Fraction(0)", [test_limits_the_page_states]),
     ("bucket_of", "if c >= float(e):", "if c > float(e):", [test_buckets_are_half_open_and_nan_is_lowest]),
-    ("gate_length", "n_lo = min(int(prm.min_draft), k_b)", "n_lo = 0", [test_min_draft_and_pre_draft_skip]),
+    ("gate_decision", "n_lo = min(int(prm.min_draft), k_b)", "n_lo = 0", [test_min_draft_and_pre_draft_skip]),
 ]
 
 
