@@ -28,6 +28,9 @@ from .spec_verify import (  # noqa: F401
     NEAR_BOUNDARY,
     BAD_LAYOUT,
     NEAR_FILTER,
+    NEAR_DECISION,
+    softmax_weight_tol,
+    softmax_decision_tol,
     BOUNDARY_REL_TOL,
     Result,
     decode_rows,

@@ -31,7 +31,11 @@ Readings of the pages that this file fixes (each restated where it is used):
   target and draft rows become ``softmax(logits / T_b)`` (computed in fp64,
   max-subtracted, then rounded to f32) and the sampling rule runs on those
   rows (llmstudio.ru section 38: p and q are the distributions after the
-  sampling transforms, warped identically).
+  sampling transforms, warped identically).  An implementation that forms
+  the weights ``2^((l - m) log2(e) / T)`` in fp32 with a hardware exp2 of
+  relative error ``e`` can take another accept decision only where the
+  oracle's test is within ``softmax_decision_tol`` of its threshold; such
+  decisions set the oracle-only ``NEAR_DECISION`` bit.
 
 Error conventions (a sequence stops at the first row where one applies):
 ``BAD_LAYOUT`` ragged offsets out of range (n = 0, next = -1);
@@ -57,6 +61,7 @@ ZERO_MASS = 4
 NEAR_BOUNDARY = 8
 BAD_LAYOUT = 64
 NEAR_FILTER = 256  # oracle only: a top-p boundary within the filter tolerance
+NEAR_DECISION = 512  # oracle only: an accept test within the softmax tolerance of its threshold
 
 BOUNDARY_REL_TOL = 1e-5
 
@@ -190,6 +195,35 @@ def inverse_cdf_draw(weights64: np.ndarray, u: float) -> Tuple[int, bool]:
     return idx, bool(near)
 
 
+EX2_REL = 2.0 ** -21  # relative error bound taken for a hardware exp2 (checked by a GPU test)
+F32_U = 2.0 ** -24
+
+
+def softmax_weight_tol(row_max: float, temperature: float) -> float:
+    """Relative error bound of one fp32 weight ``2^((l - m) k)``, k = log2(e)/T,
+    against the exact one, for a row of maximum ``m``: the exp2 (e), the
+    argument formed as ``l k - m k`` with ``m k`` rounded once and k rounded
+    once (at most ``(|m k| + 2 * 126) u`` in the exponent, weights below
+    2^-126 being flushed), and the rounding of the weight (u)."""
+    mk = abs(float(row_max)) * 1.4426950408889634 / float(temperature)
+    return EX2_REL + 0.6931471805599453 * (mk + 2 * 126.0) * F32_U + F32_U
+
+
+def softmax_decision_tol(tol_p: float, tol_q: float) -> float:
+    """Relative band of an accept test ``u qhat(t) < phat(t)`` from weights
+    within ``tol_p`` / ``tol_q`` of exact: phat(t) = w_t / Z moves by at most
+    2 tol_p (weight and mass), qhat(t) by 2 tol_q, plus the oracle's own f32
+    rounding of both probabilities (2 u)."""
+    return 2.0 * tol_p + 2.0 * tol_q + 2.0 * F32_U
+
+
+def _near_decision(u: float, p_t: float, q_t: float, zp_int: int, zq_int: int, tol: float) -> bool:
+    """Whether ``u q(t) Zp`` and ``p(t) Zq`` are within ``tol`` (relative) of each other."""
+    lhs = Fraction(float(np.float32(u))) * Fraction(float(np.float32(q_t))) * zp_int
+    rhs = Fraction(float(np.float32(p_t))) * zq_int
+    return abs(lhs - rhs) <= Fraction(tol) * max(lhs, rhs)
+
+
 def _frac_to_f64(num: int) -> float:
     """Correctly rounded float64 of ``num * 2**-149``."""
     return float(num * _TWO_M149)
@@ -199,39 +233,45 @@ RowGetter = Callable[[int], Tuple[Optional[np.ndarray], int]]
 
 
 def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
-                     u: np.ndarray, k: int, V: int) -> Tuple[int, int, int]:
+                     u: np.ndarray, k: int, V: int,
+                     decision_tol: Optional[Callable[[int], float]] = None) -> Tuple[int, int, int]:
     """One sequence of speculative sampling.  ``get_p(i)`` / ``get_q(i)``
     return ``(f32 row, error_bits)``; a row is fetched only when the
-    left-to-right walk reaches it (llmstudio.ru section 48)."""
+    left-to-right walk reaches it (llmstudio.ru section 48).  With
+    ``decision_tol`` (row -> relative band, for warped rows), a decision
+    within the band of its threshold sets ``NEAR_DECISION``."""
+    flags = 0
     for i in range(k + 1):
         if i < k:
             t = int(tokens[i])
             if not 0 <= t < V:
-                return i, -1, BAD_TOKEN
+                return i, -1, BAD_TOKEN | flags
         p, perr = get_p(i)
         if perr:
-            return i, -1, perr
+            return i, -1, perr | flags
         if i < k:
             q, qerr = get_q(i)
             if qerr:
-                return i, -1, qerr
+                return i, -1, qerr | flags
         if not _uniform_ok(u[i]):
-            return i, -1, BAD_VALUE
+            return i, -1, BAD_VALUE | flags
         zp = exact_mass_int(p)
         if zp == 0:
-            return i, -1, ZERO_MASS
+            return i, -1, ZERO_MASS | flags
         if i == k:
             # all K_b accepted: bonus draw from p_K (card, "Method").
             idx, near = inverse_cdf_draw(p.astype(np.float64) / _frac_to_f64(zp), u[i])
-            return k, idx, NEAR_BOUNDARY if near else 0
+            return k, idx, flags | (NEAR_BOUNDARY if near else 0)
         zq = exact_mass_int(q)
         if zq == 0:
-            return i, -1, ZERO_MASS
+            return i, -1, ZERO_MASS | flags
+        if decision_tol is not None and _near_decision(u[i], p[t], q[t], zp, zq, decision_tol(i)):
+            flags = NEAR_DECISION
         if accept_decision(u[i], p[t], q[t], zp, zq):
             continue
         # first rejection: resample from norm(max(0, phat - qhat)) with u_K.
         if not _uniform_ok(u[k]):
-            return i, -1, BAD_VALUE
+            return i, -1, BAD_VALUE | flags
         phat = p.astype(np.float64) / _frac_to_f64(zp)
         qhat = q.astype(np.float64) / _frac_to_f64(zq)
         resid = np.maximum(0.0, phat - qhat)
@@ -239,7 +279,7 @@ def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
         if not resid.sum() > 0.0:
             resid, status = phat, ZERO_MASS
         idx, near = inverse_cdf_draw(resid, u[k])
-        return i, idx, status | (NEAR_BOUNDARY if near else 0)
+        return i, idx, status | flags | (NEAR_BOUNDARY if near else 0)
     raise AssertionError("unreachable")
 
 
@@ -357,10 +397,13 @@ def accept_from_logits(target: np.ndarray, draft: np.ndarray, dtype: str,
     V = target.shape[1]
     res = _new_result(B)
     near_rows = [False]
+    row_tol = {}
 
-    def getter(rows, start, T, k=None, p=None):
+    def getter(rows, start, T, k=None, p=None, tag="p"):
         def get(i):
             x = decode_rows(rows[start + i], dtype)
+            finite = x[np.isfinite(x)]
+            row_tol[(tag, i)] = softmax_weight_tol(finite.max() if finite.size else 0.0, T)
             if k is not None or p is not None:
                 floor, near, bad = sf.filter_floor(x, T, k, p)
                 if bad:
@@ -390,8 +433,10 @@ def accept_from_logits(target: np.ndarray, draft: np.ndarray, dtype: str,
             fk = None if top_k is None else int(top_k[b])
             fp = None if top_p is None else float(np.float32(top_p[b]))
             near_rows[0] = False
-            n, nxt, st = _accept_sequence(getter(target, t0, T, fk, fp), getter(draft, d0, T, fk, fp),
-                                          tokens[d0:d0 + k], u[t0:t0 + k + 1], k, V)
+            row_tol.clear()
+            n, nxt, st = _accept_sequence(getter(target, t0, T, fk, fp, "p"), getter(draft, d0, T, fk, fp, "q"),
+                                          tokens[d0:d0 + k], u[t0:t0 + k + 1], k, V,
+                                          lambda i: softmax_decision_tol(row_tol[("p", i)], row_tol[("q", i)]))
             if near_rows[0]:
                 st |= NEAR_FILTER
         res.n_accepted[b], res.next_token[b], res.status[b] = n, nxt, st

@@ -8,7 +8,7 @@ import oracle
 import speculative_decoding_verification_decode_gb300 as sv
 
 DEV = torch.device("cuda", 0)
-MASK_COMPARABLE = ~np.uint32(oracle.NEAR_BOUNDARY | sv.SEQ_EXACT_PATH)
+MASK_COMPARABLE = ~np.uint32(oracle.NEAR_BOUNDARY | oracle.NEAR_FILTER | oracle.NEAR_DECISION | sv.SEQ_EXACT_PATH)
 
 
 def to_dev(a, dtype=None):
@@ -80,3 +80,19 @@ def _first_diff(a, b):
         return "equal"
     i = idx[0]
     return f"{idx.size} differences; first at sequence {i}: gpu={a[i]} oracle={b[i]}"
+
+
+def assert_softmax_agreement(gpu, ref, label, mask=None):
+    """Accepted lengths against the oracle's own fp64 softmax: equal on every
+    sequence the oracle does not flag (NEAR_DECISION: an accept test within
+    the fp32 warp's error band of its threshold; NEAR_FILTER: a top-p
+    boundary within the filter tolerance).  Prints the agreement and the
+    flagged count."""
+    sel = np.ones(gpu.n_accepted.shape, bool) if mask is None else np.asarray(mask, bool)
+    flagged = (ref.status & np.uint32(oracle.NEAR_DECISION | oracle.NEAR_FILTER)) > 0
+    same = gpu.n_accepted == ref.n_accepted
+    agree = float(same[sel].mean()) if sel.any() else 1.0
+    print(f"{label}: decisions agree with the oracle's fp64 softmax on {agree:.4f} of sequences "
+          f"({int((flagged & sel).sum())} flagged near a threshold)")
+    bad = sel & ~flagged & ~same
+    assert not bad.any(), _first_diff(np.where(bad, gpu.n_accepted, ref.n_accepted), ref.n_accepted)

@@ -282,7 +282,7 @@ FILTER_MUTATIONS = [
     (sf, "filter_floor", "J = int(np.flatnonzero(above < pz)[-1])",
      "J = int(np.flatnonzero(above < pz)[-1]) + (1 if int(np.flatnonzero(above < pz)[-1]) + 1 < vals.size else 0)",
      [pin_brute_force]),
-    (spv, "accept_from_logits", "getter(draft, d0, T, fk, fp)", "getter(draft, d0, T)", [pin_law]),
+    (spv, "accept_from_logits", "getter(draft, d0, T, fk, fp, \"q\")", "getter(draft, d0, T, tag=\"q\")", [pin_law]),
 ]
 
 
