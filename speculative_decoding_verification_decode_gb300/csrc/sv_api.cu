@@ -128,19 +128,40 @@ bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
   return found;
 }
 
-template <int MODE, typename T>
-sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
-  auto kern = svk::sv_verify_kernel<MODE, T, false>;
-  if constexpr (MODE == svk::MODE_LOGITS) {
-    if (prm.flo_t || prm.flo_d) kern = svk::sv_verify_kernel<MODE, T, true>;
+// Per device and kernel: the largest dynamic shared memory opted in so far,
+// whether the non-portable cluster size is allowed, and the cluster sizes
+// (with their shared memory) already checked to fit.  The attribute and
+// occupancy queries run once per combination instead of on every call.
+struct KernelCache {
+  size_t smem_set;
+  bool cluster16;
+  unsigned fits_mask;       // bit c: clusters of c CTAs checked at smem_fit[c]
+  size_t smem_fit[svk::kMaxCluster + 1];
+};
+
+template <int MODE, typename T, bool FL>
+KernelCache& kernel_cache(int dev) {
+  static KernelCache cache[64] = {};
+  return cache[dev >= 0 && dev < 64 ? dev : 0];
+}
+
+template <int MODE, typename T, bool FL>
+sv_status launch_k(svk::Params prm, const Plan& pl, cudaStream_t stream) {
+  auto kern = svk::sv_verify_kernel<MODE, T, FL>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  KernelCache& kc = kernel_cache<MODE, T, FL>(dev);
+  cudaError_t e;
+  if (kc.smem_set < pl.smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+    if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(smem): %s", cudaGetErrorString(e));
+    kc.smem_set = pl.smem;
   }
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(smem): %s", cudaGetErrorString(e));
-  if (pl.C > 8) {
+  if (pl.C > 8 && !kc.cluster16) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess)
       return fail(SV_ERR_CUDA, "cudaFuncSetAttribute(cluster): %s", cudaGetErrorString(e));
+    kc.cluster16 = true;
   }
   prm.slice = pl.slice;
   prm.slot_bytes = pl.slot_bytes;
@@ -162,14 +183,27 @@ sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-  if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
-  if (clusters < 1)
-    return fail(SV_ERR_UNSUPPORTED, "no cluster of %d CTAs with %zu B shared memory fits", pl.C, pl.smem);
+  const unsigned bit = 1u << pl.C;
+  if (!(kc.fits_mask & bit) || kc.smem_fit[pl.C] < pl.smem) {
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return fail(SV_ERR_CUDA, "cudaOccupancyMaxActiveClusters: %s", cudaGetErrorString(e));
+    if (clusters < 1)
+      return fail(SV_ERR_UNSUPPORTED, "no cluster of %d CTAs with %zu B shared memory fits", pl.C, pl.smem);
+    kc.fits_mask |= bit;
+    kc.smem_fit[pl.C] = pl.smem;
+  }
   e = cudaLaunchKernelEx(&cfg, kern, prm);
   if (e != cudaSuccess) return fail(SV_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   return SV_OK;
+}
+
+template <int MODE, typename T>
+sv_status launch(svk::Params prm, const Plan& pl, cudaStream_t stream) {
+  if constexpr (MODE == svk::MODE_LOGITS) {
+    if (prm.flo_t || prm.flo_d) return launch_k<MODE, T, true>(prm, pl, stream);
+  }
+  return launch_k<MODE, T, false>(prm, pl, stream);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -362,10 +362,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         else if (round > 0) mbar_wait_bounded(&sm.full[s], (round - 1) & 1u);
       }
     }
-    return;
-  }
-
-  if (warp == kDecideWarp && !sampling) return;  // greedy rows are decided by consumer warp 0
+  } else if (warp != kDecideWarp || sampling) {  // greedy rows are decided by consumer warp 0
 
   // ================================================================ consumers (and the decision warp)
   // The last consumer warp fetches every row's decision inputs (draft token,
@@ -1221,6 +1218,15 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
 
   if (abort && tid == 0) finish(0, -1, ST_TIMEOUT);
   if (tid == 0) sm.stop = 1;  // the producer stops issuing and drains its copies
+  }  // consumers and decision warp
+
+  // Peers push records into this CTA's shared memory.  On the normal path
+  // every CTA takes part in the same exchanges, but a CTA whose wait gave up
+  // must not exit while a slower peer may still push into it: every thread
+  // of the cluster meets here once (every wait above is bounded, so each
+  // one arrives) before any CTA of the cluster exits.
+  __syncwarp();
+  cluster_sync_all();
 }
 
 }  // namespace svk
