@@ -34,20 +34,38 @@ def _stale():
 
 
 def build(force=False, verbose=False):
-    """Compile the library if it is missing or older than its sources."""
+    """Compile the library if it is missing or older than its sources: one
+    nvcc process per translation unit in parallel, then one link."""
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
+    nvcc = nvcc_path()
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(LIB_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+        cmd = [nvcc, *NVCC_FLAGS[:-1], "-c", "-o", obj, src]  # no -shared for the objects
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)))
+    logs = []
+    failed = []
+    for src, pr in procs:
+        out, err = pr.communicate()
+        logs.append(out + err)
+        if pr.returncode != 0:
+            failed.append(f"{src}:\n{out}{err}")
+    if failed:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
     tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc_path(), *NVCC_FLAGS, "-o", tmp, *SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
+    res = subprocess.run([nvcc, *NVCC_FLAGS, "-o", tmp, *objs], capture_output=True, text=True)
     if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+        raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
     os.replace(tmp, LIB_PATH)
+    for obj in objs:
+        os.remove(obj)
     if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(logs) + res.stdout + res.stderr)
     return LIB_PATH
 
 
