@@ -29,6 +29,9 @@ from .spec_verify import (  # noqa: F401
     BAD_LAYOUT,
     NEAR_FILTER,
     NEAR_DECISION,
+    DRAW_CERTIFIED,
+    TIGHT_BONUS_REL,
+    TIGHT_BONUS_MAX_V,
     softmax_weight_tol,
     softmax_decision_tol,
     BOUNDARY_REL_TOL,

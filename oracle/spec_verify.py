@@ -62,8 +62,17 @@ NEAR_BOUNDARY = 8
 BAD_LAYOUT = 64
 NEAR_FILTER = 256  # oracle only: a top-p boundary within the filter tolerance
 NEAR_DECISION = 512  # oracle only: an accept test within the softmax tolerance of its threshold
+DRAW_CERTIFIED = 2048  # oracle only: a bonus draw whose id holds within TIGHT_BONUS_REL (below)
 
 BOUNDARY_REL_TOL = 1e-5
+# A bonus draw from f32 probability rows, normalised by any mass Z' (the
+# common factor Z/Z' cancels in the normalised CDF), weighted with one f32
+# rounding per element (relative u = 2^-24) and floored to 64-bit fixed point
+# with a total near 2^(62 - bitlen V): every normalised CDF value moves by at
+# most 2u + 2^(2 bitlen V - 61), below 2^-21 for V <= 2^18.  A uniform
+# farther than that from every step therefore names the same id.
+TIGHT_BONUS_REL = 2.0 ** -21
+TIGHT_BONUS_MAX_V = 1 << 18
 
 _TWO_M149 = Fraction(1, 1 << 149)
 
@@ -180,10 +189,10 @@ def accept_decision(u: float, p_t: float, q_t: float, zp_int: int, zq_int: int) 
     return lhs < rhs
 
 
-def inverse_cdf_draw(weights64: np.ndarray, u: float) -> Tuple[int, bool]:
+def inverse_cdf_draw(weights64: np.ndarray, u: float, tol: float = BOUNDARY_REL_TOL) -> Tuple[int, bool]:
     """``min{v : C_v > u * R}`` over fp64 running sums ``C`` of ``weights64``,
-    ``R = C[-1]``; also whether ``u * R`` is within ``1e-5 * R`` of a CDF
-    step (a boundary case)."""
+    ``R = C[-1]``; also whether ``u * R`` is within ``tol * R`` (default
+    ``1e-5 * R``) of a CDF step (a boundary case)."""
     c = np.cumsum(np.asarray(weights64, np.float64))
     total = float(c[-1])
     tau = float(np.float32(u)) * total
@@ -191,7 +200,7 @@ def inverse_cdf_draw(weights64: np.ndarray, u: float) -> Tuple[int, bool]:
     idx = min(idx, len(c) - 1)
     lo = float(c[idx - 1]) if idx > 0 else 0.0
     hi = float(c[idx])
-    near = min(abs(tau - lo), abs(hi - tau)) <= BOUNDARY_REL_TOL * total
+    near = min(abs(tau - lo), abs(hi - tau)) <= tol * total
     return idx, bool(near)
 
 
@@ -234,12 +243,15 @@ RowGetter = Callable[[int], Tuple[Optional[np.ndarray], int]]
 
 def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
                      u: np.ndarray, k: int, V: int,
-                     decision_tol: Optional[Callable[[int], float]] = None) -> Tuple[int, int, int]:
+                     decision_tol: Optional[Callable[[int], float]] = None,
+                     certify_bonus: bool = False) -> Tuple[int, int, int]:
     """One sequence of speculative sampling.  ``get_p(i)`` / ``get_q(i)``
     return ``(f32 row, error_bits)``; a row is fetched only when the
     left-to-right walk reaches it (llmstudio.ru section 48).  With
     ``decision_tol`` (row -> relative band, for warped rows), a decision
-    within the band of its threshold sets ``NEAR_DECISION``."""
+    within the band of its threshold sets ``NEAR_DECISION``.  With
+    ``certify_bonus`` (probability rows given as they are), a bonus draw
+    farther than ``TIGHT_BONUS_REL`` from every step sets ``DRAW_CERTIFIED``."""
     flags = 0
     for i in range(k + 1):
         if i < k:
@@ -260,7 +272,10 @@ def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
             return i, -1, ZERO_MASS | flags
         if i == k:
             # all K_b accepted: bonus draw from p_K (card, "Method").
-            idx, near = inverse_cdf_draw(p.astype(np.float64) / _frac_to_f64(zp), u[i])
+            w = p.astype(np.float64) / _frac_to_f64(zp)
+            idx, near = inverse_cdf_draw(w, u[i])
+            if certify_bonus and V <= TIGHT_BONUS_MAX_V and not inverse_cdf_draw(w, u[i], TIGHT_BONUS_REL)[1]:
+                flags |= DRAW_CERTIFIED
             return k, idx, flags | (NEAR_BOUNDARY if near else 0)
         zq = exact_mass_int(q)
         if zq == 0:
@@ -346,7 +361,7 @@ def accept(p: np.ndarray, q: np.ndarray, tokens: np.ndarray, u: np.ndarray, B: i
             continue
         k, t0, d0 = lay
         n, nxt, st = _accept_sequence(getter(p, t0), getter(q, d0), tokens[d0:d0 + k],
-                                      u[t0:t0 + k + 1], k, V)
+                                      u[t0:t0 + k + 1], k, V, certify_bonus=True)
         res.n_accepted[b], res.next_token[b], res.status[b] = n, nxt, st
     return res
 

@@ -45,7 +45,7 @@ def simulate_rounds(p, q, rounds, seed):
     P = np.tile(p, (rounds, 1))
     Q = np.tile(q, (rounds, 1))
     res = o.accept(P, Q, tok.reshape(-1), u.reshape(-1), rounds, K)
-    assert (res.status & ~np.uint32(o.NEAR_BOUNDARY)).max() == 0
+    assert (res.status & ~np.uint32(o.NEAR_BOUNDARY | o.DRAW_CERTIFIED)).max() == 0
     return res.n_accepted
 
 

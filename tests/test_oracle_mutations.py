@@ -26,8 +26,10 @@ MUTATIONS = [
      ["pin_s18_acceptance_and_residual"]),
     ("_accept_sequence", "inverse_cdf_draw(resid, u[k])", "inverse_cdf_draw(resid, u[i])",
      ["pin_enumeration_marginal_equals_target"]),
-    ("_accept_sequence", "p.astype(np.float64) / _frac_to_f64(zp), u[i]",
-     "p.astype(np.float64)[::-1] / _frac_to_f64(zp), u[i]", ["pin_enumeration_bonus_law"]),
+    ("_accept_sequence", "w = p.astype(np.float64) / _frac_to_f64(zp)",
+     "w = p.astype(np.float64)[::-1] / _frac_to_f64(zp)", ["pin_enumeration_bonus_law"]),
+    ("_accept_sequence", "inverse_cdf_draw(w, u[i], TIGHT_BONUS_REL)", "inverse_cdf_draw(w, u[i], 2.0 ** -30)",
+     ["pin_certified_bonus_draws"]),
     ("_greedy_sequence", "return i, a, status\n", "return i, (a + 1) % V, status\n",
      ["pin_greedy_reproduces_plain_decoding"]),
     ("argmax_lowest", "int(cand[0])", "int(cand[-1])",

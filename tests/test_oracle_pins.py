@@ -360,6 +360,59 @@ def pin_inverse_cdf_closed_form():
     assert o.inverse_cdf_draw(w, 0.5)[1] is False
 
 
+def _fixed_point_bonus_draw(p, u, z_rel, signs):
+    """A bonus draw as an fp32 implementation with 64-bit fixed point may take
+    it: normalise by a mass off by ``z_rel`` (relative), perturb each weight
+    by one rounding (``signs`` in {-1, 0, 1} times 2^-24, relative), floor to
+    fixed point with a total near 2^(62 - bitlen V), and search the integer
+    CDF for floor(u R).  Exact rationals throughout."""
+    V = len(p)
+    S = 62 - V.bit_length()
+    z = sum(Fraction(float(x)) for x in p) * (1 + Fraction(z_rel))
+    w = [math.floor(Fraction(float(x)) / z * (1 + int(sg) * Fraction(1, 1 << 24)) * (1 << S))
+         for x, sg in zip(p, signs)]
+    R = sum(w)
+    tau = math.floor(Fraction(float(np.float32(u))) * R)
+    c = 0
+    for j, x in enumerate(w):
+        c += x
+        if c > tau:
+            return j
+    raise AssertionError("unreachable")
+
+
+def pin_certified_bonus_draws():
+    """DRAW_CERTIFIED is sound: a certified bonus draw names the same id under
+    every perturbation its error model allows (any normaliser, one rounding
+    per weight in either direction, the fixed-point floor), and a draw that a
+    one-rounding perturbation does move is not certified."""
+    rng = np.random.default_rng(21)
+    certified = 0
+    for trial in range(60):
+        V = int(rng.integers(2, 200))
+        p = (rng.random(V) ** 3).astype(F32)
+        u = np.float32(int(rng.integers(0, 1 << 24)) * 2.0 ** -24)
+        res = o.accept(p[None], np.zeros((0, V), F32), np.zeros(0, np.int32), np.array([u], F32), 1, 0)
+        if not res.status[0] & o.DRAW_CERTIFIED:
+            continue
+        certified += 1
+        cdf = np.cumsum(p.astype(np.float64))
+        j = int(res.next_token[0])
+        for signs in (np.ones(V), -np.ones(V), np.where(np.arange(V) <= j, 1, -1),
+                      np.where(np.arange(V) <= j, -1, 1), rng.integers(-1, 2, V)):
+            for z_rel in (0.0, 1e-3, -1e-3):
+                assert _fixed_point_bonus_draw(p, u, z_rel, signs) == j, (trial, cdf[j] / cdf[-1])
+    assert certified >= 50  # the flag is not vacuous: most uniforms are far from a step
+    # F_0 = 1 / (2 - 2^-24) lies 2^-26 above u = 0.5: lowering weight 0 and
+    # raising weight 1 by one rounding each moves the draw from 0 to 1
+    p = np.array([1.0, 1.0 - 2.0 ** -24], F32)
+    res = o.accept(p[None], np.zeros((0, 2), F32), np.zeros(0, np.int32), np.array([0.5], F32), 1, 0)
+    assert res.next_token[0] == 0
+    assert _fixed_point_bonus_draw(p, 0.5, 0.0, np.array([-1, 1])) == 1
+    assert not res.status[0] & o.DRAW_CERTIFIED
+    assert res.status[0] & o.NEAR_BOUNDARY
+
+
 # ------------------------------------------------------------------ logits
 
 def pin_softmax_closed_form():
