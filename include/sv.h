@@ -81,6 +81,13 @@ typedef enum {
 /* Flags (bit OR) accepted by every entry point. */
 #define SV_FLAG_FORCE_EXACT 1u   /* decide every accept test on exact masses
                                     (testing aid; same results, slower) */
+#define SV_FLAG_EXPIRE_EXCHANGE 2u /* testing aid: every wait for the records
+                                    of the sequence's cluster gives up at once,
+                                    as a wait on a stalled peer would, so each
+                                    sequence that exchanges ends with
+                                    SV_SEQ_TIMEOUT, n = 0, next_token = -1; the
+                                    kernel still drains its own copies and
+                                    returns normally */
 
 /*
  * Greedy verification (temperature 0).
@@ -152,6 +159,25 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
                                 int32_t vocab, int32_t* n_accepted, int32_t* next_token,
                                 uint32_t* status, float* warped_target_out,
                                 float* warped_draft_out, uint32_t flags, void* stream);
+
+/*
+ * Bytes of device workspace a verification call of this size needs.  The
+ * verification calls take no workspace: a sequence's per-row partials (masses,
+ * maxima, argmax candidates, draw totals) are combined inside its thread-block
+ * cluster through distributed shared memory, so no scratch survives in global
+ * memory.  The query exists so that a caller written against a workspace
+ * interface sizes nothing; it returns 0 for every argument.
+ *   batch  B (>= 0), k  the largest K_b, vocab  V,
+ *   mode   SV_MODE_GREEDY (sv_verify_greedy), SV_MODE_PROBS (sv_accept) or
+ *          SV_MODE_LOGITS (sv_accept_from_logits).
+ * spec-verify model card, section "API": the verification calls of the card
+ * take rows and tokens only; a batched library of this kind commonly asks the
+ * caller for scratch, and this one needs none.
+ */
+#define SV_MODE_GREEDY 0
+#define SV_MODE_PROBS 1
+#define SV_MODE_LOGITS 2
+size_t sv_workspace_size(int32_t batch, int32_t k, int32_t vocab, int32_t mode);
 
 /* Static string for a status code. */
 const char* sv_status_string(sv_status s);

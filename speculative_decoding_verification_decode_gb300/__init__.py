@@ -7,6 +7,7 @@ PyTorch binding.  See the spec-verify model card, sections "Method" and
 """
 
 from ._lib import (  # noqa: F401
+    FLAG_EXPIRE_EXCHANGE,
     FLAG_FORCE_EXACT,
     SEQ_BAD_LAYOUT,
     SEQ_BAD_TOKEN,

@@ -13,10 +13,12 @@ SV_OK, SV_ERR_ARG, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3
 SEQ_BAD_TOKEN, SEQ_BAD_VALUE, SEQ_ZERO_MASS, SEQ_NEAR_BOUNDARY = 1, 2, 4, 8
 SEQ_EXACT_PATH, SEQ_TIMEOUT, SEQ_BAD_LAYOUT = 16, 32, 64
 FLAG_FORCE_EXACT = 1
+FLAG_EXPIRE_EXCHANGE = 2  # testing aid: exchange waits give up at once (SV_SEQ_TIMEOUT)
 
 _vp = ctypes.c_void_p
 _i32, _i64, _u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
 _f64 = ctypes.c_double
+SV_MODE_GREEDY, SV_MODE_PROBS, SV_MODE_LOGITS = 0, 1, 2
 
 
 class GateParams(ctypes.Structure):
@@ -34,6 +36,7 @@ SIGNATURES = {
                          _vp, _vp, _vp, _u32, _vp]),
     "sv_accept_from_logits": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
                                      _i32, _i32, _vp, _vp, _vp, _vp, _vp, _u32, _vp]),
+    "sv_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32, _i32]),
     "sv_sampler_floors": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp]),
     "sv_accept_from_logits_floored": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,

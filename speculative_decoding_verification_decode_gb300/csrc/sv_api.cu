@@ -223,7 +223,8 @@ sv_status check_common(const void* target, int64_t row_stride, const int32_t* to
                 static_cast<long long>(B) * K, sum_k);
   if (static_cast<long long>(sum_k) + B > 0x7FFFFFFFLL)
     return fail(SV_ERR_ARG, "too many rows (sum_k + batch > 2^31 - 1)");
-  if (flags & ~static_cast<uint32_t>(SV_FLAG_FORCE_EXACT)) return fail(SV_ERR_ARG, "unknown flag bits 0x%x", flags);
+  if (flags & ~static_cast<uint32_t>(SV_FLAG_FORCE_EXACT | SV_FLAG_EXPIRE_EXCHANGE))
+    return fail(SV_ERR_ARG, "unknown flag bits 0x%x", flags);
   if (B == 0) return SV_OK;
   if (!target) return fail(SV_ERR_ARG, "target pointer is NULL");
   if (sum_k > 0 && !tokens) return fail(SV_ERR_ARG, "draft_tokens is NULL");
@@ -366,6 +367,14 @@ sv_status sv_accept_from_logits_floored(const void* target_logits, const void* d
   return accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
                        uniforms, cu_k, batch, k, sum_k, vocab, floor_target, floor_draft, n_accepted,
                        next_token, status, warped_target_out, warped_draft_out, flags, stream);
+}
+
+size_t sv_workspace_size(int32_t batch, int32_t k, int32_t vocab, int32_t mode) {
+  (void)batch;
+  (void)k;
+  (void)vocab;
+  (void)mode;
+  return 0;  // partials are exchanged through distributed shared memory
 }
 
 const char* sv_status_string(sv_status s) {

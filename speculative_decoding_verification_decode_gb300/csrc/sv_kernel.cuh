@@ -58,6 +58,7 @@ constexpr int threads_of(int mode) { return mode == MODE_GREEDY ? kThreads - 32 
 constexpr uint32_t ST_BAD_TOKEN = 1u, ST_BAD_VALUE = 2u, ST_ZERO_MASS = 4u, ST_NEAR = 8u,
                    ST_EXACT = 16u, ST_TIMEOUT = 32u, ST_BAD_LAYOUT = 64u;
 constexpr uint32_t FLAG_FORCE_EXACT = 1u;
+constexpr uint32_t FLAG_EXPIRE_EXCHANGE = 2u;  // exchange waits give up without polling (tests)
 
 constexpr double kU32 = 5.9604644775390625e-8;  // 2^-24, unit roundoff of f32
 // Relative error bound used for ex2.approx.ftz.f32 (normal results); the

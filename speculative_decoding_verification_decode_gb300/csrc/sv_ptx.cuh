@@ -106,8 +106,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait_cluster(bar, parity)) return true;
   return false;
 }

@@ -432,7 +432,8 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
         dsmem_st_v4(dst + 4u * w, *reinterpret_cast<const uint4*>(&sm.myrec[w]));
       dsmem_arrive_release(dsmem_addr(&sm.xbar[slot], static_cast<uint32_t>(lane)));
     }
-    const bool ok = mbar_wait_cluster_bounded(&sm.xbar[slot], par);
+    const bool ok =
+        mbar_wait_cluster_bounded(&sm.xbar[slot], par, (P.flags & FLAG_EXPIRE_EXCHANGE) ? 0u : kWaitPolls);
     return __all_sync(0xFFFFFFFFu, ok) != 0;
   };
   auto rec = [&](uint32_t c, int w) -> uint32_t { return sm.recs[last_slot][c][w]; };

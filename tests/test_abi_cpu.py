@@ -58,6 +58,18 @@ def test_greedy_argument_errors(lib, kw, frag):
 
 def test_empty_batch_is_a_noop(lib):
     assert greedy(lib, B=0, sum_k=0, target=NULL, tok=NULL, n=NULL, nxt=NULL, st=NULL) == _lib.SV_OK
+    # both testing flags pass the host checks
+    for f in (_lib.FLAG_FORCE_EXACT, _lib.FLAG_EXPIRE_EXCHANGE, _lib.FLAG_FORCE_EXACT | _lib.FLAG_EXPIRE_EXCHANGE):
+        assert greedy(lib, B=0, sum_k=0, target=NULL, tok=NULL, n=NULL, nxt=NULL, st=NULL, flags=f) == _lib.SV_OK
+
+
+def test_workspace_size_is_zero(lib):
+    """The verification calls need no scratch in global memory (partials stay
+    in the cluster's distributed shared memory): the query answers 0 for the
+    benchmark shapes of every mode, and for degenerate ones."""
+    for mode in (_lib.SV_MODE_GREEDY, _lib.SV_MODE_PROBS, _lib.SV_MODE_LOGITS):
+        for B, K, V in ((64, 5, 128256), (256, 4, 152064), (1, 4, 32000), (0, 0, 1), (1024, 16, 262144)):
+            assert lib.sv_workspace_size(B, K, V, mode) == 0
 
 
 def test_accept_argument_errors(lib):
