@@ -23,6 +23,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -38,6 +39,10 @@ CONFIG_TEXT = {
     "config5": "B=1024 K=3 V=32000 f16 logits, half greedy / half sampled",
     "filter": "config 2 rows (B=64 K=5 V=128256 bf16 logits, T=0.8) with top-k 50 and top-p 0.9 "
               "on every sequence: floors kernel, then floored verification",
+    "greedy2": "B=64 K=5 V=128256 bf16 logits, greedy (each draft token the argmax of its bf16 "
+               "draft row)",
+    "latency1": "B=1 K=4 V=32000 f32 probabilities, rejection sampling: one B=1 call per round "
+                "(the 600 rounds of config 1 in turn)",
 }
 FILTER_TOP_K, FILTER_TOP_P = 50, 0.9
 KERNEL_NAMES = {
@@ -47,6 +52,8 @@ KERNEL_NAMES = {
     "config4": "sv_verify_kernel<1, float, false>",
     "config5": "sv_verify_kernel<2, __half, false>",
     "filter": "floors_kernel<__nv_bfloat16>",
+    "greedy2": "sv_verify_kernel<0, __nv_bfloat16, false>",
+    "latency1": "sv_verify_kernel<1, float, false>",
 }
 METRIC = "verified rows/s and achieved HBM GB/s vs GB300 peak at B=64 K=5 V=128256"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_config2_traffic.md")
@@ -125,13 +132,21 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, path=None):
+        """Samples `index`'s clocks every 100 ms into `path` (a temporary
+        file, removed after reading, when None)."""
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.keep = path is not None
+        if path is None:
+            fd, path = tempfile.mkstemp(prefix=f"sv_clocks_{index}_", suffix=".csv")
+            os.close(fd)
+        self.path = path
+        self.lines = []
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        if os.path.dirname(self.path):
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -151,12 +166,19 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            with open(self.path) as fh:
+                self.lines = fh.readlines()
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
 
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        for line in open(self.path):
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -230,8 +252,9 @@ def make_workload(name, seed_shift=0):
     """A named workload; 'filter' is config 2 with top-k 50 and top-p 0.9 on
     every sequence (the sampler filters before verification)."""
     import workloads
-    base = "config2" if name == "filter" else name
-    base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5}[base]
+    base = {"filter": "config2", "latency1": "config1"}.get(name, name)
+    base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5,
+                 "greedy2": 6}[base]
     wl = workloads.make_config(base, seed=workloads.configs.SEED_BASE + base_seed + seed_shift)
     if name == "filter":
         wl.top_k = np.full(wl.B, FILTER_TOP_K, np.int32)
@@ -244,6 +267,10 @@ def algorithmic_bytes(wl, n_acc):
     draft rows 0..min(n_b, K_b - 1) of every sampled sequence (the resident
     row pair serves the residual / bonus scan, so nothing is read twice);
     target rows 0..n_b of greedy sequences."""
+    return int(algorithmic_bytes_per_seq(wl, n_acc).sum())
+
+
+def algorithmic_bytes_per_seq(wl, n_acc):
     kb = wl.k_per_seq
     n = n_acc.astype(np.int64)
     t_rows = n + 1
@@ -253,7 +280,7 @@ def algorithmic_bytes(wl, n_acc):
         d_rows = np.minimum(n + 1, kb)
         if wl.temperature is not None:
             d_rows = np.where(wl.temperature > 0, d_rows, 0)
-    return int((t_rows + d_rows).sum()) * wl.V * wl.elem_size
+    return (t_rows + d_rows) * wl.V * wl.elem_size
 
 
 def oracle_rows_per_s(wl, budget_s=20.0):
@@ -290,11 +317,70 @@ def oracle_rows_per_s(wl, budget_s=20.0):
 
 # ------------------------------------------------------------------ arms
 
+def round_view(x, wl, r):
+    """Inputs of round r of a batch of independent B=1 rounds (views, no copy)."""
+    K = wl.K
+    out = dict(x)
+    out["target"] = x["target"][r * (K + 1):(r + 1) * (K + 1)]
+    out["draft"] = x["draft"][r * K:(r + 1) * K]
+    out["tokens"] = x["tokens"][r * K:(r + 1) * K]
+    out["uniforms"] = x["uniforms"][r * (K + 1):(r + 1) * (K + 1)]
+    return out
+
+
+def timed_steps(torch, stream, steps, flush, step_fn):
+    """Device time of each step (CUDA events on the launching stream), the
+    L2 flushed before each one."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        step_fn(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def mode_summary(torch, sv, dev, stream, flush, name, steps, warmup, peak):
+    """One more workload timed the same way (device time, L2 flushed between
+    steps): its per-round time and bandwidth, for the main line's `modes`."""
+    wl = make_workload(name)
+    x = device_inputs(wl, torch, dev)
+    if name == "latency1":
+        n_acc = call(sv, wl, x).n_accepted.cpu().numpy()
+        per_seq = algorithmic_bytes_per_seq(wl, n_acc)
+        for i in range(warmup):
+            call(sv, wl, round_view(x, wl, i % wl.B))
+        ms = timed_steps(torch, stream, steps, flush, lambda i: call(sv, wl, round_view(x, wl, i % wl.B)))
+        greedy_ms = timed_steps(torch, stream, steps, flush, lambda i: sv.verify_greedy(
+            round_view(x, wl, i % wl.B)["target"], round_view(x, wl, i % wl.B)["tokens"]))
+        t = float(np.mean(ms))
+        alg = float(np.mean([per_seq[i % wl.B] for i in range(steps)]))
+        return {"workload": CONFIG_TEXT[name], "us_per_round_sampled": t * 1e3,
+                "us_per_round_greedy": float(np.mean(greedy_ms)) * 1e3,
+                "rows_per_s_sampled": (wl.K + 1) / (t * 1e-3),
+                "algorithmic_gbs_sampled": alg / (t * 1e-3) / 1e9,
+                "rounds": f"{steps} rounds, each one B=1 call"}
+    for _ in range(warmup):
+        r = call(sv, wl, x)
+    torch.cuda.synchronize()
+    n_acc = r.n_accepted.cpu().numpy()
+    t = float(np.mean(timed_steps(torch, stream, steps, flush, lambda i: call(sv, wl, x))))
+    alg = algorithmic_bytes(wl, n_acc)
+    formula = wl.formula_bytes()
+    return {"workload": CONFIG_TEXT[name], "us_per_round": t * 1e3,
+            "rows_per_s": int((wl.k_per_seq + 1).sum()) / (t * 1e-3),
+            "mean_accepted": float(n_acc.mean()),
+            "formula_gbs": formula / (t * 1e-3) / 1e9, "formula_frac": formula / (t * 1e-3) / 1e9 / peak,
+            "algorithmic_gbs": alg / (t * 1e-3) / 1e9, "algorithmic_frac": alg / (t * 1e-3) / 1e9 / peak,
+            "kernel": KERNEL_NAMES[name]}
+
+
 def run_gpu(args):
     import torch
 
     import speculative_decoding_verification_decode_gb300 as sv
-    import workloads
     from speculative_decoding_verification_decode_gb300._build import build
 
     rank, world, local = dist_info()
@@ -307,7 +393,10 @@ def run_gpu(args):
     # every rank verifies its own batch (independent sequences: weak scaling)
     wl = make_workload(args.config, seed_shift=rank * 1000)
     x = device_inputs(wl, torch, dev)
-    rows_per_step = int((wl.k_per_seq + 1).sum())
+    per_round = args.config == "latency1"  # one B=1 call per step
+    step_x = (lambda i: round_view(x, wl, i % wl.B)) if per_round else (lambda i: x)
+    rows_per_step = wl.K + 1 if per_round else int((wl.k_per_seq + 1).sum())
+    seqs_per_step = 1 if per_round else wl.B
     stream = torch.cuda.current_stream(dev)
 
     flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -317,67 +406,66 @@ def run_gpu(args):
         flush_w.fill_(1)
         flush_r.sum()
 
-    for _ in range(args.warmup):
+    n_acc = call(sv, wl, x).n_accepted.cpu().numpy()  # every sequence (round) once
+    for i in range(args.warmup):
         flush()
-        r = call(sv, wl, x)
+        call(sv, wl, step_x(i))
     torch.cuda.synchronize(dev)
-    n_acc = r.n_accepted.cpu().numpy()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush()
-            starts[i].record(stream)
-            call(sv, wl, x)
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+    with ClockSampler(local, args.clocks_csv) as clocks:
+        per_step_ms = timed_steps(torch, stream, args.steps, flush, lambda i: call(sv, wl, step_x(i)))
     barrier(dist, dev)
-    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(per_step_ms))
     ms = max_over_ranks(ms_local, dist, dev)
     floors_ms = None
     if args.config == "filter":  # the floors kernel alone (the roofline's kernel)
-        for i in range(args.steps):
-            flush()
-            starts[i].record(stream)
-            floors(sv, wl, x)
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-        floors_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+        floors_ms = float(np.mean(timed_steps(torch, stream, args.steps, flush, lambda i: floors(sv, wl, x))))
 
     # end to end through the public API with pinned host buffers
     hx = host_inputs(wl, torch)
-    h2d = sum(t.numel() * t.element_size() for t in hx.values() if t is not None)
-    d2h = 3 * wl.B * 4
-    for _ in range(2):
-        call(sv, wl, hx)
+    step_hx = (lambda i: round_view(hx, wl, i % wl.B)) if per_round else (lambda i: hx)
+    h2d = sum(t.numel() * t.element_size() for t in step_hx(0).values() if t is not None)
+    d2h = 3 * seqs_per_step * 4
+    for i in range(2):
+        call(sv, wl, step_hx(i))
     torch.cuda.synchronize(dev)
     e_s = torch.cuda.Event(enable_timing=True)
     e_e = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 20))
     barrier(dist, dev)
     e_s.record(stream)
-    for _ in range(e2e_steps):
-        rr = call(sv, wl, hx)
+    for i in range(e2e_steps):
+        rr = call(sv, wl, step_hx(i))
     e_e.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
-    assert np.array_equal(rr.n_accepted.numpy(), n_acc)
+    last = (e2e_steps - 1) % wl.B if per_round else None
+    assert np.array_equal(rr.n_accepted.numpy(), n_acc[last:last + 1] if per_round else n_acc)
 
     result = None
     if rank == 0:
         peak, peak_kind = measured_peak_gbs()
-        alg = algorithmic_bytes(wl, n_acc)
-        formula = wl.formula_bytes()
+        if per_round:
+            per_seq = algorithmic_bytes_per_seq(wl, n_acc)
+            alg = float(np.mean([per_seq[i % wl.B] for i in range(args.steps)]))
+            formula = wl.formula_bytes() / wl.B
+        else:
+            alg = algorithmic_bytes(wl, n_acc)
+            formula = wl.formula_bytes()
         achieved = alg / (ms_local * 1e-3) / 1e9
         if floors_ms is not None:  # the floors read every row once: the formula bytes
             achieved = formula / (floors_ms * 1e-3) / 1e9
         traffic = profiled_traffic() if args.config == "config2" else None
         value = world * rows_per_step / (ms * 1e-3)
         cpu_val, cpu_seq, cpu_dt = oracle_rows_per_s(wl, budget_s=args.cpu_budget)
+        modes = None
+        if args.config == "config2" and not args.no_modes:
+            # the other mode at the same shape, and config 1 as single-sequence
+            # rounds, each measured the same way after the main line
+            modes = {name: mode_summary(torch, sv, dev, stream, flush, name, args.steps, args.warmup, peak)
+                     for name in ("greedy2", "latency1")}
         result = {
             "metric": METRIC,
             "value": value,
@@ -393,10 +481,10 @@ def run_gpu(args):
             "data": "synthetic (seeded Philox; shapes and distributions of the workload)",
             "config": {
                 "workload": f"{args.config}: {CONFIG_TEXT[args.config]}",
-                "B": wl.B, "K": wl.K, "V": wl.V, "input_dtype": wl.dtype,
+                "B": 1 if per_round else wl.B, "K": wl.K, "V": wl.V, "input_dtype": wl.dtype,
                 "rows_per_step": rows_per_step,
-                "rounds_per_s": world * wl.B / (ms * 1e-3),
-                "us_per_round": ms * 1e3,
+                "rounds_per_s": world * seqs_per_step / (ms * 1e-3),
+                "us_per_round": ms * 1e3 / seqs_per_step,
                 "mean_accepted": float(n_acc.mean()),
                 "formula_bytes_per_step": formula,
                 "formula_gbs": formula / (ms * 1e-3) / 1e9,
@@ -434,6 +522,8 @@ def run_gpu(args):
             "gpu_launches": args.steps * (2 if args.config == "filter" else 1),
             "clocks": clocks.summary(),
         }
+        if modes is not None:
+            result["modes"] = modes
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -713,7 +803,8 @@ def run_reference(args):
             per_step.append((v, nseq, dt))
     value = float(np.mean([v for v, _, _ in per_step]))
     nseq = per_step[-1][1]
-    ms = float(np.mean([dt / n for _, n, dt in per_step])) * wl.B * 1e3
+    seqs_per_step = 1 if args.config == "latency1" else wl.B  # latency1: a step is one B=1 round
+    ms = float(np.mean([dt / n for _, n, dt in per_step])) * seqs_per_step * 1e3
     result = {
         "impl": "reference",
         "metric": METRIC,
@@ -728,8 +819,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded Philox; shapes and distributions of the workload)",
-        "config": {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "B": wl.B, "K": wl.K,
-                   "V": wl.V, "input_dtype": wl.dtype},
+        "config": {"workload": f"{args.config}: {CONFIG_TEXT[args.config]}", "B": seqs_per_step,
+                   "K": wl.K, "V": wl.V, "input_dtype": wl.dtype},
         "cpu_baseline": {"value": value, "unit": "verified rows/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step: the first {nseq} of {wl.B} sequences "
                                    f"(bounded to {args.ref_step_budget:.0f} s of CPU work)"},
@@ -751,6 +842,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline field")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the SM clock samples of the timed region in this file")
+    ap.add_argument("--no-modes", action="store_true",
+                    help="config2 only: skip the greedy and single-sequence summaries")
     ap.add_argument("--ref-step-budget", type=float, default=6.0,
                     help="seconds of oracle work per step of the reference arm")
     args = ap.parse_args(argv)

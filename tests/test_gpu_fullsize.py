@@ -46,6 +46,37 @@ def test_config3_full_greedy():
     H().compare(H().run_gpu(wl), H().run_oracle(wl), exact_tokens=True)
 
 
+def test_greedy2_full_bf16_logits():
+    """Greedy at B=64, K=5, V=128256 on bf16 logits (the sampling workload's
+    shape): every accepted length and emitted token bit-exact."""
+    wl = workloads.make_config("greedy2")
+    H().compare(H().run_gpu(wl), H().run_oracle(wl), exact_tokens=True)
+
+
+def test_config1_rounds_as_single_calls():
+    """Config 1 as the benchmark's per-round latency line runs it: one B=1
+    call per round (sampled, then greedy on the same rows); each equals the
+    oracle on that round alone."""
+    wl = workloads.make_config("config1", rounds=40)
+    x = [H().to_dev(a) for a in (wl.target, wl.draft, wl.tokens, wl.uniforms)]
+    import speculative_decoding_verification_decode_gb300 as sv
+    K = wl.K
+    n_s, t_s, n_g, t_g = [], [], [], []
+    for r in range(wl.B):
+        tg, dr = x[0][r * (K + 1):(r + 1) * (K + 1)], x[1][r * K:(r + 1) * K]
+        tok, u = x[2][r * K:(r + 1) * K], x[3][r * (K + 1):(r + 1) * (K + 1)]
+        a = sv.accept(tg, dr, tok, u)
+        g = sv.verify_greedy(tg, tok)
+        n_s.append(int(a.n_accepted[0])); t_s.append(int(a.next_token[0]))
+        n_g.append(int(g.n_accepted[0])); t_g.append(int(g.next_token[0]))
+    ref_s = H().run_oracle(wl, "accept")
+    ref_g = H().run_oracle(wl, "greedy")
+    assert n_s == ref_s.n_accepted.tolist()
+    near = (ref_s.status & oracle.NEAR_BOUNDARY) > 0
+    assert ((np.array(t_s) == ref_s.next_token) | near).all()
+    assert n_g == ref_g.n_accepted.tolist() and t_g == ref_g.next_token.tolist()
+
+
 def test_config4_full_ragged():
     wl = workloads.make_config("config4")  # B=32, K_b ~ U{0..8}, V=129280
     near, diff = H().compare(H().run_gpu(wl), H().run_oracle(wl))

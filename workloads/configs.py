@@ -29,7 +29,7 @@ from typing import Optional
 
 import numpy as np
 
-CONFIG_NAMES = ("config1", "config2", "config3", "config4", "config5")
+CONFIG_NAMES = ("config1", "config2", "config3", "config4", "config5", "greedy2")
 SEED_BASE = 0x5EED0000
 
 _ROW_BLOCK = 64  # rows synthesised per block, to bound host memory
@@ -194,12 +194,14 @@ def config1_probs(seed: int = SEED_BASE + 1, rounds: int = 600, K: int = 4,
 def config2_bf16_logits(seed: int = SEED_BASE + 2, B: int = 64, K: int = 5,
                         V: int = 128256, temperature: float = 0.8,
                         logit_std: float = 3.0, n_peaks: int = 20,
-                        peak_boost: float = 8.0, draft_noise: float = 1.5) -> Workload:
+                        peak_boost: float = 8.0, draft_noise: float = 1.5,
+                        draft_choice: str = "sample") -> Workload:
     """Sampling from bf16 logits with a fused temperature-0.8 softmax.
 
     Target logits N(0, 3^2) with 20 random "peak" ids per row raised by +8;
     draft logits = target + N(0, 1.5^2); both rounded to bf16.  Draft tokens
-    are drawn from softmax(draft_bf16 / T).
+    are drawn from softmax(draft_bf16 / T) (``draft_choice="argmax"``: the
+    argmax of the bf16 draft row instead).
     """
     rng = _rng(seed)
     kb = np.full(B, K, np.int64)
@@ -219,8 +221,11 @@ def config2_bf16_logits(seed: int = SEED_BASE + 2, B: int = 64, K: int = 5,
             dl = tl[:K] + np.float32(draft_noise) * rng.standard_normal((K, V), dtype=np.float32)
             dbits = f32_to_bf16_bits(dl)
             draft[d0[b]:d0[b] + K] = dbits
-            q = _softmax_rows(_bf16_bits_to_f32(dbits), 1.0 / temperature)
-            tokens[d0[b]:d0[b] + K] = _draw_from_rows(rng, q)
+            if draft_choice == "argmax":
+                tokens[d0[b]:d0[b] + K] = np.argmax(_bf16_bits_to_f32(dbits), axis=-1)
+            else:
+                q = _softmax_rows(_bf16_bits_to_f32(dbits), 1.0 / temperature)
+                tokens[d0[b]:d0[b] + K] = _draw_from_rows(rng, q)
     u = uniforms_24bit(rng, n_t)
     temp = np.full(B, temperature, np.float32)
     return Workload("config2", "logits", "bf16", B, K, V, target, draft, tokens, u,
@@ -353,12 +358,27 @@ def config5_mixed_f16_logits(seed: int = SEED_BASE + 5, B: int = 1024, K: int = 
                     None, temp, {"draft_sigma": sig, "seed": seed})
 
 
+# ---------------------------------------------------------------- greedy at B=64 K=5 V=128256
+
+def greedy2_bf16_logits(seed: int = SEED_BASE + 6, B: int = 64, K: int = 5, V: int = 128256,
+                        **kw) -> Workload:
+    """Greedy verification at the sampling workload's shape: bf16 target
+    logits N(0, 3^2) with 20 peaks per row raised by +8, and each draft token
+    the argmax of its bf16 draft row (target + N(0, 1.5^2)), the drafter's own
+    greedy choice.  Only the target rows are kept: greedy verification reads
+    no draft row."""
+    wl = config2_bf16_logits(seed=seed, B=B, K=K, V=V, draft_choice="argmax", **kw)
+    return Workload("greedy2", "greedy", "bf16", B, K, V, wl.target, None, wl.tokens, None,
+                    None, None, {"seed": seed})
+
+
 _BUILDERS = {
     "config1": config1_probs,
     "config2": config2_bf16_logits,
     "config3": config3_greedy_probs,
     "config4": config4_ragged_probs,
     "config5": config5_mixed_f16_logits,
+    "greedy2": greedy2_bf16_logits,
 }
 
 
