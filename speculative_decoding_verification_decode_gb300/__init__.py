@@ -20,12 +20,16 @@ from ._lib import (  # noqa: F401
 )
 from .api import (  # noqa: F401
     GateResult,
+    LMHeadResult,
     SVError,
     VerifyResult,
     accept,
     accept_from_logits,
     gate_draft_lengths,
     gate_update,
+    lm_head_logits,
+    lm_head_verify,
+    lm_head_workspace,
     sampler_floors,
     verify_greedy,
 )

@@ -308,3 +308,86 @@ def gate_update(confidence: torch.Tensor, n_submitted: torch.Tensor, n_accepted:
         _check(lib.sv_gate_update(_p(conf), _p(ns), _p(na), _p(e), _p(hits), _p(total), hits.numel(), B, K,
                                   float(decay), stream))
 
+
+
+# ---------------------------------------------------------------- LM head in front of verification
+
+def _bf16_rows(x: torch.Tensor, m: "_Marshal") -> torch.Tensor:
+    x = m.dev(x)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("states and projection must be bfloat16")
+    return x.reshape(-1, x.shape[-1]).contiguous()
+
+
+def lm_head_logits(states: torch.Tensor, proj: torch.Tensor, out: Optional[torch.Tensor] = None,
+                   err: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """``states [rows, d] . proj[V, d]^T`` in fp32 on the tensor cores
+    (include/sv_lm_head.h).  ``out``: optional f32 ``[rows, >= V]`` device
+    tensor with unit stride along V; ``err``: optional int32 ``[1]`` device
+    word that receives bit 0 if a device wait gave up."""
+    m = _Marshal(states)
+    h = _bf16_rows(states, m)
+    w = _bf16_rows(proj, m)
+    if h.shape[1] != w.shape[1]:
+        raise ValueError("states and projection must have the same last dimension")
+    rows, V = h.shape[0], w.shape[0]
+    if out is None:
+        out = torch.empty(rows, (V + 3) // 4 * 4, dtype=torch.float32, device=m.device)[:, :V]
+    lib = _lib.load()
+    with torch.cuda.device(m.device):
+        _check(lib.sv_lm_head_logits(_p(h), _p(w), rows, V, h.shape[1], _p(out), out.stride(0), _p(err),
+                                     m.stream()))
+    return out.cpu() if m.host else out
+
+
+class LMHeadResult(NamedTuple):
+    n_accepted: torch.Tensor
+    next_token: torch.Tensor
+    status: torch.Tensor
+    target_logits: Optional[torch.Tensor]  # f32 [target rows, V] the verification read (views of the workspace)
+    draft_logits: Optional[torch.Tensor]
+
+
+def lm_head_workspace(batch: int, sum_k: int, vocab: int, device=None) -> torch.Tensor:
+    """A workspace for sv_lm_head_verify of this size (uninitialised bytes)."""
+    n = int(_lib.load().sv_lm_head_workspace_size(batch, sum_k, vocab))
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda", torch.cuda.current_device()))
+
+
+def lm_head_verify(target_states: torch.Tensor, draft_states: torch.Tensor, proj: torch.Tensor,
+                   temperature: torch.Tensor, draft_tokens: torch.Tensor, uniforms: torch.Tensor,
+                   cu_k: Optional[torch.Tensor] = None, k: Optional[int] = None, flags: int = 0,
+                   workspace: Optional[torch.Tensor] = None) -> LMHeadResult:
+    """Verification from hidden states (include/sv_lm_head.h): the target and
+    draft positions' logits through the one bf16 projection ``proj [V, d]``,
+    then the mixed greedy / sampled verification of accept_from_logits.
+    Returns the verification results and, for device inputs, the fp32 logits
+    it read (views of the workspace, valid until it is reused)."""
+    m = _Marshal(target_states)
+    ht = _bf16_rows(target_states, m)
+    hd = _bf16_rows(draft_states, m)
+    w = _bf16_rows(proj, m)
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    u = m.dev(uniforms.reshape(-1), torch.float32)
+    T = m.dev(temperature.reshape(-1), torch.float32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(ht.shape[0], tok, cu, k)
+    V, d = w.shape
+    if ht.shape[1] != d or (hd.numel() and hd.shape[1] != d):
+        raise ValueError("states and projection must have the same last dimension")
+    lib = _lib.load()
+    need = int(lib.sv_lm_head_workspace_size(B, sum_k, V))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = lm_head_workspace(B, sum_k, V, m.device)
+    n, nxt, st = m.outputs(B)
+    with torch.cuda.device(m.device):
+        _check(lib.sv_lm_head_verify(_p(ht), _p(hd), _p(w), d, _p(T), _p(tok), _p(u), _p(cu), B, K, sum_k, V,
+                                     _p(n), _p(nxt), _p(st), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), flags, m.stream()))
+    res = m.finish(VerifyResult(n, nxt, st))
+    lt = ld = None
+    if not m.host:
+        ldv = (V + 3) // 4 * 4
+        f = workspace[256:256 + (2 * sum_k + B) * ldv * 4].view(torch.float32).view(-1, ldv)
+        lt, ld = f[:sum_k + B, :V], f[sum_k + B:, :V]
+    return LMHeadResult(res.n_accepted, res.next_token, res.status, lt, ld)

@@ -303,15 +303,15 @@ sv_status sv_accept(const float* target_probs, const float* draft_probs, int64_t
   return launch<svk::MODE_PROBS, float>(p, pl, static_cast<cudaStream_t>(stream));
 }
 
-namespace {
+}  // extern "C"
 
-sv_status accept_logits(const void* target_logits, const void* draft_logits, sv_dtype dtype,
-                        int64_t row_stride, const float* temperature, const int32_t* draft_tokens,
-                        const float* uniforms, const int32_t* cu_k, int32_t batch, int32_t k,
-                        int32_t sum_k, int32_t vocab, const float* floor_target,
-                        const float* floor_draft, int32_t* n_accepted, int32_t* next_token,
-                        uint32_t* status, float* warped_target_out, float* warped_draft_out,
-                        uint32_t flags, void* stream) {
+sv_status svh::accept_logits(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                             int64_t row_stride, const float* temperature, const int32_t* draft_tokens,
+                             const float* uniforms, const int32_t* cu_k, int32_t batch, int32_t k,
+                             int32_t sum_k, int32_t vocab, const float* floor_target,
+                             const float* floor_draft, int32_t* n_accepted, int32_t* next_token,
+                             uint32_t* status, float* warped_target_out, float* warped_draft_out,
+                             const uint32_t* ext_err, uint32_t flags, void* stream) {
   sv_status s = check_common(target_logits, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
                              n_accepted, next_token, status, flags);
   if (s != SV_OK || batch == 0) return s;
@@ -331,6 +331,7 @@ sv_status accept_logits(const void* target_logits, const void* draft_logits, sv_
   p.wd_out = warped_draft_out;
   p.flo_t = floor_target;
   p.flo_d = floor_draft;
+  p.ext_err = ext_err;
   p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
               (row_stride * elem) % 16 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -341,7 +342,7 @@ sv_status accept_logits(const void* target_logits, const void* draft_logits, sv_
   }
 }
 
-}  // namespace
+extern "C" {
 
 sv_status sv_accept_from_logits(const void* target_logits, const void* draft_logits,
                                 sv_dtype dtype, int64_t row_stride, const float* temperature,
@@ -350,9 +351,10 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
                                 int32_t vocab, int32_t* n_accepted, int32_t* next_token,
                                 uint32_t* status, float* warped_target_out,
                                 float* warped_draft_out, uint32_t flags, void* stream) {
-  return accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
-                       uniforms, cu_k, batch, k, sum_k, vocab, nullptr, nullptr, n_accepted,
-                       next_token, status, warped_target_out, warped_draft_out, flags, stream);
+  return svh::accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
+                            uniforms, cu_k, batch, k, sum_k, vocab, nullptr, nullptr, n_accepted,
+                            next_token, status, warped_target_out, warped_draft_out, nullptr, flags,
+                            stream);
 }
 
 sv_status sv_accept_from_logits_floored(const void* target_logits, const void* draft_logits,
@@ -364,9 +366,10 @@ sv_status sv_accept_from_logits_floored(const void* target_logits, const void* d
                                         int32_t* next_token, uint32_t* status,
                                         float* warped_target_out, float* warped_draft_out,
                                         uint32_t flags, void* stream) {
-  return accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
-                       uniforms, cu_k, batch, k, sum_k, vocab, floor_target, floor_draft, n_accepted,
-                       next_token, status, warped_target_out, warped_draft_out, flags, stream);
+  return svh::accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens,
+                            uniforms, cu_k, batch, k, sum_k, vocab, floor_target, floor_draft, n_accepted,
+                            next_token, status, warped_target_out, warped_draft_out, nullptr, flags,
+                            stream);
 }
 
 size_t sv_workspace_size(int32_t batch, int32_t k, int32_t vocab, int32_t mode) {

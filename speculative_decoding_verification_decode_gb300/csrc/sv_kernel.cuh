@@ -82,6 +82,7 @@ struct Params {
   float* wd_out;
   const float* flo_t;  // per-row floors of the sampler filters (NULL: none)
   const float* flo_d;
+  const unsigned* ext_err;  // nonzero word: the kernel that wrote the rows gave up (NULL: none)
   unsigned flags;
   int slice;       // elements per CTA slice (multiple of the vector width)
   int slot_bytes;  // bytes per ring slot (multiple of 16)

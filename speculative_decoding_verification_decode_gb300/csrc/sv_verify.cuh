@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     if (rank == 0 && tid == 0) {
       P.n_out[b] = 0;
       P.next_out[b] = -1;
-      P.st_out[b] = layout_ok ? ST_BAD_VALUE : ST_BAD_LAYOUT;
+      P.st_out[b] = (layout_ok ? ST_BAD_VALUE : ST_BAD_LAYOUT) | (P.ext_err && *P.ext_err ? ST_TIMEOUT : 0u);
     }
     return;
   }
@@ -448,6 +448,11 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
     sm.myrec[w + 1] = static_cast<uint32_t>(v >> 32);
   };
   auto finish = [&](int n, int nxt, uint32_t s) {  // thread 0 of the writing CTA
+    if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
+      n = 0;
+      nxt = -1;
+      s |= ST_TIMEOUT;
+    }
     P.n_out[b] = n;
     P.next_out[b] = nxt;
     P.st_out[b] = s;

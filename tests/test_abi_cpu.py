@@ -195,3 +195,25 @@ def test_floors_binding_checks_row_counts_before_any_device_work():
     with pytest.raises(ValueError, match="cu_k needs"):
         sampler_floors(torch.zeros(5, 8), torch.zeros(2, 8), T, None, torch.full((4,), 0.9),
                        torch.tensor([0, 1, 2, 3, 4], dtype=torch.int32), k=1, sum_k=4)
+
+
+def test_lm_head_host_checks(lib):
+    """Host-side argument checks of the LM head (nothing is launched)."""
+    P = 1 << 12
+    assert lib.sv_lm_head_logits(P, P, 4, 100, 12, P, 100, NULL, NULL) == _lib.SV_ERR_ARG  # dim % 8
+    assert b"dim" in lib.sv_last_error()
+    assert lib.sv_lm_head_logits(P, P, 4, 100, 64, P, 98, NULL, NULL) == _lib.SV_ERR_ARG  # ld < vocab
+    assert lib.sv_lm_head_logits(P, P, 4, 100, 64, P, 102, NULL, NULL) == _lib.SV_ERR_ARG  # ld % 4
+    assert lib.sv_lm_head_logits(P + 8, P, 4, 100, 64, P, 100, NULL, NULL) == _lib.SV_ERR_ARG  # alignment
+    assert lib.sv_lm_head_logits(P, P, 0, 100, 64, P, 100, NULL, NULL) == _lib.SV_OK  # nothing to do
+    # workspace: 256 flag bytes, then (2 sum_k + B) rows of ceil4(V) floats
+    assert lib.sv_lm_head_workspace_size(64, 320, 128256) == 256 + 704 * 128256 * 4
+    assert lib.sv_lm_head_workspace_size(3, 6, 1001) == 256 + 15 * 1004 * 4
+    need = lib.sv_lm_head_workspace_size(2, 6, 100)
+    args = [P, P, P, 64, P, P, P, NULL, 2, 3, 6, 100, P, P, P]
+    assert lib.sv_lm_head_verify(*args, P, need - 4, 0, NULL) == _lib.SV_ERR_ARG
+    assert b"workspace_bytes" in lib.sv_last_error()
+    assert lib.sv_lm_head_verify(*args, P, need, 8, NULL) == _lib.SV_ERR_ARG  # unknown flag
+    assert lib.sv_lm_head_verify(*args, P + 8, need, 0, NULL) == _lib.SV_ERR_ARG  # workspace alignment
+    assert lib.sv_lm_head_verify(P, P, P, 64, P, P, P, NULL, 2, 3, 5, 100, P, P, P, P, need, 0,
+                                 NULL) == _lib.SV_ERR_ARG  # sum_k != B * K without cu_k
