@@ -702,6 +702,161 @@ class _TableModel:
         return self.torch.stack([self.next_logits(tokens, lengths + j) for j in range(k + 1)], dim=1)
 
 
+LMHEAD_TEXT = ("verification from hidden states: B=64 K=5 V=128256 d=4096, bf16 states and projection, "
+               "T=0.8 rejection sampling; logits = H W^T on the tensor cores, then the logits verification")
+
+
+def measured_peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_lmhead(args):
+    """One step = the LM head over every verified position (target and draft
+    states) and the verification of those logits (a memset and two launches).
+    The product dominates: it is reported against the tensor-core peak."""
+    import torch
+
+    import speculative_decoding_verification_decode_gb300 as sv
+    from speculative_decoding_verification_decode_gb300._build import build
+    from workloads.lm_head import make_lm_head
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    build()
+    sv.load_library()
+    wl = make_lm_head(seed=0x5EED0007 + 1000 * rank)
+    B, K, V, d = wl.B, wl.K, wl.V, wl.d
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    ht, hd, w = bf(wl.h_target), bf(wl.h_draft), bf(wl.w)
+    T = torch.from_numpy(wl.temperature).to(dev)
+    tok = torch.from_numpy(wl.tokens).to(dev)
+    u = torch.from_numpy(wl.uniforms).to(dev)
+    ws = sv.lm_head_workspace(B, B * K, V, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    step = lambda i: sv.lm_head_verify(ht, hd, w, T, tok, u, workspace=ws)
+    for i in range(args.warmup):
+        flush()
+        r = step(i)
+    torch.cuda.synchronize(dev)
+    n_acc = r.n_accepted.cpu().numpy()
+    barrier(dist, dev)
+    with ClockSampler(local, args.clocks_csv) as clocks:
+        per_step = timed_steps(torch, stream, args.steps, flush, step)
+    barrier(dist, dev)
+    ms_local = float(np.mean(per_step))
+    ms = max_over_ranks(ms_local, dist, dev)
+    # the product alone (the roofline's kernel) over the same 704 rows, into
+    # the same workspace rows (target rows and draft rows are contiguous there)
+    ldv = (V + 3) // 4 * 4
+    rows = B * (2 * K + 1)
+    hall = torch.cat([ht, hd])
+    lall = ws[256:256 + rows * ldv * 4].view(torch.float32).view(-1, ldv)[:, :V]
+    prod_ms = float(np.mean(timed_steps(torch, stream, args.steps, flush,
+                                        lambda i: sv.lm_head_logits(hall, w, out=lall))))
+    # end to end: states, tokens, uniforms and temperatures from pinned host
+    # memory (the projection is a resident weight), results back
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    hth = pin(wl.h_target.view(np.int16)).view(torch.bfloat16)
+    hdh = pin(wl.h_draft.view(np.int16)).view(torch.bfloat16)
+    Th, tokh, uh = pin(wl.temperature), pin(wl.tokens), pin(wl.uniforms)
+    h2d = sum(x.numel() * x.element_size() for x in (hth, hdh, Th, tokh, uh))
+    for _ in range(2):
+        sv.lm_head_verify(hth, hdh, w, Th, tokh, uh, workspace=ws)
+    torch.cuda.synchronize(dev)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        rr = sv.lm_head_verify(hth, hdh, w, Th, tokh, uh, workspace=ws)
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dist, dev)
+    assert np.array_equal(rr.n_accepted.numpy(), n_acc)
+    result = None
+    if rank == 0:
+        import oracle
+        burst, sustained, kind = measured_peak_tflops()
+        flops = 2.0 * rows * V * d
+        achieved = flops / (prod_ms * 1e-3) / 1e12
+        t0 = time.perf_counter()
+        oracle.accept_lm_head(wl.h_target[:K + 1], wl.h_draft[:K], wl.w, "bf16", wl.temperature[:1],
+                              wl.tokens[:K], wl.uniforms[:K + 1], 1, K)
+        cpu_dt = time.perf_counter() - t0
+        result = {
+            "metric": METRIC,
+            "value": world * B * (K + 1) / (ms * 1e-3),
+            "unit": "verified rows/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded Philox states and projection, random-init)",
+            "config": {
+                "workload": f"lmhead: {LMHEAD_TEXT}",
+                "B": B, "K": K, "V": V, "d": d,
+                "us_per_round": ms * 1e3,
+                "rounds_per_s": world * B / (ms * 1e-3),
+                "mean_accepted": float(n_acc.mean()),
+                "product_us": prod_ms * 1e3,
+                "verify_us": (ms_local - prod_ms) * 1e3,
+                "product_flops_per_step": flops,
+                "l2": "flushed between timed steps (512 MB write, then a 512 MB read)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "roofline": {
+                "bound": "tensor",
+                "kernel": "svl::lm_head_kernel",
+                "achieved": achieved,
+                "peak": sustained,
+                "peak_kind": f"{kind} (MEASURED_PEAKS.json bf16_tflops_sustained; burst {burst})",
+                "unit": "TFLOP/s",
+                "frac": achieved / sustained,
+                "frac_of_burst": achieved / burst,
+                "traffic": None,
+            },
+            "cpu_baseline": {
+                "value": (K + 1) / cpu_dt,
+                "unit": "verified rows/s",
+                "cores": 1,
+                "kind": "oracle",
+                "sample": f"one sequence of the same workload ({cpu_dt:.1f} s, fp64 numpy products "
+                          "then the Python verification)",
+            },
+            "e2e": {
+                "value": world * B * (K + 1) / (e2e_ms * 1e-3),
+                "unit": "verified rows/s",
+                "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 3 * B * 4,
+                "ms_per_step": e2e_ms,
+            },
+            "gpu_launches": args.steps * 2,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
 def run_decoder(args):
     """One step = one speculative decoding round of the whole batch, replayed
     from a CUDA graph; the metric counts committed tokens."""
@@ -836,7 +991,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT) + ["gate", "decoder"],
+    ap.add_argument("--config", default="config2", choices=list(CONFIG_TEXT) + ["gate", "decoder", "lmhead"],
                     help="a verification workload, 'gate' for the draft-length gate, or 'decoder' "
                          "for whole speculative decoding rounds")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -857,6 +1012,12 @@ def main(argv=None):
                               "oracle verifies single steps"}), flush=True)
             return None
         return run_decoder(args)
+    if args.config == "lmhead":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the LM head's reference is the oracle's "
+                              "fp64 product; its time is the lmhead line's cpu_baseline"}), flush=True)
+            return None
+        return run_lmhead(args)
     if args.config == "gate":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the gate's reference is the oracle; "

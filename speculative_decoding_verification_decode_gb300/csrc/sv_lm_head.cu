@@ -3,17 +3,20 @@
 // it (llmstudio.ru, "Как работает speculative decoding и MTP при инференсе
 // LLM", sections 21-22).
 //
-// One CTA per 128 x 256 tile of logits, six warps:
-//   warps 0-3  epilogue: wait for the accumulator, read it out of tensor
-//              memory (warp w owns TMEM lanes 32w..32w+31, the tile's rows)
-//              and store it as fp32 rows;
-//   warp 4     producer: TMA loads of the H (128 x 64) and W (256 x 64) tiles
-//              of every K step into a 4-stage ring, 128-byte swizzled;
-//   warp 5     allocates 256 TMEM columns, one thread issues the MMAs
-//              (M = 128, N = 256, K = 16, bf16 x bf16 -> fp32) and commits
-//              each stage back to the producer, then frees TMEM.
-// The grid walks the M tiles of one N tile together (blockIdx.x), so the
-// CTAs that share a W tile run at the same time and read it once from HBM.
+// Work units of 256 x 256 logits (two 128-row slabs of states against one
+// 256-row projection tile); one persistent CTA per SM, six warps:
+//   warps 0-3  epilogue: wait for a unit's accumulators, read them out of
+//              tensor memory (warp w owns TMEM lanes 32w..32w+31, the slabs'
+//              rows), store them as fp32 rows and hand them back;
+//   warp 4     producer: TMA loads of the two H slabs (128 x 64 each) and the
+//              W tile (256 x 64) of every K step into a 3-stage ring,
+//              128-byte swizzled;
+//   warp 5     allocates 2 x 256 TMEM columns (one accumulator per slab), one
+//              thread issues the MMAs (M = 128, N = 256, K = 16, bf16 x bf16
+//              -> fp32) and commits each stage back to the producer, then
+//              frees TMEM.
+// Consecutive units share their W tile (all slab pairs of one W tile first),
+// so the CTAs working on a W tile at the same time read it once from HBM.
 // Every mbarrier wait is bounded; a wait that gives up sets bit 0 of *err.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -32,12 +35,12 @@ using svk::mbar_init;
 using svk::mbar_wait_bounded;
 using svk::smem_u32;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB: one 128-row slab of states
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB: 256 projection rows
+constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // two slabs share the projection tile
 constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;  // the fp32 accumulator: 128 lanes x 256 columns
+constexpr uint32_t TMEM_COLS = 256;  // one fp32 accumulator: 128 lanes x 256 columns
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5), A and B
 // bf16 (bits 7-9, 10-12), both K-major (bits 15, 16 clear), N / 8 (bits
@@ -99,25 +102,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 struct __align__(8) Bars {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t acc;
+  uint64_t full[STAGES];   // producer -> MMA: the stage's tiles landed
+  uint64_t empty[STAGES];  // MMA -> producer: the stage's MMAs have read it
+  uint64_t acc_full;       // MMA -> epilogue: both accumulators are final
+  uint64_t acc_empty;      // epilogue -> MMA: both accumulators were read out
   uint32_t tmem;
+  volatile int abort;      // a wait gave up: every role skips its remaining work
 };
 
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 + static_cast<int>(sizeof(Bars));
 
 // Two row blocks share the launch (the target states, then the draft
-// states): M tiles 0..mt0-1 read map a0 and write out0, the rest a1 / out1.
+// states): 128-row slabs 0..mt0-1 come from map a0 and go to out0, the
+// rest from a1 to out1.  A work unit is a pair of slabs (2p, 2p + 1; the
+// second may not exist) against one 256-column projection tile: unit u is
+// pair u % pairs, N tile u / pairs.
 struct Args {
-  int rows0, rows1, mt0;
-  int vocab, nk;
+  int rows0, rows1, mt0, mt, pairs;
+  int vocab, nk, units;
   long long ld;
   float* out0;
   float* out1;
   unsigned* err;
 };
 
+// A bounded wait that also gives up at once once another role has.
+__device__ __forceinline__ bool wait_or_abort(Bars& bars, uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (bars.abort) return false;
+  if (svk::mbar_wait_bounded(bar, parity)) return true;
+  bars.abort = 1;
+  atomicOr(err, 1u);
+  return false;
+}
+
+// Persistent: CTA c takes units c, c + gridDim.x, ...  Each K step loads two
+// 128-row slabs of states and one 256-row projection tile (64 KB) and issues
+// two MMAs that share the projection tile, into two 256-column accumulators
+// (all 512 TMEM columns): half the shared-memory bytes per FLOP of a single
+// slab, so three stages keep twice the work in flight.  The producer streams
+// ahead into the next unit while the epilogue drains the accumulators.
 __global__ void __launch_bounds__(THREADS, 1)
     lm_head_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                    const __grid_constant__ CUtensorMap w, Args g) {
@@ -127,24 +150,20 @@ __global__ void __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool second = static_cast<int>(blockIdx.x) >= g.mt0;
-  const int m0 = (second ? static_cast<int>(blockIdx.x) - g.mt0 : static_cast<int>(blockIdx.x)) * BM;
-  const int n0 = static_cast<int>(blockIdx.y) * BN;
-  const CUtensorMap* amap = second ? &a1 : &a0;
-  const int rows = second ? g.rows1 : g.rows0;
-  float* out = second ? g.out1 : g.out0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars.full[s], 1);
       mbar_init(&bars.empty[s], 1);
     }
-    mbar_init(&bars.acc, 1);
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_empty, 4);  // one arrival per epilogue warp
+    bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {  // the whole warp allocates
+  if (warp == 5) {  // the whole warp allocates both accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem)),
-                 "r"(TMEM_COLS)
+                 "r"(2 * TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -154,73 +173,111 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = bars.tmem;
 
   if (warp == 4) {
+    // ---- producer: one thread, every K step of every unit of this CTA
     if (lane == 0) {
-      int issued = 0;
-      for (int ks = 0; ks < g.nk; ++ks) {
-        const int s = ks % STAGES;
-        if (ks >= STAGES && !mbar_wait_bounded(&bars.empty[s], ((ks / STAGES) - 1) & 1)) {
-          atomicOr(g.err, 1u);
-          break;
+      int gk = 0;  // K steps issued so far (stage gk % STAGES, use gk / STAGES)
+      for (int u = blockIdx.x; u < g.units && !bars.abort; u += gridDim.x) {
+        const int p = u % g.pairs, n0 = (u / g.pairs) * BN;
+        const bool two = 2 * p + 1 < g.mt;
+        const CUtensorMap* map[2];
+        int m0[2];
+        for (int h = 0; h < 2; ++h) {
+          const int sl = 2 * p + h;
+          const bool second = sl >= g.mt0;
+          map[h] = second ? &a1 : &a0;
+          m0[h] = (second ? sl - g.mt0 : sl) * BM;
         }
-        const uint32_t a = smem_u32(smem + s * STAGE_BYTES), b = a + A_BYTES;
-        mbar_arrive_expect_tx(&bars.full[s], STAGE_BYTES);
-        tma_load_2d(a, amap, ks * BK, m0, &bars.full[s]);
-        tma_load_2d(b, &w, ks * BK, n0, &bars.full[s]);
-        ++issued;
+        for (int ks = 0; ks < g.nk; ++ks, ++gk) {
+          const int s = gk % STAGES;
+          if (gk >= STAGES && !wait_or_abort(bars, &bars.empty[s], ((gk / STAGES) - 1) & 1, g.err)) break;
+          const uint32_t a = smem_u32(smem + s * STAGE_BYTES), b = a + 2 * A_BYTES;
+          mbar_arrive_expect_tx(&bars.full[s], two ? STAGE_BYTES : STAGE_BYTES - A_BYTES);
+          tma_load_2d(a, map[0], ks * BK, m0[0], &bars.full[s]);
+          if (two) tma_load_2d(a + A_BYTES, map[1], ks * BK, m0[1], &bars.full[s]);
+          tma_load_2d(b, &w, ks * BK, n0, &bars.full[s]);
+        }
       }
-      // no copy may still be writing shared memory at exit: the last loads
-      // of every stage have landed (the MMA warp normally saw them already)
-      for (int ks = issued - STAGES > 0 ? issued - STAGES : 0; ks < issued; ++ks)
-        if (!mbar_wait_bounded(&bars.full[ks % STAGES], (ks / STAGES) & 1)) atomicOr(g.err, 1u);
+      // no copy may still be writing shared memory at exit: the last load of
+      // every stage has landed (the MMA thread normally saw it already)
+      for (int k = gk - STAGES > 0 ? gk - STAGES : 0; k < gk; ++k)
+        if (!svk::mbar_wait_bounded(&bars.full[k % STAGES], (k / STAGES) & 1)) atomicOr(g.err, 1u);
     }
   } else if (warp == 5) {
+    // ---- MMA: one thread issues, the tensor core accumulates in TMEM
     if (lane == 0) {
-      for (int ks = 0; ks < g.nk; ++ks) {
-        const int s = ks % STAGES;
-        if (!mbar_wait_bounded(&bars.full[s], (ks / STAGES) & 1)) {
-          atomicOr(g.err, 1u);
-          break;
-        }
+      int gk = 0, j = 0;
+      for (int u = blockIdx.x; u < g.units && !bars.abort; u += gridDim.x, ++j) {
+        const bool two = 2 * (u % g.pairs) + 1 < g.mt;
+        if (j >= 1 && !wait_or_abort(bars, &bars.acc_empty, (j - 1) & 1, g.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a = smem_u32(smem + s * STAGE_BYTES), b = a + A_BYTES;
+        bool ok = true;
+        for (int ks = 0; ks < g.nk; ++ks, ++gk) {
+          const int s = gk % STAGES;
+          if (!wait_or_abort(bars, &bars.full[s], (gk / STAGES) & 1, g.err)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t a = smem_u32(smem + s * STAGE_BYTES), b = a + 2 * A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled rows
-          mma_bf16(tmem, desc_sw128(a + kk * 32), desc_sw128(b + kk * 32), (ks | kk) ? 1u : 0u);
-        mma_commit(&bars.empty[s]);  // the stage is free once these MMAs have read it
+          for (int kk = 0; kk < BK / 16; ++kk) {  // K = 16 per MMA: 32 bytes along the swizzled rows
+            const uint64_t bd = desc_sw128(b + kk * 32);
+            const uint32_t first = (ks | kk) ? 1u : 0u;
+            mma_bf16(tmem, desc_sw128(a + kk * 32), bd, first);
+            if (two) mma_bf16(tmem + TMEM_COLS, desc_sw128(a + A_BYTES + kk * 32), bd, first);
+          }
+          mma_commit(&bars.empty[s]);  // the stage is free once these MMAs have read it
+        }
+        mma_commit(&bars.acc_full);  // the accumulators are final once every MMA issued so far is
+        if (!ok) break;
       }
-      mma_commit(&bars.acc);  // the accumulator is final once every MMA issued so far is
     }
   } else {
-    // epilogue: warp w holds rows m0 + 32 w + lane
-    if (!mbar_wait_bounded(&bars.acc, 0)) {
-      if (lane == 0) atomicOr(g.err, 1u);
-    } else {
+    // ---- epilogue: warp w holds rows 32 w + lane of each slab
+    int j = 0;
+    for (int u = blockIdx.x; u < g.units; u += gridDim.x, ++j) {
+      if (!wait_or_abort(bars, &bars.acc_full, j & 1, g.err)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int row = m0 + warp * 32 + lane;
-      float* dst_row = out + static_cast<long long>(row) * g.ld;
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c * 32), v);
-        const int col = n0 + c * 32;
-        if (row < rows && col < g.vocab) {
-          if (col + 32 <= g.vocab) {
-            float4* d4 = reinterpret_cast<float4*>(dst_row + col);
+      const int p = u % g.pairs, n0 = (u / g.pairs) * BN;
+      for (int h = 0; h < 2; ++h) {
+        const int sl = 2 * p + h;
+        if (sl >= g.mt) break;
+        const bool second = sl >= g.mt0;
+        const int row = (second ? sl - g.mt0 : sl) * BM + warp * 32 + lane;
+        const int rows = second ? g.rows1 : g.rows0;
+        float* dst_row = (second ? g.out1 : g.out0) + static_cast<long long>(row) * g.ld;
+        const uint32_t acc =
+            tmem + static_cast<uint32_t>(h) * TMEM_COLS + (static_cast<uint32_t>(warp * 32) << 16);
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
+          const int col = n0 + c * 32;
+          if (row < rows && col < g.vocab) {
+            if (col + 32 <= g.vocab) {
+              float4* d4 = reinterpret_cast<float4*>(dst_row + col);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          } else {
+              for (int q = 0; q < 8; ++q)
+                d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col + j < g.vocab) dst_row[col + j] = v[j];
+              for (int q = 0; q < 32; ++q)
+                if (col + q < g.vocab) dst_row[col + q] = v[q];
+            }
           }
         }
       }
+      // this warp's reads are complete: hand the accumulators back to the MMAs
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) svk::mbar_arrive_local(&bars.acc_empty);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 5) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TMEM_COLS)
+                 : "memory");
   }
 }
 
@@ -275,13 +332,25 @@ sv_status launch(const void* s0, int rows0, const void* s1, int rows1, const voi
   g.rows0 = rows0;
   g.rows1 = rows1;
   g.mt0 = (rows0 + BM - 1) / BM;
+  g.mt = g.mt0 + (rows1 + BM - 1) / BM;
+  g.pairs = (g.mt + 1) / 2;
   g.vocab = vocab;
   g.nk = (dim + BK - 1) / BK;
+  const long long tiles = static_cast<long long>(g.pairs) * ((vocab + BN - 1) / BN);
+  if (tiles > 0x7FFFFFFFLL) return svh::fail(SV_ERR_UNSUPPORTED, "too many tiles");
+  g.units = static_cast<int>(tiles);
   g.ld = ld;
   g.out0 = out0;
   g.out1 = out1;
   g.err = err;
-  const dim3 grid(static_cast<unsigned>(g.mt0 + (rows1 + BM - 1) / BM), static_cast<unsigned>((vocab + BN - 1) / BN));
+  // one CTA per SM (the ring takes most of its shared memory), each walking tiles
+  static int sms[64] = {0};
+  if (!sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sms[dev] = n;
+  }
+  const unsigned grid = static_cast<unsigned>(tiles < sms[dev] ? tiles : sms[dev]);
   lm_head_kernel<<<grid, THREADS, kSmemBytes, stream>>>(m0, m1, mw, g);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return svh::fail(SV_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
