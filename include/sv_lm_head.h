@@ -76,6 +76,33 @@ sv_status sv_lm_head_verify(const void* target_states, const void* draft_states,
                             uint32_t* status, void* workspace, size_t workspace_bytes, uint32_t flags,
                             void* stream);
 
+/*
+ * sv_lm_head_verify without a workspace: the library's own scratch, a device
+ * array of SV_STATIC_SCRATCH_BYTES reserved once per device when libsv.so's
+ * module loads there, takes the workspace's place.  The pages have no
+ * counterpart to this call; it is this library's, for callers that cannot
+ * allocate device memory per call or keep a workspace: code that runs where
+ * no allocator is reachable (a plugin whose host framework owns every
+ * allocation) or that must not call cudaMalloc on the decode path (it
+ * synchronises the device).
+ *   Arguments, results and launches as sv_lm_head_verify (no workspace
+ *   arguments).  A call whose sv_lm_head_workspace_size() exceeds
+ *   SV_STATIC_SCRATCH_BYTES returns SV_ERR_UNSUPPORTED and enqueues nothing
+ *   (64 MiB hold, for example, B = 8, K = 5 at V = 128256).
+ *   Every call on a device uses the same scratch: calls that overlap on the
+ *   GPU (different streams, or different host threads with no ordering
+ *   between them) race on it and their results are undefined.  Issue them on
+ *   one stream.
+ *   The first call on each device looks up the scratch's address (a host-side
+ *   runtime query); make that first call before any stream capture.
+ */
+#define SV_STATIC_SCRATCH_BYTES (64u << 20)
+sv_status sv_lm_head_verify_static(const void* target_states, const void* draft_states, const void* proj,
+                                   int32_t dim, const float* temperature, const int32_t* draft_tokens,
+                                   const float* uniforms, const int32_t* cu_k, int32_t batch, int32_t k,
+                                   int32_t sum_k, int32_t vocab, int32_t* n_accepted, int32_t* next_token,
+                                   uint32_t* status, uint32_t flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

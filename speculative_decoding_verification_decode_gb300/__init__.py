@@ -29,6 +29,7 @@ from .api import (  # noqa: F401
     gate_update,
     lm_head_logits,
     lm_head_verify,
+    lm_head_verify_static,
     lm_head_workspace,
     sampler_floors,
     verify_greedy,

@@ -49,6 +49,8 @@ SIGNATURES = {
     "sv_lm_head_workspace_size": (ctypes.c_size_t, [_i32, _i32, _i32]),
     "sv_lm_head_verify": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                  _vp, _vp, _vp, _vp, ctypes.c_size_t, _u32, _vp]),
+    "sv_lm_head_verify_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                        _vp, _vp, _vp, _u32, _vp]),
     "sv_status_string": (ctypes.c_char_p, [_i32]),
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (_i32, []),

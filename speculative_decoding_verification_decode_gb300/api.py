@@ -391,3 +391,29 @@ def lm_head_verify(target_states: torch.Tensor, draft_states: torch.Tensor, proj
         f = workspace[256:256 + (2 * sum_k + B) * ldv * 4].view(torch.float32).view(-1, ldv)
         lt, ld = f[:sum_k + B, :V], f[sum_k + B:, :V]
     return LMHeadResult(res.n_accepted, res.next_token, res.status, lt, ld)
+
+
+def lm_head_verify_static(target_states: torch.Tensor, draft_states: torch.Tensor, proj: torch.Tensor,
+                          temperature: torch.Tensor, draft_tokens: torch.Tensor, uniforms: torch.Tensor,
+                          cu_k: Optional[torch.Tensor] = None, k: Optional[int] = None,
+                          flags: int = 0) -> VerifyResult:
+    """lm_head_verify on the library's own fixed device scratch
+    (sv_lm_head_verify_static, include/sv_lm_head.h): no workspace is
+    allocated or passed.  Calls larger than the scratch raise SVError; calls
+    that overlap on the GPU race on the scratch (issue them on one stream)."""
+    m = _Marshal(target_states)
+    ht = _bf16_rows(target_states, m)
+    hd = _bf16_rows(draft_states, m)
+    w = _bf16_rows(proj, m)
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    u = m.dev(uniforms.reshape(-1), torch.float32)
+    T = m.dev(temperature.reshape(-1), torch.float32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(ht.shape[0], tok, cu, k)
+    V, d = w.shape
+    n, nxt, st = m.outputs(B)
+    lib = _lib.load()
+    with torch.cuda.device(m.device):
+        _check(lib.sv_lm_head_verify_static(_p(ht), _p(hd), _p(w), d, _p(T), _p(tok), _p(u), _p(cu), B, K, sum_k,
+                                            V, _p(n), _p(nxt), _p(st), flags, m.stream()))
+    return m.finish(VerifyResult(n, nxt, st))
