@@ -9,7 +9,9 @@ only) or from the tests themselves.
 
 ``lm_head`` puts the LM head (logits = H W^T, llmstudio.ru section 21) in
 front of the verification.  ``sampler_filter`` holds the top-k / top-p filters applied to p and q
-before verification (llmstudio.ru section 38).  ``draft_gate`` is the
+before verification (llmstudio.ru section 38); ``penalties`` the repetition,
+frequency and presence penalties ahead of them, with the sampler state of
+each row following the speculative branch (sections 38-39).  ``draft_gate`` is the
 draft-length gate that produces the ragged ``cu_k``
 (PocketLLM docs/dspark.md, the draft-length gate section).
 
@@ -60,6 +62,10 @@ from .lm_head import (  # noqa: F401
     lm_head_logits,
     accept_lm_head,
     verify_greedy_lm_head,
+)
+from .penalties import (  # noqa: F401
+    penalize_value,
+    penalize_rows,
 )
 from .draft_gate import (  # noqa: F401
     GateParams,
