@@ -29,6 +29,12 @@ Readings this file fixes:
   are exact).
 * A history id outside [0, V) is skipped (it names no logit); so is a draft
   id outside [0, V) (verification reports it as BAD_TOKEN at its row).
+* A sequence whose parameters are unusable (``r`` not a positive finite
+  number, ``freq`` or ``pres`` not finite) is reported BAD_VALUE and its rows
+  are left as they are; so are rows of a sequence with out-of-range offsets
+  (BAD_LAYOUT) or with more than MAX_DISTINCT distinct in-range ids in its
+  history and drafts together (BAD_LAYOUT: the capacity of the per-sequence
+  count table of the GPU path, part of its interface).
 """
 
 from __future__ import annotations
@@ -38,7 +44,9 @@ from typing import Optional, Tuple
 
 import numpy as np
 
+BAD_VALUE = 2
 BAD_LAYOUT = 64
+MAX_DISTINCT = 8192
 F32 = np.float32
 
 
@@ -104,8 +112,15 @@ def penalize_rows(target: np.ndarray, draft: np.ndarray, dtype: str, hist_offset
         if h0 < 0 or h1 < h0 or h1 > len(hist_tokens):
             st[b] = BAD_LAYOUT
             continue
+        r_ok = np.isfinite(rep[b]) and rep[b] > 0
+        if not (r_ok and np.isfinite(freq[b]) and np.isfinite(pres[b])):
+            st[b] = BAD_VALUE
+            continue
         hist = hist_tokens[h0:h1]
         drafts = tokens[d0:d0 + k]
+        if len(row_counts(hist, drafts, k, V)) > MAX_DISTINCT:
+            st[b] = BAD_LAYOUT
+            continue
         for i in range(k + 1):
             for v, c in row_counts(hist, drafts, i, V).items():
                 rows = [(tg, t0 + i)] + ([(dr, d0 + i)] if i < k else [])

@@ -165,6 +165,38 @@ def test_bad_offsets_leave_rows_alone():
     assert np.array_equal(t2[3:6], tg[3:6]) and np.array_equal(d2[2:4], dr[2:4])
 
 
+def test_unusable_parameters_are_bad_values():
+    rng = np.random.default_rng(6)
+    B, K, V = 4, 2, 10
+    tg, dr = _rows(rng, B, K, V, "f32")
+    tok = rng.integers(0, V, B * K).astype(np.int32)
+    hist = rng.integers(0, V, 8).astype(np.int32)
+    off = np.array([0, 2, 4, 6, 8], np.int32)
+    rep = np.array([0.0, np.nan, 1.5, 1.5], F32)
+    fr = np.array([0.0, 0.0, np.inf, 0.1], F32)
+    pr = np.zeros(B, F32)
+    t2, d2, st = pen.penalize_rows(tg, dr, "f32", off, hist, tok, B, K, None, rep, fr, pr)
+    assert list(st) == [pen.BAD_VALUE] * 3 + [0]
+    assert np.array_equal(t2[:9], tg[:9]) and not np.array_equal(t2[9:], tg[9:])
+
+
+def test_distinct_id_capacity():
+    B, K, V = 2, 1, 20000
+    tg = np.zeros((B * (K + 1), V), F32)
+    dr = np.zeros((B * K, V), F32)
+    tok = np.array([5, 6], np.int32)
+    h = np.concatenate([np.arange(pen.MAX_DISTINCT - 1), np.arange(pen.MAX_DISTINCT)]).astype(np.int32)
+    off = np.array([0, pen.MAX_DISTINCT - 1, len(h)], np.int32)
+    # sequence 0: 8191 history ids + draft 5 (already counted) -> 8191 distinct;
+    # sequence 1: 8192 history ids + draft 6 (already there) -> 8192: both fit
+    a = [np.full(B, 1.0, F32), np.full(B, 0.5, F32), np.zeros(B, F32)]
+    _, _, st = pen.penalize_rows(tg, dr, "f32", off, h, tok, B, K, None, *a)
+    assert list(st) == [0, 0]
+    tok2 = np.array([9000, 9001], np.int32)  # a new id each: 8192 fits, 8193 does not
+    _, _, st = pen.penalize_rows(tg, dr, "f32", off, h, tok2, B, K, None, *a)
+    assert list(st) == [0, pen.BAD_LAYOUT]
+
+
 MUTATIONS = [
     ("row_counts", "drafts[:i]", "drafts[:i + 1]", [test_branch_state_rule_against_a_rolling_sampler]),
     ("penalize_value", "v * r32 if v < 0 else v / r32", "v / r32 if v < 0 else v * r32", [test_hand_values]),
