@@ -25,6 +25,7 @@ from .api import (  # noqa: F401
     VerifyResult,
     accept,
     accept_from_logits,
+    apply_penalties,
     gate_draft_lengths,
     gate_update,
     lm_head_logits,

@@ -6,7 +6,7 @@ import re
 
 from ._build import LIB_PATH, PKG_DIR
 
-HEADERS = [os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h", "sv_filter.h", "sv_lm_head.h")]
+HEADERS = [os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h", "sv_filter.h", "sv_lm_head.h", "sv_penalties.h")]
 
 SV_F32, SV_BF16, SV_F16 = 0, 1, 2
 SV_OK, SV_ERR_ARG, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -51,6 +51,8 @@ SIGNATURES = {
                                  _vp, _vp, _vp, _vp, ctypes.c_size_t, _u32, _vp]),
     "sv_lm_head_verify_static": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                         _vp, _vp, _vp, _u32, _vp]),
+    "sv_apply_penalties": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32,
+                                  _vp, _vp, _vp, _vp, _vp]),
     "sv_status_string": (ctypes.c_char_p, [_i32]),
     "sv_last_error": (ctypes.c_char_p, []),
     "sv_version": (_i32, []),

@@ -417,3 +417,40 @@ def lm_head_verify_static(target_states: torch.Tensor, draft_states: torch.Tenso
         _check(lib.sv_lm_head_verify_static(_p(ht), _p(hd), _p(w), d, _p(T), _p(tok), _p(u), _p(cu), B, K, sum_k,
                                             V, _p(n), _p(nxt), _p(st), flags, m.stream()))
     return m.finish(VerifyResult(n, nxt, st))
+
+
+# ---------------------------------------------------------------- penalties (in place)
+
+def apply_penalties(target_logits: torch.Tensor, draft_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                    repetition: torch.Tensor, frequency: torch.Tensor, presence: torch.Tensor,
+                    hist_offsets: Optional[torch.Tensor] = None, hist_tokens: Optional[torch.Tensor] = None,
+                    cu_k: Optional[torch.Tensor] = None, k: Optional[int] = None) -> torch.Tensor:
+    """Repetition / frequency / presence penalties on the raw logits rows, in
+    place (include/sv_penalties.h): row i of a sequence sees its history plus
+    the drafts before position i.  The rows must be CUDA tensors with unit
+    stride along V.  Returns the per-sequence status (int32 [B])."""
+    for x in (target_logits, draft_logits):
+        if x.device.type != "cuda" or x.stride(-1) != 1:
+            raise ValueError("the rows must be CUDA tensors with unit stride along V (modified in place)")
+    dev = target_logits.device
+    tg = target_logits.reshape(-1, target_logits.shape[-1])
+    dr = draft_logits.reshape(-1, draft_logits.shape[-1])
+    if tg.data_ptr() != target_logits.data_ptr() or dr.data_ptr() != draft_logits.data_ptr():
+        raise ValueError("the rows must be addressable as [rows, V] in place")
+    if dr.numel() and dr.stride(0) != tg.stride(0):
+        raise ValueError("target and draft rows must have the same row stride")
+    m = _Marshal(target_logits)
+    tok = m.dev(draft_tokens.reshape(-1), torch.int32)
+    cu = m.dev(cu_k, torch.int32)
+    B, K, sum_k = _layout(tg.shape[0], tok, cu, k)
+    f = lambda x: m.dev(x.reshape(-1), torch.float32)
+    r, fr, pr = f(repetition), f(frequency), f(presence)
+    ho = m.dev(hist_offsets, torch.int32)
+    ht = m.dev(hist_tokens, torch.int32)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        _check(lib.sv_apply_penalties(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(ho), _p(ht),
+                                      0 if ht is None else ht.numel(), _p(tok), _p(cu), B, K, sum_k, tg.shape[1],
+                                      _p(r), _p(fr), _p(pr), _p(st), m.stream()))
+    return st

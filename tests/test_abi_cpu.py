@@ -217,3 +217,23 @@ def test_lm_head_host_checks(lib):
     assert lib.sv_lm_head_verify(*args, P + 8, need, 0, NULL) == _lib.SV_ERR_ARG  # workspace alignment
     assert lib.sv_lm_head_verify(P, P, P, 64, P, P, P, NULL, 2, 3, 5, 100, P, P, P, P, need, 0,
                                  NULL) == _lib.SV_ERR_ARG  # sum_k != B * K without cu_k
+
+
+def test_penalties_host_checks(lib):
+    P = 1 << 12
+    base = dict(t=P, d=P, dt=1, stride=100, ho=P, ht=P, hn=10, tok=P, cu=NULL, B=2, K=3, sk=6, V=100,
+                r=P, f=P, p=P, st=P, stream=NULL)
+
+    def call(**kw):
+        a = dict(base)
+        a.update(kw)
+        return lib.sv_apply_penalties(*a.values())
+
+    assert call(K=1025, sk=2050) == _lib.SV_ERR_UNSUPPORTED
+    assert call(ho=NULL) == _lib.SV_ERR_ARG and b"hist" in lib.sv_last_error()
+    assert call(ho=NULL, ht=NULL, hn=3) == _lib.SV_ERR_ARG
+    assert call(sk=5) == _lib.SV_ERR_ARG
+    assert call(stride=99) == _lib.SV_ERR_ARG
+    assert call(dt=5) == _lib.SV_ERR_ARG
+    assert call(st=NULL) == _lib.SV_ERR_ARG
+    assert call(B=0, sk=0, t=NULL, d=NULL, tok=NULL, st=NULL) == _lib.SV_OK
