@@ -106,8 +106,14 @@ void layout(bool sampling, int V, int elem, int C, int ring_slots, Plan& p) {
 // brings the slice down to kSampleSliceEl elements.  A sampling sequence is a
 // chain of dependent row passes, so slices past that length lengthen every
 // link; smaller ones add cluster exchanges and launch more CTAs than fit at
-// once (measured on GB300 at V = 32000 and V = 128256).
+// once (measured on GB300 at V = 32000 and V = 128256).  A batch too small to
+// give half the SMs a CTA at that size keeps splitting its rows (down to
+// kMinSampleSliceEl elements, up to 16 CTAs): the SMs are idle otherwise, and
+// shorter slices shorten every link of its chains (measured: one sequence at
+// V = 32000 f32 23.2 -> 17.1 us, eight at V = 128256 bf16 25.2 -> 21.2 us;
+// sixteen at V = 128256 went from 29.3 to 35.5 us at 16 CTAs, hence the half).
 constexpr long long kSampleSliceEl = 16384;
+constexpr long long kMinSampleSliceEl = 2048;
 
 bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
   const int vec = 16 / elem;
@@ -122,7 +128,9 @@ bool make_plan(bool sampling, int B, int V, int elem, Plan& out) {
     out = p;
     found = true;
     if (p.smem <= kSmemTwoCtas &&
-        (static_cast<long long>(B) * p.C >= want || (sampling && p.slice <= kSampleSliceEl)))
+        (static_cast<long long>(B) * p.C >= want ||
+         (sampling && p.slice <= kSampleSliceEl &&
+          (2LL * B * p.C >= sm_count() || p.slice <= kMinSampleSliceEl))))
       break;
   }
   return found;
