@@ -373,16 +373,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     return;
   }
 
-  // ---- pass 1: the row maximum and non-NaN count; a strided sample of
-  // kCap keys (0: NaN) into `col`
-  float mx = -kInfF;
-  uint32_t nan_n = 0u;
-  for_each_raw<T>(row, a.V, [&](uint32_t raw) {
-    const float x = KT::value_raw(raw);
-    mx = fmaxf(mx, x);  // NaN never wins
-    nan_n += x != x ? 1u : 0u;
-  });
-  uint32_t nn = nan_n;  // NaN count here; the non-NaN count after the reduction
+  // ---- a strided sample of kCap keys (0: NaN) into `col`
 #pragma unroll
   for (int j = 0; j < kCap / kThreads; ++j) {
     const int e = static_cast<int>((static_cast<long long>(tid * (kCap / kThreads) + j) * a.V) / kCap);
@@ -392,21 +383,88 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     uint32_t k;
     col[tid * (kCap / kThreads) + j] = KT::key(raw, k) ? k : 0u;
   }
-  mx = svk::warp_max_f(mx);
-  nn = __reduce_add_sync(0xFFFFFFFFu, nn);
-  if (lane == 0) {
-    r_max[warp] = mx;
-    r_cnt[warp] = nn;
-  }
   if (tid == 0) n_col = 0;
-  __syncthreads();
-  mx = -kInfF;
-  nn = 0u;
-  for (int w = 0; w < kWarpsF; ++w) {
-    mx = fmaxf(mx, r_max[w]);
-    nn += r_cnt[w];
+  auto none = [](uint32_t) { return 0ull; };
+  auto samp_src = [&](auto f) {
+    for (int j = tid; j < kCap; j += kThreads) {
+      const uint32_t k = col[j];
+      if (k) f(k);
+    }
+  };
+  // a lower bound L of the floor from the sample: the sample's rank of `j`
+  // logits (a rank beyond the sample collects every logit); every logit >= L
+  // is collected below
+  auto lower_bound = [&](unsigned long long j) -> uint32_t {
+    uint32_t Lk = 1u;  // every key is >= 1
+    if (j >= 1ull && j < static_cast<unsigned long long>(kCap)) {
+      radix_select<KT>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
+      if (sel.ok) Lk = sel.prefix;
+    }
+    __syncthreads();  // the sample is no longer read
+    return Lk;
+  };
+  // every key >= L into `col` (its count is exact), the row maximum and its
+  // non-NaN count, and with `need_z` the total weight (the maximum known)
+  float mx = -kInfF;
+  uint32_t nan_n = 0u;
+  unsigned long long z = 0ull;
+  auto collect = [&](uint32_t L, bool need_max, bool need_z, const auto& wfz) {
+    // compared as values (NaN never passes; -0 and +0 compare equal, as
+    // their keys are equal); keys only for the logits collected
+    const float Lf = L == 1u ? -kInfF : KT::value(L);
+    for_each_raw<T>(row, a.V, [&](uint32_t raw) {
+      const float x = KT::value_raw(raw);
+      if (need_max) {
+        mx = fmaxf(mx, x);  // NaN never wins
+        nan_n += x != x ? 1u : 0u;
+      }
+      if (need_z && x == x) z += svk::floor_u64(__fmul_rn(wfz(x), 0x1p40f));
+      if (x >= Lf) {
+        uint32_t k;
+        KT::key(raw, k);
+        const int at = atomicAdd(&n_col, 1);
+        if (at < kCap) col[at] = k;
+      }
+    });
+  };
+  auto reduce_max = [&]() -> uint32_t {  // the CTA's maximum into mx; returns the non-NaN count
+    float wm = svk::warp_max_f(mx);
+    uint32_t wn = __reduce_add_sync(0xFFFFFFFFu, nan_n);
+    if (lane == 0) {
+      r_max[warp] = wm;
+      r_cnt[warp] = wn;
+    }
+    __syncthreads();
+    mx = -kInfF;
+    wn = 0u;
+    for (int w = 0; w < kWarpsF; ++w) {
+      mx = fmaxf(mx, r_max[w]);
+      wn += r_cnt[w];
+    }
+    return static_cast<uint32_t>(a.V) - wn;
+  };
+  auto no_wf = [](float) { return 0.f; };
+
+  uint32_t nn;
+  if (use_k) {
+    // top-k: one pass over the row collects every key >= L (the sample's
+    // rank of 2k logits, taking every logit as non-NaN, plus a margin) and
+    // takes the maximum and the non-NaN count on the way
+    const uint32_t L = lower_bound(2ull * static_cast<unsigned long long>(kk) * kCap / a.V + 16ull);
+    collect(L, true, false, no_wf);
+    nn = reduce_max();
+  } else {
+    // top-p alone: the maximum first (the weights need it), then a pass that
+    // collects every key >= L (the sample's rank of about 0.6 kCap logits:
+    // a nucleus of up to a couple of thousand logits is then complete) and
+    // sums the row's weight Z
+    for_each_raw<T>(row, a.V, [&](uint32_t raw) {
+      const float x = KT::value_raw(raw);
+      mx = fmaxf(mx, x);
+      nan_n += x != x ? 1u : 0u;
+    });
+    nn = reduce_max();
   }
-  nn = static_cast<uint32_t>(a.V) - nn;
   if (nn == 0u || !(mx > -kInfF && mx < kInfF)) {  // no finite maximum: no filter
     if (tid == 0) *out = -kInfF;
     return;
@@ -414,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   uint32_t kmax;
   KT::key(KT::raw_of(mx), kmax);
   const float m = KT::value(kmax);
-  if (use_k && static_cast<uint32_t>(kk) >= nn) use_k = false;  // k covers the row
+  bool k_covers = use_k && static_cast<uint32_t>(kk) >= nn;  // k covers the row
+  if (k_covers) use_k = false;
   if (!use_k && !use_p) {
     if (tid == 0) *out = -kInfF;
     return;
@@ -435,68 +494,27 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   auto weight = [&](uint32_t k) -> unsigned long long {
     return svk::floor_u64(__fmul_rn(wf(KT::value(k)), 0x1p40f));
   };
-  auto none = [](uint32_t) { return 0ull; };
   auto col_src = [&](auto f) {
     const int n = min(n_col, kCap);
     for (int j = tid; j < n; j += kThreads) f(col[j]);
   };
-  auto samp_src = [&](auto f) {
-    for (int j = tid; j < kCap; j += kThreads) {
-      const uint32_t k = col[j];
-      if (k) f(k);
-    }
-  };
 
-  // ---- a lower bound L of the floor from the sample: every logit >= L is
-  // collected in pass 2.  Top-k: the sample's rank of 2k logits, plus a
-  // margin.  Top-p alone: the rank of about 0.6 kCap logits (a nucleus of up
-  // to a couple of thousand logits is then complete in the list).  A sample
-  // rank beyond the sample collects every logit.
-  uint32_t L = 1u;  // every key is >= 1
-  {
-    const unsigned long long ns = kCap;  // samples drawn (a short row is sampled repeatedly)
-    const unsigned long long j = use_k ? 2ull * static_cast<unsigned long long>(kk) * ns / nn + 16ull
-                                       : (6ull * kCap / 10ull) * ns / nn;
-    if (j >= 1ull && j < ns) {
-      radix_select<KT>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
-      if (sel.ok) L = sel.prefix;
-    }
-  }
-  __syncthreads();  // the sample is no longer read
-
-  // ---- pass 2: collect every key >= L (its count is exact); with top-p alone
-  // also the total weight Z
-  unsigned long long z = 0ull;
-  {
-    const bool need_z = !use_k;
-    // compared as values (NaN never passes; -0 and +0 compare equal, as
-    // their keys are equal); keys only for the logits collected
-    const float Lf = L == 1u ? -kInfF : KT::value(L);
-    for_each_raw<T>(row, a.V, [&](uint32_t raw) {
-      const float x = KT::value_raw(raw);
-      if (need_z && x == x) z += svk::floor_u64(__fmul_rn(wf(x), 0x1p40f));
-      if (x >= Lf) {
-        uint32_t k;
-        KT::key(raw, k);
-        const int at = atomicAdd(&n_col, 1);
-        if (at < kCap) col[at] = k;
-      }
-    });
-    if (need_z) {
+  if (!use_k && !k_covers) {  // top-p alone: the collecting pass with Z
+    const uint32_t L = lower_bound((6ull * kCap / 10ull) * kCap / nn);
+    collect(L, false, true, wf);
 #pragma unroll
-      for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-      if (lane == 0) r_z[warp] = z;
-    }
-  }
-  __syncthreads();
-  if (!use_k) {
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+    if (lane == 0) r_z[warp] = z;
+    __syncthreads();
     z = 0ull;
     for (int w = 0; w < kWarpsF; ++w) z += r_z[w];
   }
+  __syncthreads();
   const int nc = n_col;
   // the collection holds every key >= L unless it overflowed; for top-k it
-  // must also reach k keys (else the k-th largest lies below L)
-  bool fast = nc <= kCap && (!use_k || nc >= kk);
+  // must also reach k keys (else the k-th largest lies below L).  A top-k
+  // that covers the row leaves top-p alone without its Z: the full-row path.
+  bool fast = !k_covers && nc <= kCap && (!use_k || nc >= kk);
 
   uint32_t key_k = 0u, key_p = 0u;
   if (fast) {
