@@ -13,17 +13,19 @@
 // (sign, exponent and two mantissa bits of an f32), so the logits of a row
 // spread over many bins and the shared-memory atomics rarely collide.
 //
-// Two passes over the row.  The first takes the row maximum, the non-NaN
-// count and a strided sample of 4096 logits; the sample gives a lower bound L
-// of the floor (for top-k the rank 2k plus a margin, for top-p alone the rank
-// of about 2500 logits), and the second pass appends every logit >= L to a
-// shared-memory list and, for top-p alone, sums the row's weight Z.  The
-// exact selects then run on the list: its counts and weights are complete
-// for every key >= L, so a floor found there is the row's own when (top-k)
-// the list holds at least k keys, or (top-p alone) the test already fails
-// once the chosen key's own group is added.  When a check fails or the list
-// overflows, the same selects run over the whole row instead (a few more
-// passes; correct, only slower).
+// A sample of 4096 logits (64 runs of consecutive logits spread over the
+// row, one round trip) gives a lower bound L of the floor.  Top-k: the lowest
+// key of the first-level bin holding the sample's rank of 2k logits plus a
+// margin; one pass over the row then takes the maximum and the non-NaN count
+// and appends every logit >= L to a shared-memory list.  Top-p alone: a first
+// pass takes the maximum (the weights need it), L is the sample's rank of
+// about 2500 logits, and a second pass appends every logit >= L and sums the
+// row's weight Z.  The exact selects then run on the list: its counts and
+// weights are complete for every key >= L, so a floor found there is the
+// row's own when (top-k) the list holds at least k keys, or (top-p alone)
+// the test already fails once the chosen key's own group is added.  When a
+// check fails or the list overflows, the same selects run over the whole row
+// instead (a few more passes; correct, only slower).
 //
 // Counts are 32-bit integers and weights 64-bit fixed point (2^-40 units,
 // truncated, converted with integer operations), so every sum is exact and
@@ -46,6 +48,7 @@ constexpr int kThreads = 512;
 constexpr int kWarpsF = kThreads / 32;
 constexpr int kMaxBins = 2048;
 constexpr int kCap = 4096;  // sampled keys, then collected keys, in shared memory
+constexpr int kSampleRuns = 64;  // runs of consecutive logits the sample takes
 
 struct Args {
   const void* tgt;
@@ -281,14 +284,16 @@ __device__ __forceinline__ void scan_bins(const unsigned* hc, const unsigned lon
 // skipping keys below `lower`: leaves in `sel` the lowest key whose keys above
 // pass the test, their count and weight, and the count and weight of the
 // keys equal to it.  Collective (every thread of the CTA).
-template <typename KT, typename Src, typename WFn>
+// LEVELS < KT::kLevels stops early: the prefix then names the bin (a range
+// of keys) that holds the answer.
+template <typename KT, int LEVELS = KT::kLevels, typename Src, typename WFn>
 __device__ __forceinline__ void radix_select(const Src& src, const WFn& weight, bool use_mass, uint32_t lower,
                                              const Crit& cr, unsigned* h_cnt, unsigned long long* h_mass,
                                              Sel& sel) {
   const int tid = threadIdx.x;
   __syncthreads();  // earlier readers of `sel` and of the histograms are done
   if (tid == 0) sel = Sel{0u, 1, 0ull, 0ull, 0ull, 0ull};
-  for (int l = 0; l < KT::kLevels; ++l) {
+  for (int l = 0; l < LEVELS; ++l) {
     const int nb = 1 << KT::width(l);
     const int sh = KT::shift(l);
     const int hs = sh + KT::width(l);
@@ -373,15 +378,25 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     return;
   }
 
-  // ---- a strided sample of kCap keys (0: NaN) into `col`
+  // ---- a sample of kCap keys (0: NaN) into `col`: kSampleRuns runs of
+  // consecutive logits spread evenly over the row (a few sectors each, so
+  // the sample costs one round trip and a few KB, not one sector per key)
+  {
+    constexpr int kRun = kCap / kSampleRuns;
+    constexpr int kPer = kCap / kThreads;  // consecutive sampled logits per thread
+    static_assert(kRun % kPer == 0, "runs split evenly over threads");
+    const int e0 = tid * kPer;  // this thread's first sample slot
+    const long long span = a.V > kRun ? static_cast<long long>(a.V - kRun) : 0;
+    const long long base = span * (e0 / kRun) / (kSampleRuns - 1);
 #pragma unroll
-  for (int j = 0; j < kCap / kThreads; ++j) {
-    const int e = static_cast<int>((static_cast<long long>(tid * (kCap / kThreads) + j) * a.V) / kCap);
-    uint32_t raw;
-    if constexpr (sizeof(T) == 4) raw = __ldg(reinterpret_cast<const uint32_t*>(row) + e);
-    else raw = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e));
-    uint32_t k;
-    col[tid * (kCap / kThreads) + j] = KT::key(raw, k) ? k : 0u;
+    for (int j = 0; j < kPer; ++j) {
+      const long long e = (base + (e0 % kRun) + j) % a.V;
+      uint32_t raw;
+      if constexpr (sizeof(T) == 4) raw = __ldg(reinterpret_cast<const uint32_t*>(row) + e);
+      else raw = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e));
+      uint32_t k;
+      col[e0 + j] = KT::key(raw, k) ? k : 0u;
+    }
   }
   if (tid == 0) n_col = 0;
   auto none = [](uint32_t) { return 0ull; };
@@ -392,13 +407,20 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     }
   };
   // a lower bound L of the floor from the sample: the sample's rank of `j`
-  // logits (a rank beyond the sample collects every logit); every logit >= L
-  // is collected below
-  auto lower_bound = [&](unsigned long long j) -> uint32_t {
+  // logits, or with `coarse` the lowest key of the first-level bin that holds
+  // it (one radix level instead of all; a rank beyond the sample collects
+  // every logit); every logit >= L is collected below
+  auto lower_bound = [&](unsigned long long j, bool coarse) -> uint32_t {
     uint32_t Lk = 1u;  // every key is >= 1
     if (j >= 1ull && j < static_cast<unsigned long long>(kCap)) {
-      radix_select<KT>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
-      if (sel.ok) Lk = sel.prefix;
+      if (coarse) {
+        radix_select<KT, 1>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
+        if (sel.ok) Lk = sel.prefix << KT::shift(0);
+      } else {
+        radix_select<KT>(samp_src, none, false, 0u, Crit{true, j, 0.0}, h_cnt, h_mass, sel);
+        if (sel.ok) Lk = sel.prefix;
+      }
+      if (Lk == 0u) Lk = 1u;
     }
     __syncthreads();  // the sample is no longer read
     return Lk;
@@ -450,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     // top-k: one pass over the row collects every key >= L (the sample's
     // rank of 2k logits, taking every logit as non-NaN, plus a margin) and
     // takes the maximum and the non-NaN count on the way
-    const uint32_t L = lower_bound(2ull * static_cast<unsigned long long>(kk) * kCap / a.V + 16ull);
+    const uint32_t L = lower_bound(2ull * static_cast<unsigned long long>(kk) * kCap / a.V + 16ull, true);
     collect(L, true, false, no_wf);
     nn = reduce_max();
   } else {
@@ -500,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   };
 
   if (!use_k && !k_covers) {  // top-p alone: the collecting pass with Z
-    const uint32_t L = lower_bound((6ull * kCap / 10ull) * kCap / nn);
+    const uint32_t L = lower_bound((6ull * kCap / 10ull) * kCap / nn, false);
     collect(L, false, true, wf);
 #pragma unroll
     for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
