@@ -37,6 +37,7 @@
 
 #include <cfloat>
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/sv_filter.h"
 #include "sv_host.h"
@@ -430,17 +431,21 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   float mx = -kInfF;
   uint32_t nan_n = 0u;
   unsigned long long z = 0ull;
-  auto collect = [&](uint32_t L, bool need_max, bool need_z, const auto& wfz) {
+  // need_max / need_z: std::true_type or std::false_type (each pass is
+  // compiled with exactly the work it does per element)
+  auto collect = [&](uint32_t L, auto need_max, auto need_z, const auto& wfz) {
     // compared as values (NaN never passes; -0 and +0 compare equal, as
     // their keys are equal); keys only for the logits collected
     const float Lf = L == 1u ? -kInfF : KT::value(L);
     for_each_raw<T>(row, a.V, [&](uint32_t raw) {
       const float x = KT::value_raw(raw);
-      if (need_max) {
+      if constexpr (decltype(need_max)::value) {
         mx = fmaxf(mx, x);  // NaN never wins
         nan_n += x != x ? 1u : 0u;
       }
-      if (need_z && x == x) z += svk::floor_u64(__fmul_rn(wfz(x), 0x1p40f));
+      if constexpr (decltype(need_z)::value) {
+        if (x == x) z += svk::floor_u64(__fmul_rn(wfz(x), 0x1p40f));
+      }
       if (x >= Lf) {
         uint32_t k;
         KT::key(raw, k);
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
     // rank of 2k logits, taking every logit as non-NaN, plus a margin) and
     // takes the maximum and the non-NaN count on the way
     const uint32_t L = lower_bound(2ull * static_cast<unsigned long long>(kk) * kCap / a.V + 16ull, true);
-    collect(L, true, false, no_wf);
+    collect(L, std::true_type{}, std::false_type{}, no_wf);
     nn = reduce_max();
   } else {
     // top-p alone: the maximum first (the weights need it), then a pass that
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
 
   if (!use_k && !k_covers) {  // top-p alone: the collecting pass with Z
     const uint32_t L = lower_bound((6ull * kCap / 10ull) * kCap / nn, false);
-    collect(L, false, true, wf);
+    collect(L, std::false_type{}, std::true_type{}, wf);
 #pragma unroll
     for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
     if (lane == 0) r_z[warp] = z;
