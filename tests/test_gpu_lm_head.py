@@ -152,3 +152,39 @@ def test_verify_full_size():
         scale = (np.abs(hs) * np.abs(ws)).sum(1)
         assert (np.abs(logits[r, c] - exact) <= REL * scale).all()
     _against_own_logits(wl, res, lt, ld, "full size")
+
+
+def test_whole_sampling_pipeline_from_states():
+    """llmstudio.ru section 38's pipeline end to end on the GPU: the LM head's
+    logits, penalties (section 39's branch state), then the temperature,
+    top-k and top-p (the floors) and the verification; against the oracle
+    running the same pipeline on the kernel's logits: penalised rows bit for
+    bit, decisions equal outside the oracle's flagged bands."""
+    from oracle import penalties as pen
+    wl = make_lm_head(B=6, K=4, V=3000, d=256)
+    B, K, V = wl.B, wl.K, wl.V
+    hist = np.random.default_rng(3).integers(0, V, 60).astype(np.int32)
+    off = np.array([0, 10, 20, 30, 40, 50, 60], np.int32)
+    rep, fr, pr = (np.full(B, 1.3, np.float32), np.full(B, 0.2, np.float32), np.full(B, 0.5, np.float32))
+    top_k = np.array([50, 0, 5, 50, 200, 1], np.int32)
+    top_p = np.array([0.9, 0.8, 1.0, 0.95, 0.9, 0.5], np.float32)
+    lt = sv().lm_head_logits(bf16_dev(wl.h_target), bf16_dev(wl.w))
+    ld = sv().lm_head_logits(bf16_dev(wl.h_draft), bf16_dev(wl.w))
+    raw_t, raw_d = lt.cpu().numpy().copy(), ld.cpu().numpy().copy()
+    dev = lambda a: torch.from_numpy(a).to(DEV)
+    st = sv().apply_penalties(lt, ld, dev(wl.tokens), dev(rep), dev(fr), dev(pr), hist_offsets=dev(off),
+                              hist_tokens=dev(hist))
+    T = dev(wl.temperature)
+    r = sv().accept_from_logits(lt, ld, T, dev(wl.tokens), dev(wl.uniforms), top_k=dev(top_k), top_p=dev(top_p))
+    torch.cuda.synchronize()
+    assert (st.cpu().numpy() == 0).all()
+    pt, pd, _ = pen.penalize_rows(raw_t, raw_d, "f32", off, hist, wl.tokens, B, K, None, rep, fr, pr)
+    assert np.array_equal(lt.cpu().numpy(), pt) and np.array_equal(ld.cpu().numpy(), pd)
+    ref = oracle.accept_from_logits(pt, pd, "f32", wl.temperature, wl.tokens, wl.uniforms, B, K,
+                                    top_k=top_k, top_p=top_p)
+    res = oracle.Result(r.n_accepted.cpu().numpy(), r.next_token.cpu().numpy(),
+                        r.status.cpu().numpy().astype(np.uint32))
+    H().assert_softmax_agreement(res, ref, "states -> penalties -> filters -> verification")
+    same = res.n_accepted == ref.n_accepted
+    near = (ref.status & np.uint32(oracle.NEAR_BOUNDARY | oracle.NEAR_FILTER | oracle.NEAR_DECISION)) > 0
+    assert ((res.next_token == ref.next_token) | near | ~same).all()
