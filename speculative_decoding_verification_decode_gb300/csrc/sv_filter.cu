@@ -50,6 +50,7 @@ constexpr int kWarpsF = kThreads / 32;
 constexpr int kMaxBins = 2048;
 constexpr int kCap = 4096;  // sampled keys, then collected keys, in shared memory
 constexpr int kSampleRuns = 64;  // runs of consecutive logits the sample takes
+constexpr int kTopSet = 64;      // a top-k set this small takes top-p by ranking
 
 struct Args {
   const void* tgt;
@@ -326,6 +327,46 @@ __device__ __forceinline__ void radix_select(const Src& src, const WFn& weight, 
   }
 }
 
+// Warp: the top-p floor of a top-k set of n <= kTopSet keys (tk[0..n)):
+// the lowest key whose higher-ranked weight (the keys strictly above it)
+// passes the test.  Each lane ranks its two keys against all n (ties: by
+// position) and places them in descending order in `ord`; lane 0 then walks
+// the ranking once, group by group.  Returns the key on every lane.
+template <typename WFn>
+__device__ __forceinline__ uint32_t top_p_small(uint32_t* tk, int n, const WFn& weight, const Crit& cr) {
+  const int lane = threadIdx.x & 31;
+  __shared__ uint32_t ord[kTopSet];
+  for (int h = 0; h < kTopSet / 32; ++h) {
+    const int j = lane + 32 * h;
+    if (j >= n) continue;
+    const uint32_t kj = tk[j];
+    int rank = 0;
+    for (int m = 0; m < n; ++m) {
+      const uint32_t km = tk[m];
+      rank += (km > kj || (km == kj && m < j)) ? 1 : 0;
+    }
+    ord[rank] = kj;
+  }
+  __syncwarp();
+  uint32_t ans = 0u;
+  if (lane == 0) {
+    unsigned long long above = 0ull;  // weight of the keys strictly above the current group
+    int j = 0;
+    while (j < n) {
+      const uint32_t g = ord[j];
+      if (!cr.within(0ull, above)) break;
+      ans = g;
+      unsigned long long w = 0ull;
+      while (j < n && ord[j] == g) {
+        w += weight(g);
+        ++j;
+      }
+      above += w;
+    }
+  }
+  return __shfl_sync(0xFFFFFFFFu, ans, 0);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_constant__ Args a) {
   using KT = KeyOf<T>;
@@ -338,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
   __shared__ unsigned long long r_z[kWarpsF];
   __shared__ Sel sel;
   __shared__ int n_col;
+  __shared__ uint32_t tk[kTopSet];  // the top-k set, when small
+  __shared__ int n_tk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   const long long b = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
@@ -553,10 +596,15 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
       key_p = key_k;
     }
     if (fast && use_p && key_k < kmax) {
-      if (use_k) {  // Z over the top-k set, all of it collected
+      if (use_k) {  // Z over the top-k set, all of it collected; the set itself into tk
+        if (tid == 0) n_tk = 0;
+        __syncthreads();
         unsigned long long zk = 0ull;
         col_src([&](uint32_t k) {
-          if (k >= key_k) zk += weight(k);
+          if (k < key_k) return;
+          zk += weight(k);
+          const int at = atomicAdd(&n_tk, 1);
+          if (at < kTopSet) tk[at] = k;
         });
 #pragma unroll
         for (int o = 16; o; o >>= 1) zk += __shfl_xor_sync(0xFFFFFFFFu, zk, o);
@@ -567,11 +615,22 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
         for (int w = 0; w < kWarpsF; ++w) z += r_z[w];
       }
       const Crit cr{false, 0ull, static_cast<double>(p) * static_cast<double>(z)};
-      radix_select<KT>(col_src, weight, true, key_k, cr, h_cnt, h_mass, sel);
-      // with top-k every key above the answer is collected; with top-p alone
-      // the answer is the row's own once the test fails with its own group
-      fast = sel.ok && (use_k || !cr.within(0ull, sel.m_above + sel.m_grp));
-      key_p = sel.prefix;
+      if (use_k && n_tk <= kTopSet) {
+        // a top-k set of at most kTopSet keys: warp 0 ranks them, sums the
+        // weights in descending order and keeps the groups of equal keys
+        // whose higher-ranked weight passes the test (the radix select's
+        // rule, key by key)
+        if (warp == 0) key_p = top_p_small(tk, n_tk, weight, cr);
+        if (tid == 0) sel.prefix = key_p;
+        __syncthreads();
+        key_p = sel.prefix;
+      } else {
+        radix_select<KT>(col_src, weight, true, key_k, cr, h_cnt, h_mass, sel);
+        // with top-k every key above the answer is collected; with top-p alone
+        // the answer is the row's own once the test fails with its own group
+        fast = sel.ok && (use_k || !cr.within(0ull, sel.m_above + sel.m_grp));
+        key_p = sel.prefix;
+      }
     }
   }
   if (!fast) {  // full-row radix selects
