@@ -47,6 +47,11 @@ constexpr uint32_t TMEM_COLS = 256;  // one fp32 accumulator: 128 lanes x 256 co
 // 17-22), M / 16 (bits 24-28).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(BN) >> 3) << 17) |
                             ((uint32_t(BM) >> 4) << 24);
+// The same with M = 64, for a slab that holds at most 64 rows: its results
+// occupy lanes 0-15 of each 32-lane quarter of tensor memory (row r in lane
+// 32 (r / 16) + r % 16), and the MMA does half the work.
+constexpr uint32_t kIdesc64 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t(BN) >> 3) << 17) |
+                              ((64u >> 4) << 24);
 
 // Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
 // rows of 64 bf16 (128 bytes), 8-row groups 1024 bytes apart (stride byte
@@ -69,11 +74,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t acc) {
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(acc)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -125,6 +131,13 @@ struct Args {
   float* out1;
   unsigned* err;
 };
+
+// Rows of slab sl that hold data (at most BM).
+__device__ __forceinline__ int slab_rows(const Args& g, int sl) {
+  const bool second = sl >= g.mt0;
+  const int left = (second ? g.rows1 : g.rows0) - (second ? sl - g.mt0 : sl) * BM;
+  return left < BM ? left : BM;
+}
 
 // A bounded wait that also gives up at once once another role has.
 __device__ __forceinline__ bool wait_or_abort(Bars& bars, uint64_t* bar, uint32_t parity, unsigned* err) {
@@ -207,7 +220,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       int gk = 0, j = 0;
       for (int u = blockIdx.x; u < g.units && !bars.abort; u += gridDim.x, ++j) {
-        const bool two = 2 * (u % g.pairs) + 1 < g.mt;
+        const int p0 = 2 * (u % g.pairs);
+        const bool two = p0 + 1 < g.mt;
+        const uint32_t id0 = slab_rows(g, p0) <= 64 ? kIdesc64 : kIdesc;
+        const uint32_t id1 = two && slab_rows(g, p0 + 1) <= 64 ? kIdesc64 : kIdesc;
         if (j >= 1 && !wait_or_abort(bars, &bars.acc_empty, (j - 1) & 1, g.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         bool ok = true;
@@ -223,8 +239,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {  // K = 16 per MMA: 32 bytes along the swizzled rows
             const uint64_t bd = desc_sw128(b + kk * 32);
             const uint32_t first = (ks | kk) ? 1u : 0u;
-            mma_bf16(tmem, desc_sw128(a + kk * 32), bd, first);
-            if (two) mma_bf16(tmem + TMEM_COLS, desc_sw128(a + A_BYTES + kk * 32), bd, first);
+            mma_bf16(tmem, desc_sw128(a + kk * 32), bd, id0, first);
+            if (two) mma_bf16(tmem + TMEM_COLS, desc_sw128(a + A_BYTES + kk * 32), bd, id1, first);
           }
           mma_commit(&bars.empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -243,7 +259,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int sl = 2 * p + h;
         if (sl >= g.mt) break;
         const bool second = sl >= g.mt0;
-        const int row = (second ? sl - g.mt0 : sl) * BM + warp * 32 + lane;
+        const bool m64 = slab_rows(g, sl) <= 64;  // rows in lanes 0-15 of each quarter
+        const int row = (second ? sl - g.mt0 : sl) * BM + (m64 ? (lane < 16 ? warp * 16 + lane : BM) : warp * 32 + lane);
         const int rows = second ? g.rows1 : g.rows0;
         float* dst_row = (second ? g.out1 : g.out0) + static_cast<long long>(row) * g.ld;
         const uint32_t acc =
