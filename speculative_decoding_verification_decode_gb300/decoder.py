@@ -5,7 +5,8 @@ runtime"; the spec-verify card, "Usage"):
 
 1. draft K tokens, one drafter step per position (greedy: the argmax of the
    drafter's logits; sampling: an inverse-CDF draw from softmax(logits / T)
-   with an explicit uniform);
+   with an explicit uniform, taken by the verification kernel as the bonus
+   draw of a one-row, no-draft sequence);
 2. one target pass scores the K + 1 positions (the committed prefix and each
    draft prefix);
 3. verification in one kernel launch (``sv_verify_greedy`` or
@@ -56,6 +57,7 @@ class SpeculativeDecoder:
         self.rows = torch.arange(self.B, device=self.device)
         self.drafts = torch.zeros(self.B, self.k, dtype=torch.int32, device=self.device)
         self.draft_logits = None
+        self._no_tokens = torch.zeros(0, dtype=torch.int32, device=self.device)
         self.last = None
         self.graph = None
 
@@ -74,16 +76,19 @@ class SpeculativeDecoder:
 
     def _draw(self, logits: torch.Tensor, u: torch.Tensor) -> torch.Tensor:
         """Greedy argmax (lowest index on ties) or an inverse-CDF draw from
-        softmax(logits / T) per sequence (T = 0 rows are greedy)."""
-        greedy = logits.float().argmax(dim=-1)
+        softmax(logits / T) per sequence (T = 0 rows are greedy): the
+        verification kernel itself, on one row per sequence with no drafts
+        (K_b = 0: the next token is the bonus draw from that row with the
+        given uniform), so the drafts come from the same fp32 weights q that
+        the verification later compares against.  A row the kernel cannot
+        use (NaN, no finite maximum) yields -1, written as token 0."""
+        empty = logits[:0]
+        no_tokens = self._no_tokens
         if self.temperature is None:
-            return greedy.to(torch.int32)
-        t = self.temperature.to(logits.device).float()
-        x = logits.float() / torch.where(t > 0, t, torch.ones_like(t))[:, None]
-        p = torch.softmax(x, dim=-1)
-        c = torch.cumsum(p, dim=-1)
-        idx = torch.searchsorted(c, (u * c[:, -1])[:, None], right=True).squeeze(1).clamp_(max=self.vocab - 1)
-        return torch.where(t > 0, idx, greedy).to(torch.int32)
+            r = api.verify_greedy(logits, no_tokens)
+        else:
+            r = api.accept_from_logits(logits, empty, self.temperature, no_tokens, u.contiguous())
+        return r.next_token.clamp(min=0)
 
     def round(self):
         """One draft / verify / commit round for every sequence (no host sync)."""
