@@ -32,6 +32,8 @@ from .spec_verify import (  # noqa: F401
     NEAR_FILTER,
     NEAR_DECISION,
     DRAW_CERTIFIED,
+    NEAR_EMPTY,
+    EMPTY_PROB_TOL,
     TIGHT_BONUS_REL,
     TIGHT_BONUS_MAX_V,
     softmax_weight_tol,

@@ -36,6 +36,12 @@ Readings of the pages that this file fixes (each restated where it is used):
   relative error ``e`` can take another accept decision only where the
   oracle's test is within ``softmax_decision_tol`` of its threshold; such
   decisions set the oracle-only ``NEAR_DECISION`` bit.
+* Empty residual.  After a rejection the exact residual mass is positive
+  (q(t) > p(t) there) but may be tiny; one whose mass lies within the fp32
+  error band of zero (``EMPTY_PROB_TOL`` for probability rows, the row pair's
+  softmax band for warped rows, the same bound on sum |d(phat - qhat)|) may
+  come out empty in fp32 arithmetic, so the oracle flags it ``NEAR_EMPTY``
+  (and ``NEAR_BOUNDARY``: which id it names is decided by rounding).
 
 Error conventions (a sequence stops at the first row where one applies):
 ``BAD_LAYOUT`` ragged offsets out of range (n = 0, next = -1);
@@ -63,6 +69,7 @@ BAD_LAYOUT = 64
 NEAR_FILTER = 256  # oracle only: a top-p boundary within the filter tolerance
 NEAR_DECISION = 512  # oracle only: an accept test within the softmax tolerance of its threshold
 DRAW_CERTIFIED = 2048  # oracle only: a bonus draw whose id holds within TIGHT_BONUS_REL (below)
+NEAR_EMPTY = 4096  # oracle only: a residual mass within the fp32 error band of zero (below)
 
 BOUNDARY_REL_TOL = 1e-5
 # A bonus draw from f32 probability rows, normalised by any mass Z' (the
@@ -73,6 +80,15 @@ BOUNDARY_REL_TOL = 1e-5
 # farther than that from every step therefore names the same id.
 TIGHT_BONUS_REL = 2.0 ** -21
 TIGHT_BONUS_MAX_V = 1 << 18
+# After a rejection the residual mass R = sum_v max(0, phat_v - qhat_v) is
+# positive in exact arithmetic, but it can be as small as (1 - u) qhat(t).
+# Normalising f32 probability rows in fp32 (a rounded reciprocal of the mass,
+# a rounded product, a rounded difference) moves each term by at most
+# 4u (phat_v + qhat_v) + u |phat_v - qhat_v|, so R by at most 9u < 2^-20.  A
+# residual with R at or below that band may come out empty (ZERO_MASS and a
+# draw from phat) or not, and its draw is decided by rounding: NEAR_EMPTY and
+# NEAR_BOUNDARY.  Warped rows use the softmax band of the row pair instead.
+EMPTY_PROB_TOL = 2.0 ** -20
 
 _TWO_M149 = Fraction(1, 1 << 149)
 
@@ -249,7 +265,9 @@ def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
     return ``(f32 row, error_bits)``; a row is fetched only when the
     left-to-right walk reaches it (llmstudio.ru section 48).  With
     ``decision_tol`` (row -> relative band, for warped rows), a decision
-    within the band of its threshold sets ``NEAR_DECISION``.  With
+    within the band of its threshold sets ``NEAR_DECISION``, and the same
+    band bounds the residual mass that sets ``NEAR_EMPTY`` (sum_v of
+    |d phat_v| <= 2 tol_p + u and of |d qhat_v| <= 2 tol_q + u).  With
     ``certify_bonus`` (probability rows given as they are), a bonus draw
     farther than ``TIGHT_BONUS_REL`` from every step sets ``DRAW_CERTIFIED``."""
     flags = 0
@@ -291,6 +309,9 @@ def _accept_sequence(get_p: RowGetter, get_q: RowGetter, tokens: np.ndarray,
         qhat = q.astype(np.float64) / _frac_to_f64(zq)
         resid = np.maximum(0.0, phat - qhat)
         status = 0
+        band = decision_tol(i) if decision_tol is not None else EMPTY_PROB_TOL
+        if not resid.sum() > band:
+            flags |= NEAR_EMPTY | NEAR_BOUNDARY
         if not resid.sum() > 0.0:
             resid, status = phat, ZERO_MASS
         idx, near = inverse_cdf_draw(resid, u[k])

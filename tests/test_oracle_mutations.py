@@ -30,6 +30,8 @@ MUTATIONS = [
      "w = p.astype(np.float64)[::-1] / _frac_to_f64(zp)", ["pin_enumeration_bonus_law"]),
     ("_accept_sequence", "inverse_cdf_draw(w, u[i], TIGHT_BONUS_REL)", "inverse_cdf_draw(w, u[i], 2.0 ** -30)",
      ["pin_certified_bonus_draws"]),
+    ("_accept_sequence", "if not resid.sum() > band:", "if not resid.sum() > 0.0:",
+     ["pin_near_empty_residual"]),
     ("_greedy_sequence", "return i, a, status\n", "return i, (a + 1) % V, status\n",
      ["pin_greedy_reproduces_plain_decoding"]),
     ("argmax_lowest", "int(cand[0])", "int(cand[-1])",

@@ -503,6 +503,30 @@ def pin_sampling_error_codes():
     assert r == (0, 0, 0)
 
 
+def pin_near_empty_residual():
+    """After a rejection the residual mass is q(t) - p(t) summed the other
+    way: with p = (1/2, 1/2) and q = (1/2 + d, 1/2 - d), rejecting token 0
+    leaves the residual (0, d), whose mass d is flagged NEAR_EMPTY (with
+    NEAR_BOUNDARY) exactly when d is inside the fp32 band; the draw still
+    names token 1, the only one with residual weight."""
+    p = [[0.5, 0.5], [0.5, 0.5]]
+    u = [1.0 - 2.0 ** -24, 0.5]  # u q(0) > p(0) for any d >= 2^-23: a rejection
+    for d, flagged in ((2.0 ** -23, True), (2.0 ** -21, True), (2.0 ** -19, False), (0.0625, False)):
+        assert run_one(p, [[0.5 + d, 0.5 - d]], [0], u) == (
+            0, 1, (o.NEAR_EMPTY | o.NEAR_BOUNDARY) if flagged else 0), d
+    assert o.EMPTY_PROB_TOL == 2.0 ** -20
+    # warped rows: the band is the row pair's softmax band (about 4.4e-5 for
+    # logits near 0 at T = 1), against sigmoid(x) - 1/2 ~ x / 4
+    tgt = np.zeros((2, 2), F32)
+    for x, flagged in ((1e-6, True), (1e-4, True), (1e-3, False), (0.5, False)):
+        dft = np.array([[x, 0.0]], F32)
+        r = o.accept_from_logits(tgt, dft, "f32", np.ones(1, F32), np.zeros(1, np.int32),
+                                 np.array(u, F32), 1, 1)
+        assert (int(r.n_accepted[0]), int(r.next_token[0])) == (0, 1), x
+        assert bool(r.status[0] & o.NEAR_EMPTY) == flagged, (x, r.status[0])
+        assert not flagged or r.status[0] & o.NEAR_BOUNDARY
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
