@@ -88,6 +88,11 @@ typedef enum {
                                     SV_SEQ_TIMEOUT, n = 0, next_token = -1; the
                                     kernel still drains its own copies and
                                     returns normally */
+#define SV_FLAG_PLAN_ROWS 4u     /* take the row-parallel plan where the shape
+                                    allows it (same results; for comparisons) */
+#define SV_FLAG_PLAN_CHAIN 8u    /* take the chain plan (one cluster per
+                                    sequence walking its rows); wins over
+                                    SV_FLAG_PLAN_ROWS */
 
 /*
  * Greedy verification (temperature 0).

@@ -9,6 +9,8 @@ PyTorch binding.  See the spec-verify model card, sections "Method" and
 from ._lib import (  # noqa: F401
     FLAG_EXPIRE_EXCHANGE,
     FLAG_FORCE_EXACT,
+    FLAG_PLAN_CHAIN,
+    FLAG_PLAN_ROWS,
     SEQ_BAD_LAYOUT,
     SEQ_BAD_TOKEN,
     SEQ_BAD_VALUE,

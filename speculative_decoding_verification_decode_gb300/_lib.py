@@ -14,6 +14,8 @@ SEQ_BAD_TOKEN, SEQ_BAD_VALUE, SEQ_ZERO_MASS, SEQ_NEAR_BOUNDARY = 1, 2, 4, 8
 SEQ_EXACT_PATH, SEQ_TIMEOUT, SEQ_BAD_LAYOUT = 16, 32, 64
 FLAG_FORCE_EXACT = 1
 FLAG_EXPIRE_EXCHANGE = 2  # testing aid: exchange waits give up at once (SV_SEQ_TIMEOUT)
+FLAG_PLAN_ROWS = 4  # the row-parallel plan where the shape allows it
+FLAG_PLAN_CHAIN = 8  # the chain plan (wins over FLAG_PLAN_ROWS)
 
 _vp = ctypes.c_void_p
 _i32, _i64, _u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32

@@ -231,7 +231,8 @@ sv_status check_common(const void* target, int64_t row_stride, const int32_t* to
                 static_cast<long long>(B) * K, sum_k);
   if (static_cast<long long>(sum_k) + B > 0x7FFFFFFFLL)
     return fail(SV_ERR_ARG, "too many rows (sum_k + batch > 2^31 - 1)");
-  if (flags & ~static_cast<uint32_t>(SV_FLAG_FORCE_EXACT | SV_FLAG_EXPIRE_EXCHANGE))
+  if (flags & ~static_cast<uint32_t>(SV_FLAG_FORCE_EXACT | SV_FLAG_EXPIRE_EXCHANGE | SV_FLAG_PLAN_ROWS |
+                                     SV_FLAG_PLAN_CHAIN))
     return fail(SV_ERR_ARG, "unknown flag bits 0x%x", flags);
   if (B == 0) return SV_OK;
   if (!target) return fail(SV_ERR_ARG, "target pointer is NULL");
@@ -265,6 +266,38 @@ svk::Params base_params(const void* tgt, const void* drf, int64_t stride, const 
   return p;
 }
 
+// The plan of a call: the row-parallel kernel (sv_rows.cuh) or the chain
+// kernel (sv_verify.cuh).  The chain walks a sequence's rows one dependent
+// link after another; the row-parallel plan decides every row at once but
+// pays a whole launch of items per wave of clusters.  So it takes long
+// drafts (K >= 8, where accepted chains can be long) whose items fit in about
+// two waves of three CTAs per SM.  Measured on GB300: sampling, K = 40 at
+// acceptance 0.995, twelve sequences of V = 3001, 35 us against 517 us;
+// K = 16, four sequences of V = 32000, 23 against 50 us; K = 8, eight
+// sequences of V = 128256 bf16, 34 against 40 us; greedy with every draft
+// accepted, K = 8, eight sequences of V = 128256, 19 against 36 us (with none
+// accepted, one sequence of V = 32000, 13 against 9 us); while B = 64, K = 5
+// at V = 128256 (six waves of items) takes 68 against 60 us.
+bool choose_rows(uint32_t flags, int mode, int elem, const svk::Params& p) {
+  if (flags & SV_FLAG_PLAN_CHAIN) return false;
+  const int C = svh::rows_cluster_size(mode, elem, p);
+  if (C == 0) return false;
+  if (flags & SV_FLAG_PLAN_ROWS) return true;
+  const long long ctas = static_cast<long long>(C) * p.B * (p.K + 1LL);
+  return p.K >= 8 && ctas <= 6LL * sm_count();
+}
+
+// Launches the row-parallel plan; false (error message cleared) when it
+// declined the call (no scratch slot for the stream), so the chain plan runs.
+bool try_rows(int mode, sv_dtype dtype, const svk::Params& p, bool filtered, cudaStream_t st, sv_status& out) {
+  out = svh::launch_rows(mode, dtype, p, filtered, st);
+  if (out == SV_ERR_UNSUPPORTED) {
+    g_err[0] = '\0';
+    return false;
+  }
+  return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -285,6 +318,8 @@ sv_status sv_verify_greedy(const void* target, sv_dtype dtype, int64_t row_strid
                               batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
   p.use_tma = aligned16(target) && (row_stride * elem) % 16 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  sv_status rs;
+  if (choose_rows(flags, svk::MODE_GREEDY, elem, p) && try_rows(svk::MODE_GREEDY, dtype, p, false, st, rs)) return rs;
   switch (dtype) {
     case SV_F32: return launch<svk::MODE_GREEDY, float>(p, pl, st);
     case SV_BF16: return launch<svk::MODE_GREEDY, __nv_bfloat16>(p, pl, st);
@@ -308,6 +343,10 @@ sv_status sv_accept(const float* target_probs, const float* draft_probs, int64_t
                               nullptr, batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
   p.use_tma = aligned16(target_probs) && (!draft_probs || aligned16(draft_probs)) &&
               (row_stride * 4) % 16 == 0;
+  sv_status rs;
+  if (choose_rows(flags, svk::MODE_PROBS, 4, p) &&
+      try_rows(svk::MODE_PROBS, SV_F32, p, false, static_cast<cudaStream_t>(stream), rs))
+    return rs;
   return launch<svk::MODE_PROBS, float>(p, pl, static_cast<cudaStream_t>(stream));
 }
 
@@ -343,6 +382,10 @@ sv_status svh::accept_logits(const void* target_logits, const void* draft_logits
   p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
               (row_stride * elem) % 16 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  sv_status rs;
+  if (choose_rows(flags, svk::MODE_LOGITS, elem, p) &&
+      try_rows(svk::MODE_LOGITS, dtype, p, floor_target || floor_draft, st, rs))
+    return rs;
   switch (dtype) {
     case SV_F32: return launch<svk::MODE_LOGITS, float>(p, pl, st);
     case SV_BF16: return launch<svk::MODE_LOGITS, __nv_bfloat16>(p, pl, st);

@@ -1,6 +1,12 @@
 // Host helpers shared by the library's translation units (not part of the ABI).
 #pragma once
+#include <cuda_runtime.h>
+
 #include "../../include/sv.h"
+
+namespace svk {
+struct Params;
+}
 
 namespace svh {
 
@@ -20,5 +26,13 @@ sv_status accept_logits(const void* target_logits, const void* draft_logits, sv_
                         const float* floor_draft, int32_t* n_accepted, int32_t* next_token,
                         uint32_t* status, float* warped_target_out, float* warped_draft_out,
                         const uint32_t* ext_err, uint32_t flags, void* stream);
+
+// The row-parallel plan (sv_rows.cu): the cluster size it would launch a
+// call of this shape with (0: the shape cannot take it), and its launch
+// (SV_ERR_UNSUPPORTED when no scratch slot is free for the stream, or the
+// shape does not fit; the caller then takes the chain plan).  `p` carries the
+// call's arguments as the chain kernel's parameters do.
+int rows_cluster_size(int mode, int elem, const svk::Params& p);
+sv_status launch_rows(int mode, sv_dtype dtype, const svk::Params& p, bool filtered, cudaStream_t stream);
 
 }  // namespace svh

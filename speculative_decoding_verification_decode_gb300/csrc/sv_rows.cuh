@@ -1,0 +1,948 @@
+// Row-parallel verification: one thread-block cluster per (row, sequence).
+//
+// The chain kernel (sv_verify.cuh) walks the rows of a sequence one after
+// another, so a batch whose sequences fit one wave of clusters waits on a
+// chain of dependent row links.  Here every row i of every sequence b is an
+// item of its own, processed by a cluster of C CTAs that hold their slices
+// of target row i and draft row i in shared memory:
+//   * items are numbered row-major (i * B + b), so row 0 of every sequence is
+//     launched first; an item whose sequence has already posted a terminal
+//     row before i (a rejection, an error, a miss) skips its loads and work;
+//   * the cluster takes the row's decision exactly as the chain kernel does
+//     (the same defined weights, the same exact predicate and fallback), and,
+//     if the row ends its sequence by a rejection or is the bonus row, its
+//     inverse-CDF draw from the resident slices (no second read of the row);
+//   * each item writes a small record of its outcome to global scratch and
+//     counts itself in; the last item of a sequence to arrive (an atomic
+//     counter, no waiting) combines the records left to right, writes the
+//     sequence's outputs, and resets the counter and the posted row for the
+//     next launch.
+// Nothing waits on another cluster: the only waits are on the CTA's own bulk
+// copies and on the cluster's exchanges, all bounded.
+#pragma once
+#include "sv_verify.cuh"
+
+namespace svk {
+
+constexpr int kRowsThreads = 256;  // 8 warps, every one reduces
+constexpr uint32_t kRecTerminal = 0x80000000u;
+constexpr int kRowsExchanges = 5;  // maxima / sums, masses, exact limbs, draw, draw from p
+
+struct RowsParams {
+  Params p;
+  int* seq_count;  // per sequence: items arrived (0 between launches)
+  int* seq_first;  // per sequence: INT_MAX - (first terminal row posted), 0 when none
+  uint4* rec;      // per target row: {status | kRecTerminal, next, n, 0}
+  int nadd;        // fp32 additions of any element inside its thread (mass bounds)
+  int x_off;       // byte offset of the draft slice
+  int vsum_off;    // byte offset of the draw's group sums / the exact buckets
+  int tail_off;    // byte offset of RowsTail
+};
+
+struct __align__(16) RowsTail {
+  uint32_t xr[4][kMaxCluster][8];  // records of exchanges 0, 1, 3, 4
+  uint32_t xe[kMaxCluster][32];    // records of exchange 2 (exact limbs)
+  uint32_t my[32];                 // this CTA's outgoing record
+  uint64_t xbar[kRowsExchanges];
+  uint64_t full;
+  float wf[kWarps][4];
+  int wi[kWarps][4];
+  unsigned long long wu[kWarps];
+  uint32_t lp[kLimbs], lq[kLimbs], infl;
+  // decision inputs of the item's row, loaded while the slices stream in
+  int t;
+  float u, ud, gp, gq, lo_p, lo_q;
+  int skip;
+  // the cluster's view after an exchange (written by warp 0)
+  float fv[4];
+  uint32_t iv[4];
+  float dpar[4];
+  int bi[4];
+  // rank 0: the drawn id and status pushed by the draw's owner
+  int out_tok;
+  uint32_t out_st;
+};
+
+// NaN-propagating maximum of a shared-memory slice of n elements (+-Inf
+// count as values), over the CTA's 256 threads; the thread's partial.
+template <typename T>
+__device__ __forceinline__ float slice_max_nan(const T* s, int n) {
+  constexpr int VEC = ElemTraits<T>::kVec;
+  const int nv = n / VEC;
+  float m = -kInfF;
+  if constexpr (sizeof(T) == 4) {
+    for (int vi = threadIdx.x; vi < nv; vi += kRowsThreads) {
+      const float4 v = reinterpret_cast<const float4*>(s)[vi];
+      m = fmax_nan(m, fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w)));
+    }
+  } else {
+    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+    uint32_t h = kBf ? 0xFF80FF80u : 0xFC00FC00u;
+    for (int vi = threadIdx.x; vi < nv; vi += kRowsThreads) {
+      const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+      if constexpr (kBf) h = bf16x2_max_nan(h, bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w)));
+      else h = f16x2_max_nan(h, f16x2_max_nan(f16x2_max_nan(v.x, v.y), f16x2_max_nan(v.z, v.w)));
+    }
+    m = kBf ? fmax_nan(bf_lo(h), bf_hi(h)) : fmax_nan(h_lo(h), h_hi(h));
+  }
+  for (int e = nv * VEC + threadIdx.x; e < n; e += kRowsThreads) m = fmax_nan(m, ElemTraits<T>::to_f(s[e]));
+  return m;
+}
+
+// fp32 sum of the defined weights wf(l) of a shared-memory slice: a pairwise
+// tree per 16-byte vector, added into the thread's sum (one addition per
+// vector, plus one per tail element); four vectors at a time for independent
+// exponentials.
+template <typename T, typename W>
+__device__ __forceinline__ float slice_mass(const T* s, int n, const W& wf) {
+  constexpr int VEC = ElemTraits<T>::kVec;
+  constexpr int U = 4;
+  const int nv = n / VEC;
+  Acc a;
+  a.init();
+  for (int base = threadIdx.x; base < nv; base += U * kRowsThreads) {
+    float t[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int vi = base + u * kRowsThreads;
+      float x[VEC], e[VEC];
+      if (vi < nv) unpack_vec<T>(reinterpret_cast<const uint4*>(s)[vi], x);
+#pragma unroll
+      for (int k = 0; k < VEC; ++k) e[k] = vi < nv ? wf(x[k]) : 0.f;
+      t[u] = tree_sum<VEC>(e);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u * kRowsThreads < nv) a.add(t[u]);
+  }
+  for (int e = nv * VEC + threadIdx.x; e < n; e += kRowsThreads) a.add(wf(ElemTraits<T>::to_f(s[e])));
+  return a.f;
+}
+
+// Draw weights of vector vi of a resident slice pair (q may be null): VEC
+// entries, zero past the slice end; returns the number of real elements.
+template <typename T, typename D>
+__device__ __forceinline__ int smem_draw_weights(const T* p, const T* q, int n, int vi, const D& dw, float* r) {
+  constexpr int VEC = ElemTraits<T>::kVec;
+  const int e0 = vi * VEC;
+  float xp[VEC], xq[VEC];
+  int cnt = VEC;
+  if (e0 + VEC <= n) {
+    unpack_vec<T>(reinterpret_cast<const uint4*>(p)[vi], xp);
+    if (q) unpack_vec<T>(reinterpret_cast<const uint4*>(q)[vi], xq);
+  } else {
+    cnt = n - e0;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      xp[k] = k < cnt ? ElemTraits<T>::to_f(p[e0 + k]) : 0.f;
+      xq[k] = (q && k < cnt) ? ElemTraits<T>::to_f(q[e0 + k]) : 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < VEC; ++k) r[k] = k < cnt ? dw(xp[k], q ? xq[k] : 0.f) : 0.f;
+  return cnt;
+}
+
+}  // namespace svk
+
+namespace svk {
+
+enum : int { OUT_ACCEPT = 0, OUT_TERM = 1, OUT_SKIP = 2, OUT_TIMEOUT = 3, OUT_DRAW = 4 };
+
+template <int MODE, typename T, bool FL = false>
+__global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_constant__ RowsParams R) {
+  static_assert(kRowsThreads == kConsumers, "the chunk passes stride by kConsumers threads");
+  const Params& P = R.p;
+  using TR = ElemTraits<T>;
+  constexpr int VEC = TR::kVec;
+  using WarpT =
+      typename std::conditional<MODE == MODE_LOGITS, typename WarpOf<T>::type, NoWarp>::type;
+  using DrawT = typename std::conditional<MODE == MODE_LOGITS, DrawLogits<FL>, DrawProbs>::type;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  T* sp = reinterpret_cast<T*>(smem);
+  T* sq = reinterpret_cast<T*>(smem + R.x_off);
+  unsigned long long* vsum = reinterpret_cast<unsigned long long*>(smem + R.vsum_off);
+  RowsTail& sm = *reinterpret_cast<RowsTail*>(smem + R.tail_off);
+  const int tid = threadIdx.x;
+  const int warp = __shfl_sync(0xFFFFFFFFu, tid >> 5, 0);
+  const int lane = tid & 31;
+  const uint32_t C = cluster_size();
+  const uint32_t rank = cluster_rank();
+  const long long item = blockIdx.x / C;
+  const int b = static_cast<int>(item % P.B);
+  const int i = static_cast<int>(item / P.B);
+
+  // ---------------------------------------------------------------- sequence layout
+  int kb = P.K;
+  long long t0 = static_cast<long long>(b) * (P.K + 1LL), d0 = static_cast<long long>(b) * P.K;
+  bool layout_ok = true;
+  if (P.cu_k) {
+    const int lo = P.cu_k[b], hi = P.cu_k[b + 1];
+    if (lo < 0 || hi < lo || hi > P.sum_k || hi - lo > P.K) {
+      layout_ok = false;
+    } else {
+      kb = hi - lo;
+      t0 = lo + static_cast<long long>(b);
+      d0 = lo;
+    }
+  }
+  bool sampling = MODE != MODE_GREEDY;
+  float temp = 0.f;
+  bool temp_ok = true;
+  if (MODE == MODE_LOGITS && layout_ok) {
+    temp = P.temp[b];
+    temp_ok = temp >= 0.f && temp <= FLT_MAX;
+    sampling = temp > 0.f;
+  }
+  if (!layout_ok || !temp_ok) {  // row 0's item reports it; no other item of b takes part
+    if (i == 0 && rank == 0 && tid == 0) {
+      P.n_out[b] = 0;
+      P.next_out[b] = -1;
+      P.st_out[b] = (layout_ok ? ST_BAD_VALUE : ST_BAD_LAYOUT) | (P.ext_err && *P.ext_err ? ST_TIMEOUT : 0u);
+    }
+    return;
+  }
+  if (i > kb) return;  // the whole cluster shares b and i
+  const bool bonus = i == kb;
+  const bool two = sampling && !bonus;  // the item also holds draft row i
+
+  const T* tgt = static_cast<const T*>(P.tgt);
+  const T* drf = static_cast<const T*>(P.drf);
+  const int v_lo = static_cast<int>(rank) * P.slice;
+  const int n_el = max(0, min(P.V, v_lo + P.slice) - v_lo);
+  const T* rowp = tgt + (t0 + i) * P.stride + v_lo;
+  const T* rowq = two ? drf + (d0 + i) * P.stride + v_lo : nullptr;
+
+  if (tid == 0) {
+    int skip = 0;
+    if (i > 0) {  // an earlier row of b already ended the sequence
+      const int s = *reinterpret_cast<const volatile int*>(R.seq_first + b);
+      skip = (s != 0 && INT_MAX - s < i) ? 1 : 0;
+    }
+    sm.skip = skip;
+    for (int x = 0; x < kRowsExchanges; ++x) mbar_init(&sm.xbar[x], C);
+    mbar_init(&sm.full, 1);
+    sm.out_tok = INT_MIN;
+    sm.out_st = 0u;
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  const bool skip_mine = sm.skip != 0;
+
+  // ---------------------------------------------------------------- loads
+  if (!skip_mine) {
+    if (P.use_tma) {
+      if (warp == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(n_el) * static_cast<uint32_t>(sizeof(T));
+        const uint32_t tma = bytes & ~15u;
+        for (int e = static_cast<int>(tma / sizeof(T)) + lane; e < n_el; e += 32) {
+          sp[e] = rowp[e];
+          if (two) sq[e] = rowq[e];
+        }
+        __syncwarp();
+        if (lane == 0) {
+          if (tma) {
+            mbar_arrive_expect_tx(&sm.full, two ? 2u * tma : tma);
+            bulk_g2s(sp, rowp, tma, &sm.full);
+            if (two) bulk_g2s(sq, rowq, tma, &sm.full);
+          } else {
+            mbar_arrive_local(&sm.full);
+          }
+        }
+      }
+    } else {
+      for (int e = tid; e < n_el; e += kRowsThreads) {
+        sp[e] = rowp[e];
+        if (two) sq[e] = rowq[e];
+      }
+    }
+    if (tid == 32) {  // the row's decision inputs, while the slices stream in
+      int t = -1;
+      float gpv = 0.f, gqv = 0.f;
+      if (!bonus) {
+        t = ld_issue_s32(P.tok + d0 + i);
+        if (sampling && t >= 0 && t < P.V) {
+          gpv = TR::to_f(tgt[(t0 + i) * P.stride + t]);
+          gqv = TR::to_f(drf[(d0 + i) * P.stride + t]);
+        }
+      }
+      sm.t = t;
+      sm.gp = gpv;
+      sm.gq = gqv;
+      sm.u = sampling ? P.uni[t0 + i] : 0.f;
+      sm.ud = sampling ? P.uni[t0 + kb] : 0.f;
+      float lp = -kInfF, lq = -kInfF;
+      if constexpr (FL) {
+        if (P.flo_t) lp = __ldg(P.flo_t + t0 + i);
+        if (P.flo_d && two) lq = __ldg(P.flo_d + d0 + i);
+      }
+      sm.lo_p = lp;
+      sm.lo_q = lq;
+    }
+  }
+  cluster_sync_all();  // every peer runs and its barriers exist before the first remote arrive
+  int bad = 0;  // this CTA's wait for its own copies gave up
+  if (!skip_mine && P.use_tma) bad = mbar_wait_bounded(&sm.full, 0u) ? 0 : 1;
+  __syncthreads();
+
+  // Exchange of sm.my with every CTA of the cluster through exchange slot x
+  // (a collective of warp 0; each slot's barrier completes once per launch).
+  auto exchange = [&](int x, int words) -> bool {
+    warp_converged();
+    __syncwarp();
+    uint32_t* base = x == 2 ? &sm.xe[0][0] : &sm.xr[x < 2 ? x : x - 1][0][0];
+    const int stride = x == 2 ? 32 : 8;
+    if (lane < static_cast<int>(C)) {
+      const uint32_t dst = dsmem_addr(base + rank * stride, static_cast<uint32_t>(lane));
+      for (int w = 0; w < words; w += 4) dsmem_st_v4(dst + 4u * w, *reinterpret_cast<const uint4*>(&sm.my[w]));
+      dsmem_arrive_release(dsmem_addr(&sm.xbar[x], static_cast<uint32_t>(lane)));
+    }
+    const bool ok =
+        mbar_wait_cluster_bounded(&sm.xbar[x], 0u, (P.flags & FLAG_EXPIRE_EXCHANGE) ? 0u : kWaitPolls);
+    return __all_sync(0xFFFFFFFFu, ok) != 0;
+  };
+  auto xrec = [&](int x, int c, int w) -> uint32_t {
+    return x == 2 ? sm.xe[c][w] : sm.xr[x < 2 ? x : x - 1][c][w];
+  };
+  auto xrecf = [&](int x, int c, int w) -> float { return __uint_as_float(xrec(x, c, w)); };
+  auto post_terminal = [&]() {  // rank 0: later rows of b may skip
+    if (rank == 0 && tid == 0) atomicMax(R.seq_first + b, INT_MAX - i);
+  };
+
+  int out = OUT_TIMEOUT;  // the item's outcome (the same in every CTA of the cluster)
+  int o_n = 0, o_next = -1;
+  uint32_t o_st = 0u;
+
+  if (!sampling) {
+    // ============================================================== greedy: argmax of target row i
+    float bv = __int_as_float(0x7FFFFFFF);  // NaN: no candidate yet
+    int bi = INT_MAX;
+    uint32_t nanf = 0;
+    if (!skip_mine) chunk_argmax<T>(sp, n_el, v_lo, bv, bi, nanf);
+    if (bv != bv) bi = INT_MAX;
+    warp_converged();
+    warp_argmax(bv, bi);
+    const uint32_t fl = __reduce_or_sync(0xFFFFFFFFu, nanf);
+    if (lane == 0) {
+      sm.wf[warp][0] = bv;
+      sm.wi[warp][0] = bi;
+      sm.wi[warp][1] = static_cast<int>(fl);
+    }
+    bad = __syncthreads_or(bad);
+    if (warp == 0) {
+      warp_converged();
+      float v = lane < kWarps ? sm.wf[lane][0] : 0.f;
+      int a = lane < kWarps ? sm.wi[lane][0] : INT_MAX;
+      const uint32_t f = __reduce_or_sync(0xFFFFFFFFu, lane < kWarps ? static_cast<uint32_t>(sm.wi[lane][1]) : 0u);
+      warp_argmax(v, a);
+      if (lane == 0) {
+        sm.my[0] = __float_as_uint(v);
+        sm.my[1] = static_cast<uint32_t>(a);
+        sm.my[2] = f | (bad ? 2u : 0u) | (skip_mine ? 4u : 0u);
+        sm.my[3] = 0u;
+      }
+      uint32_t g = 2u;
+      int ga = INT_MAX;
+      if (exchange(0, 4)) {
+        const bool cl = lane < static_cast<int>(C);
+        v = cl ? xrecf(0, lane, 0) : 0.f;
+        a = cl ? static_cast<int>(xrec(0, lane, 1)) : INT_MAX;
+        g = __reduce_or_sync(0xFFFFFFFFu, cl ? xrec(0, lane, 2) : 0u);
+        warp_argmax(v, a);
+        ga = a;
+      }
+      if (lane == 0) {
+        sm.iv[0] = g;
+        sm.bi[0] = ga;
+      }
+    }
+    __syncthreads();
+    const uint32_t g = sm.iv[0];
+    int a = sm.bi[0];
+    if (g & 2u) {
+      out = OUT_TIMEOUT;
+    } else if (g & 4u) {
+      out = OUT_SKIP;
+    } else {
+      if (a == INT_MAX) a = 0;  // an all-NaN row
+      o_st = (g & 1u) ? ST_BAD_VALUE : 0u;
+      o_next = a;
+      out = OUT_TERM;
+      if (bonus) {
+        o_n = kb;
+      } else {
+        const int t = sm.t;
+        o_n = i;
+        if (t < 0 || t >= P.V) o_st |= ST_BAD_TOKEN;
+        else if (t == a) out = OUT_ACCEPT;
+      }
+      if (out == OUT_TERM) post_terminal();
+    }
+  } else {
+    // ============================================================== sampling
+    float khi = 0.f, klo = 0.f;
+    if (MODE == MODE_LOGITS) log2e_over(temp, khi, klo);
+    auto make_warp = [&](float m, float lo) {
+      WarpT w;
+      if constexpr (MODE == MODE_LOGITS) {
+        if constexpr (sizeof(T) == 4) {
+          w.m = m;
+          w.khi = khi;
+          w.klo = klo;
+        } else {
+          w.m = m;
+          w.k = khi;
+        }
+      }
+      w.lo = lo;
+      (void)m;
+      return w;
+    };
+
+    // ---- exact masses of the row from the resident slices (collective);
+    // the summed limbs and +Inf flags land in sm.lp / sm.lq / sm.infl
+    auto exact_pass = [&](const WarpT& fp, const WarpT& fq) -> bool {
+      for (int k = tid; k < 2 * kBuckets; k += kRowsThreads) vsum[k] = 0ull;
+      __syncthreads();
+      int bp = 0, bq = 0;
+      for (int e = tid; e < n_el; e += kRowsThreads) {
+        const float x = fp(TR::to_f(sp[e]));
+        if (!(x <= FLT_MAX)) bp = 1;  // +Inf (NaN and negatives were rejected before)
+        else bucket_add(vsum, x);
+        if (two) {
+          const float y = fq(TR::to_f(sq[e]));
+          if (!(y <= FLT_MAX)) bq = 1;
+          else bucket_add(vsum + kBuckets, y);
+        }
+      }
+      bp = __syncthreads_or(bp);
+      bq = __syncthreads_or(bq);
+      if (tid == 0) {
+        buckets_to_limbs(vsum, &sm.my[0]);
+        buckets_to_limbs(vsum + kBuckets, &sm.my[kLimbs]);
+        sm.my[2 * kLimbs] = (bp ? 1u : 0u) | (bq ? 2u : 0u);
+        sm.my[2 * kLimbs + 1] = sm.my[2 * kLimbs + 2] = sm.my[2 * kLimbs + 3] = 0u;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const bool ok = exchange(2, 2 * kLimbs + 4);
+        if (lane == 0) {
+          if (ok) {
+            unsigned long long ap[kLimbs], aq[kLimbs];
+            for (int k = 0; k < kLimbs; ++k) ap[k] = aq[k] = 0ull;
+            uint32_t infl = 0;
+            for (uint32_t c = 0; c < C; ++c) {
+              for (int k = 0; k < kLimbs; ++k) {
+                ap[k] += xrec(2, c, k);
+                aq[k] += xrec(2, c, kLimbs + k);
+              }
+              infl |= xrec(2, c, 2 * kLimbs);
+            }
+            unsigned long long cp = 0, cq = 0;
+            for (int k = 0; k < kLimbs; ++k) {
+              cp += ap[k];
+              cq += aq[k];
+              sm.lp[k] = static_cast<uint32_t>(cp);
+              sm.lq[k] = static_cast<uint32_t>(cq);
+              cp >>= 32;
+              cq >>= 32;
+            }
+            sm.infl = infl;
+          }
+          sm.bi[1] = ok ? 1 : 0;
+        }
+      }
+      __syncthreads();
+      return sm.bi[1] != 0;
+    };
+
+    // ---- pass A: probabilities: masses and minima; logits: maxima
+    uint32_t flags = 1u;  // cluster view: 1 a wait gave up, 2 / 4 target / draft row invalid, 8 skip
+    float mp = -kInfF, mq = -kInfF;
+    DF Zp = {0.f, 0.f}, Zq = {0.f, 0.f};
+    float Bp = 0.f, Bq = 0.f;
+    if constexpr (MODE == MODE_PROBS) {
+      Acc ap, aq;
+      ap.init();
+      aq.init();
+      float mnp = kInfF, mnq = kInfF;
+      if (!skip_mine) {
+        chunk_mass_f32(reinterpret_cast<const float*>(sp), n_el, ap, mnp);
+        if (two) chunk_mass_f32(reinterpret_cast<const float*>(sq), n_el, aq, mnq);
+      }
+      warp_converged();
+      const float s0 = warp_sum_f(ap.f), s1 = warp_sum_f(aq.f);
+      const float m0 = warp_min_nan_f(mnp), m1 = warp_min_nan_f(mnq);
+      if (lane == 0) {
+        sm.wf[warp][0] = s0;
+        sm.wf[warp][1] = s1;
+        sm.wf[warp][2] = m0;
+        sm.wf[warp][3] = m1;
+      }
+      bad = __syncthreads_or(bad);
+      if (warp == 0) {
+        warp_converged();
+        const bool wl = lane < kWarps;
+        const float c0 = warp_sum_f<8>(wl ? sm.wf[lane][0] : 0.f);
+        const float c1 = warp_sum_f<8>(wl ? sm.wf[lane][1] : 0.f);
+        const float n0 = warp_min_nan_f<8>(wl ? sm.wf[lane][2] : kInfF);
+        const float n1 = warp_min_nan_f<8>(wl ? sm.wf[lane][3] : kInfF);
+        if (lane == 0) {
+          sm.my[0] = __float_as_uint(c0);
+          sm.my[1] = __float_as_uint(c1);
+          sm.my[2] = (bad ? 1u : 0u) | (n0 >= 0.f ? 0u : 2u) | (n1 >= 0.f ? 0u : 4u) | (skip_mine ? 8u : 0u);
+          sm.my[3] = 0u;
+        }
+        float zp = 0.f, zq = 0.f;
+        uint32_t f = 1u;
+        if (exchange(0, 4)) {
+          const bool cl = lane < static_cast<int>(C);
+          zp = warp_sum_f<16>(cl ? xrecf(0, lane, 0) : 0.f);
+          zq = warp_sum_f<16>(cl ? xrecf(0, lane, 1) : 0.f);
+          f = __reduce_or_sync(0xFFFFFFFFu, cl ? xrec(0, lane, 2) : 0u);
+        }
+        if (lane == 0) {
+          sm.fv[0] = zp;
+          sm.fv[1] = zq;
+          sm.iv[0] = f;
+        }
+      }
+      __syncthreads();
+      Zp.hi = sm.fv[0];
+      Zq.hi = sm.fv[1];
+      flags = sm.iv[0];
+      Bp = sum_bound(Zp.hi, R.nadd);
+      Bq = sum_bound(Zq.hi, R.nadd);
+    } else {
+      float xp = -kInfF, xq = -kInfF;
+      if (!skip_mine) {
+        xp = slice_max_nan<T>(sp, n_el);
+        if (two) xq = slice_max_nan<T>(sq, n_el);
+      }
+      warp_converged();
+      xp = warp_max_nan_f(xp);
+      xq = warp_max_nan_f(xq);
+      if (lane == 0) {
+        sm.wf[warp][0] = xp;
+        sm.wf[warp][1] = xq;
+      }
+      bad = __syncthreads_or(bad);
+      if (warp == 0) {
+        warp_converged();
+        const bool wl = lane < kWarps;
+        const float c0 = warp_max_nan_f<8>(wl ? sm.wf[lane][0] : -kInfF);
+        const float c1 = warp_max_nan_f<8>(wl ? sm.wf[lane][1] : -kInfF);
+        if (lane == 0) {
+          sm.my[0] = __float_as_uint(c0);
+          sm.my[1] = __float_as_uint(c1);
+          sm.my[2] = (bad ? 1u : 0u) | (skip_mine ? 8u : 0u);
+          sm.my[3] = 0u;
+        }
+        float gp = -kInfF, gq = -kInfF;
+        uint32_t f = 1u;
+        if (exchange(0, 4)) {
+          const bool cl = lane < static_cast<int>(C);
+          gp = warp_max_nan_f<16>(cl ? xrecf(0, lane, 0) : -kInfF);
+          gq = warp_max_nan_f<16>(cl ? xrecf(0, lane, 1) : -kInfF);
+          f = __reduce_or_sync(0xFFFFFFFFu, cl ? xrec(0, lane, 2) : 0u);
+        }
+        if (lane == 0) {
+          sm.fv[0] = gp;
+          sm.fv[1] = gq;
+          sm.iv[0] = f;
+        }
+      }
+      __syncthreads();
+      mp = sm.fv[0];
+      mq = sm.fv[1];
+      flags = sm.iv[0];
+      if (!(mp < kInfF)) flags |= 2u;  // a NaN or +Inf logit
+      if (two && !(mq < kInfF)) flags |= 4u;
+    }
+
+    // ---- inverse-CDF draw over the resident slices (collective).  Returns
+    // 0 when done (the owner pushed the id to rank 0), 1 when the residual
+    // is empty, 2 when p itself has no draw mass, -1 when an exchange gave up.
+    auto draw = [&](const DrawT& dw, bool resid, int x, uint32_t st_in, float ud) -> int {
+      const T* qs = resid ? sq : nullptr;
+      const int nvt = (n_el + VEC - 1) / VEC;
+      const int ng = (nvt + kGroupVecs - 1) / kGroupVecs;
+      constexpr int U = 4;
+      constexpr int LG = kGroupVecs / U;  // lanes per group
+      static_assert(LG == 8, "group sums reduce over 8 lanes");
+      unsigned long long mine = 0;
+      for (int it = 0; it * kRowsThreads * U < nvt; ++it) {  // same trip count for every thread
+        const int v0 = (it * kRowsThreads + tid) * U;
+        unsigned long long fs = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int vi = v0 + u;
+          if (vi < nvt) {
+            float r[VEC];
+            smem_draw_weights<T>(sp, qs, n_el, vi, dw, r);
+            fs += dw.fix(seq_sum<VEC>(r));
+          }
+        }
+        mine += fs;
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 1);
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 2);
+        fs += __shfl_xor_sync(0xFFFFFFFFu, fs, 4);
+        const int g = v0 / kGroupVecs;
+        if ((lane & (LG - 1)) == 0 && g < ng) vsum[g] = fs;
+      }
+      warp_converged();
+      mine = warp_sum_u64(mine);
+      if (lane == 0) sm.wu[warp] = mine;
+      __syncthreads();
+      if (warp == 0) {
+        warp_converged();
+        const unsigned long long tot = warp_sum_u64(lane < kWarps ? sm.wu[lane] : 0ull);
+        if (lane == 0) {
+          sm.my[0] = static_cast<uint32_t>(tot);
+          sm.my[1] = static_cast<uint32_t>(tot >> 32);
+          sm.my[2] = sm.my[3] = 0u;
+        }
+        int code = -1;
+        if (exchange(x, 4)) {
+          warp_converged();
+          const unsigned long long rc =
+              lane < static_cast<int>(C)
+                  ? (static_cast<unsigned long long>(xrec(x, lane, 0)) |
+                     (static_cast<unsigned long long>(xrec(x, lane, 1)) << 32))
+                  : 0ull;
+          unsigned long long inc = rc;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += n;
+          }
+          const unsigned long long Rt = __shfl_sync(0xFFFFFFFFu, inc, 31);
+          if (Rt == 0) {
+            code = resid ? 1 : 2;
+          } else {
+            const unsigned long long tau = tau_of(ud, Rt);
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, lane < static_cast<int>(C) && tau < inc);
+            const int owner = hit ? __ffs(hit) - 1 : -1;
+            const unsigned long long before = owner >= 0 ? __shfl_sync(0xFFFFFFFFu, inc - rc, owner) : 0ull;
+            if (owner < 0) {
+              code = -1;  // cannot happen: tau < Rt
+            } else if (owner == static_cast<int>(rank)) {
+              code = 3;  // this CTA walks its slice
+              if (lane == 0) {
+                sm.wu[0] = tau - before;
+                sm.wu[1] = Rt;
+              }
+            } else {
+              code = 0;
+            }
+          }
+        }
+        if (lane == 0) sm.bi[0] = code;
+      }
+      __syncthreads();
+      const int code = sm.bi[0];
+      if (code != 3) return code;
+      if (warp != 0) return 0;
+      // ---- the owner's warp 0: a scan of the group sums (lane l takes a run
+      // of consecutive groups), then the crossing group's vectors, then one
+      // vector's elements, all from shared memory
+      warp_converged();
+      const unsigned long long tloc = sm.wu[0];
+      const double Rd = static_cast<double>(sm.wu[1]);
+      const int seg = (ng + 31) / 32;
+      const int lo = min(ng, lane * seg), hi = min(ng, lo + seg);
+      unsigned long long s = 0;
+      for (int g = lo; g < hi; ++g) s += vsum[g];
+      unsigned long long inc = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += n;
+      }
+      const unsigned long long ex = inc - s;
+      const uint32_t seg_hit = __ballot_sync(0xFFFFFFFFu, tloc >= ex && tloc < inc);
+      int g_hit = -1;
+      unsigned long long c0 = 0;
+      if (seg_hit) {
+        const int L = __ffs(seg_hit) - 1;
+        if (lane == L) {
+          c0 = ex;
+          int g = lo;
+          for (; g < hi - 1; ++g) {
+            if (tloc < c0 + vsum[g]) break;
+            c0 += vsum[g];
+          }
+          g_hit = g;
+        }
+        g_hit = __shfl_sync(0xFFFFFFFFu, g_hit, L);
+        c0 = __shfl_sync(0xFFFFFFFFu, c0, L);
+      }
+      int found = -1, near_b = 0;
+      if (g_hit >= 0) {
+        const int v = g_hit * kGroupVecs + lane;
+        float r[VEC];
+        int cnt = 0;
+        unsigned long long f = 0;
+        if (v < nvt) {
+          cnt = smem_draw_weights<T>(sp, qs, n_el, v, dw, r);
+          f = dw.fix(seq_sum<VEC>(r));
+        }
+        unsigned long long vinc = f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, vinc, o);
+          if (lane >= o) vinc += n;
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, v < nvt && tloc < c0 + vinc);
+        if (hit) {
+          const int L = __ffs(hit) - 1;
+          if (lane == L) {
+            const unsigned long long cv = c0 + vinc - f;  // the CDF before this vector
+            float acc = r[0];
+            unsigned long long prev = cv;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+              if (k > 0) acc = __fadd_rn(acc, r[k]);
+              const unsigned long long cur = cv + dw.fix(acc);
+              if (k < cnt && (tloc < cur || k == cnt - 1)) {
+                const unsigned long long dlo = tloc - prev, dhi = cur > tloc ? cur - tloc : 0ull;
+                const unsigned long long dmin = dlo < dhi ? dlo : dhi;
+                found = v_lo + v * VEC + k;
+                near_b = static_cast<double>(dmin) <= 1e-5 * Rd ? 1 : 0;
+                break;
+              }
+              prev = cur;
+            }
+          }
+          found = __shfl_sync(0xFFFFFFFFu, found, L);
+          near_b = __shfl_sync(0xFFFFFFFFu, near_b, L);
+        }
+      }
+      if (lane == 0) {
+        const uint32_t sfin = found >= 0 ? (st_in | (near_b ? ST_NEAR : 0u)) : ST_TIMEOUT;
+        dsmem_st_u32(dsmem_addr(&sm.out_tok, 0u), static_cast<uint32_t>(found));
+        dsmem_st_u32(dsmem_addr(&sm.out_st, 0u), sfin);
+      }
+      return 0;
+    };
+
+    if (flags & 1u) {
+      out = OUT_TIMEOUT;
+    } else if (flags & 8u) {
+      out = OUT_SKIP;
+    } else {
+      const int t = sm.t;
+      const float u = sm.u;
+      const WarpT wfp = make_warp(mp, sm.lo_p), wfq = make_warp(mq, sm.lo_q);
+      uint32_t err = 0u;
+      if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
+      bool p_bad = (flags & 2u) != 0u, q_bad = two && (flags & 4u) != 0u;
+      if constexpr (MODE == MODE_LOGITS) {
+        p_bad = p_bad || wfp.lo != wfp.lo;  // a NaN floor (an invalid filter parameter)
+        q_bad = q_bad || (two && wfq.lo != wfq.lo);
+      }
+      bool have_exact = false, failed = false;
+      double Zp_ex = 0.0, Zq_ex = 0.0;
+      auto take_exact = [&]() {
+        if (exact_pass(wfp, wfq)) {
+          have_exact = true;
+          Zp_ex = limbs_to_double(sm.lp);
+          Zq_ex = two ? limbs_to_double(sm.lq) : 0.0;
+        } else {
+          failed = true;
+        }
+      };
+      if constexpr (MODE == MODE_PROBS) {
+        // a non-finite approximate mass means a +Inf element or an fp32
+        // overflow of the partial sums: the exact pass tells them apart
+        if (!err && !p_bad && !q_bad && (!(Zp.hi <= FLT_MAX) || (two && !(Zq.hi <= FLT_MAX)))) {
+          take_exact();
+          if (have_exact) {
+            p_bad = p_bad || (sm.infl & 1u);
+            q_bad = q_bad || (two && (sm.infl & 2u));
+          }
+        }
+      }
+      uint32_t st = 0u;
+      if (!failed) {
+        if (!err && p_bad) err = ST_BAD_VALUE;
+        if (!err && q_bad) err = ST_BAD_VALUE;
+        if (!err && !(u >= 0.f && u < 1.f)) err = ST_BAD_VALUE;
+        const bool p_zero = MODE == MODE_PROBS ? (have_exact ? Zp_ex == 0.0 : Zp.hi == 0.f) : mp == -kInfF;
+        const bool q_zero = MODE == MODE_PROBS ? (have_exact ? Zq_ex == 0.0 : Zq.hi == 0.f) : mq == -kInfF;
+        out = OUT_TERM;
+        o_n = i;
+        o_next = -1;
+        if (err) {
+          o_st = err;
+        } else if (p_zero) {
+          o_st = ST_ZERO_MASS;
+        } else if (!bonus && q_zero) {
+          o_st = ST_ZERO_MASS;
+        } else {
+          if constexpr (MODE == MODE_LOGITS) {
+            // pass B: the masses of the defined weights (their exact sums
+            // are what the accept predicate compares)
+            float zp = slice_mass<T>(sp, n_el, wfp);
+            float zq = two ? slice_mass<T>(sq, n_el, wfq) : 0.f;
+            warp_converged();
+            zp = warp_sum_f(zp);
+            zq = warp_sum_f(zq);
+            if (lane == 0) {
+              sm.wf[warp][0] = zp;
+              sm.wf[warp][1] = zq;
+            }
+            __syncthreads();
+            if (warp == 0) {
+              warp_converged();
+              const bool wl = lane < kWarps;
+              const float c0 = warp_sum_f<8>(wl ? sm.wf[lane][0] : 0.f);
+              const float c1 = warp_sum_f<8>(wl ? sm.wf[lane][1] : 0.f);
+              if (lane == 0) {
+                sm.my[0] = __float_as_uint(c0);
+                sm.my[1] = __float_as_uint(c1);
+                sm.my[2] = sm.my[3] = 0u;
+              }
+              const bool ok = exchange(1, 4);
+              float z0 = 0.f, z1 = 0.f;
+              if (ok) {
+                const bool cl = lane < static_cast<int>(C);
+                z0 = warp_sum_f<16>(cl ? xrecf(1, lane, 0) : 0.f);
+                z1 = warp_sum_f<16>(cl ? xrecf(1, lane, 1) : 0.f);
+              }
+              if (lane == 0) {
+                sm.fv[2] = z0;
+                sm.fv[3] = z1;
+                sm.bi[2] = ok ? 1 : 0;
+              }
+            }
+            __syncthreads();
+            if (!sm.bi[2]) failed = true;
+            Zp.hi = sm.fv[2];
+            Zq.hi = sm.fv[3];
+            Bp = sum_bound(Zp.hi, R.nadd);
+            Bq = sum_bound(Zq.hi, R.nadd);
+          }
+          if (!failed) {
+            if (bonus) {
+              out = OUT_DRAW;  // all K_b drafts accepted: the bonus comes from p_K
+              o_n = kb;
+            } else {
+              const float pt = wfp(sm.gp), qt = wfq(sm.gq);
+              int dec = have_exact ? -1 : filter_decide(u, pt, qt, Zp, Bp, Zq, Bq);
+              if (!have_exact && ((P.flags & FLAG_FORCE_EXACT) || dec < 0)) take_exact();
+              if (!failed) {
+                if (have_exact) {
+                  if (tid == 0) sm.bi[3] = exact_accept(u, pt, qt, sm.lp, sm.lq) ? 1 : 0;
+                  __syncthreads();
+                  dec = sm.bi[3];
+                  st |= ST_EXACT;
+                }
+                out = dec ? OUT_ACCEPT : OUT_DRAW;
+                o_st = st;
+              }
+            }
+          }
+        }
+        if (!failed && (out == OUT_TERM || out == OUT_DRAW)) post_terminal();
+      }
+      if (failed) out = OUT_TIMEOUT;
+
+      if (out == OUT_DRAW) {
+        // ---- the bonus from p_K, or the residual after the rejection, with u_K
+        const float ud = sm.ud;
+        if (!bonus && !(ud >= 0.f && ud < 1.f)) {
+          out = OUT_TERM;
+          o_st = st | ST_BAD_VALUE;
+        } else {
+          DrawT dw;
+          dw.scale = __uint_as_float(static_cast<uint32_t>(127 + P.fixed_shift) << 23);
+          dw.resid = bonus ? 0 : 1;
+          const float zp = have_exact ? static_cast<float>(Zp_ex) : Zp.hi;
+          const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : Zq.hi);
+          if constexpr (MODE == MODE_LOGITS) {
+            dw.k = khi;  // c = -m k - log2 Z, folded into one FMA per element
+            const DF mk = two_prod(mp, khi), qk = two_prod(mq, khi);
+            dw.cp = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
+            dw.cq = bonus ? 0.f : -__fadd_rn(qk.hi, __fadd_rn(qk.lo, log2f(zq)));
+            dw.lo_p = sm.lo_p;
+            dw.lo_q = bonus ? -kInfF : sm.lo_q;
+          } else {
+            const double zpd = have_exact ? Zp_ex : static_cast<double>(zp);
+            const double zqd = have_exact && !bonus ? Zq_ex : static_cast<double>(zq);
+            norm_factors(zpd, dw.sp, dw.ap);
+            norm_factors(zqd, dw.sq, dw.aq);
+          }
+          int code = draw(dw, !bonus, 3, st, ud);
+          if (code == 1) {  // an empty residual: the draw falls back to p
+            dw.resid = 0;
+            st |= ST_ZERO_MASS;
+            code = draw(dw, false, 4, st, ud);
+          }
+          if (code == 2) {
+            out = OUT_TERM;
+            o_st = st | ST_ZERO_MASS;
+          } else if (code < 0) {
+            out = OUT_TIMEOUT;
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- record, count, combine
+  if (bad && tid == 0) mbar_wait_bounded(&sm.full, 0u);  // no copy may land after exit
+  __syncthreads();
+  // Peers push records (and the draw's owner its id) into this CTA's shared
+  // memory: every thread of the cluster meets here once before any CTA of
+  // the cluster exits or rank 0 reads the drawn id.
+  cluster_sync_all();
+  if (rank == 0 && tid == 0) {
+    uint4 rv = make_uint4(ST_TIMEOUT | kRecTerminal, 0xFFFFFFFFu, 0u, 0u);
+    if (out == OUT_ACCEPT) {
+      rv = make_uint4(o_st, 0u, 0u, 0u);
+    } else if (out == OUT_TERM) {
+      rv = make_uint4(o_st | kRecTerminal, static_cast<uint32_t>(o_next), static_cast<uint32_t>(o_n), 0u);
+    } else if (out == OUT_DRAW && sm.out_tok != INT_MIN) {
+      rv = make_uint4(sm.out_st | kRecTerminal, static_cast<uint32_t>(sm.out_tok), static_cast<uint32_t>(o_n), 0u);
+    }
+    if (out != OUT_SKIP) R.rec[t0 + i] = rv;
+    __threadfence();
+    const int old = atomicAdd(R.seq_count + b, 1);
+    if (old == kb) {  // the last of the sequence's kb + 1 items: every record is written
+      __threadfence();
+      uint32_t st = 0u;
+      int n = 0, nxt = -1;
+      bool term = false;
+      for (int r = 0; r <= kb; ++r) {
+        const uint4 v = __ldcg(R.rec + t0 + r);
+        if (v.x & kRecTerminal) {
+          st |= v.x & ~kRecTerminal;
+          nxt = static_cast<int>(v.y);
+          n = static_cast<int>(v.z);
+          term = true;
+          break;
+        }
+        st |= v.x;
+      }
+      if (!term || (st & ST_TIMEOUT)) {
+        n = 0;
+        nxt = -1;
+        st = ST_TIMEOUT;
+      }
+      if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
+        n = 0;
+        nxt = -1;
+        st |= ST_TIMEOUT;
+      }
+      P.n_out[b] = n;
+      P.next_out[b] = nxt;
+      P.st_out[b] = st;
+      R.seq_count[b] = 0;  // ready for the next launch
+      R.seq_first[b] = 0;
+    }
+  }
+}
+
+}  // namespace svk

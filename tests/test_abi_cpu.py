@@ -45,7 +45,7 @@ def greedy(lib, **kw):
     (dict(V=0), b"vocab"),
     (dict(stride=8), b"row_stride"),
     (dict(sum_k=5), b"sum_k must equal"),
-    (dict(flags=8), b"flag"),
+    (dict(flags=16), b"flag"),
     (dict(target=NULL), b"target"),
     (dict(tok=NULL), b"draft_tokens"),
     (dict(n=NULL), b"output"),
@@ -59,7 +59,8 @@ def test_greedy_argument_errors(lib, kw, frag):
 def test_empty_batch_is_a_noop(lib):
     assert greedy(lib, B=0, sum_k=0, target=NULL, tok=NULL, n=NULL, nxt=NULL, st=NULL) == _lib.SV_OK
     # both testing flags pass the host checks
-    for f in (_lib.FLAG_FORCE_EXACT, _lib.FLAG_EXPIRE_EXCHANGE, _lib.FLAG_FORCE_EXACT | _lib.FLAG_EXPIRE_EXCHANGE):
+    for f in (_lib.FLAG_FORCE_EXACT, _lib.FLAG_EXPIRE_EXCHANGE, _lib.FLAG_FORCE_EXACT | _lib.FLAG_EXPIRE_EXCHANGE,
+              _lib.FLAG_PLAN_ROWS, _lib.FLAG_PLAN_CHAIN, _lib.FLAG_PLAN_ROWS | _lib.FLAG_PLAN_CHAIN):
         assert greedy(lib, B=0, sum_k=0, target=NULL, tok=NULL, n=NULL, nxt=NULL, st=NULL, flags=f) == _lib.SV_OK
 
 
@@ -213,7 +214,7 @@ def test_lm_head_host_checks(lib):
     args = [P, P, P, 64, P, P, P, NULL, 2, 3, 6, 100, P, P, P]
     assert lib.sv_lm_head_verify(*args, P, need - 4, 0, NULL) == _lib.SV_ERR_ARG
     assert b"workspace_bytes" in lib.sv_last_error()
-    assert lib.sv_lm_head_verify(*args, P, need, 8, NULL) == _lib.SV_ERR_ARG  # unknown flag
+    assert lib.sv_lm_head_verify(*args, P, need, 16, NULL) == _lib.SV_ERR_ARG  # unknown flag
     assert lib.sv_lm_head_verify(*args, P + 8, need, 0, NULL) == _lib.SV_ERR_ARG  # workspace alignment
     assert lib.sv_lm_head_verify(P, P, P, 64, P, P, P, NULL, 2, 3, 5, 100, P, P, P, P, need, 0,
                                  NULL) == _lib.SV_ERR_ARG  # sum_k != B * K without cu_k
