@@ -43,7 +43,10 @@ CONFIG_TEXT = {
                "draft row)",
     "latency1": "B=1 K=4 V=32000 f32 probabilities, rejection sampling: one B=1 call per round "
                 "(the 600 rounds of config 1 in turn)",
+    "long16": "B=8 K=16 V=128256 bf16 logits, temperature 0.8, draft = target + N(0, 0.3^2) (long "
+              "accepted chains): the row-parallel plan",
 }
+WORKLOAD_OVERRIDES = {"long16": dict(B=8, K=16, draft_noise=0.3)}
 FILTER_TOP_K, FILTER_TOP_P = 50, 0.9
 KERNEL_NAMES = {
     "config1": "sv_verify_kernel<1, float, false>",
@@ -54,6 +57,7 @@ KERNEL_NAMES = {
     "filter": "floors_kernel<__nv_bfloat16>",
     "greedy2": "sv_verify_kernel<0, __nv_bfloat16, false>",
     "latency1": "sv_verify_kernel<1, float, false>",
+    "long16": "sv_rows_kernel<2, __nv_bfloat16, false>",
 }
 METRIC = "verified rows/s and achieved HBM GB/s vs GB300 peak at B=64 K=5 V=128256"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_config2_traffic.md")
@@ -252,10 +256,11 @@ def make_workload(name, seed_shift=0):
     """A named workload; 'filter' is config 2 with top-k 50 and top-p 0.9 on
     every sequence (the sampler filters before verification)."""
     import workloads
-    base = {"filter": "config2", "latency1": "config1"}.get(name, name)
+    base = {"filter": "config2", "latency1": "config1", "long16": "config2"}.get(name, name)
     base_seed = {"config1": 1, "config2": 2, "config3": 3, "config4": 4, "config5": 5,
                  "greedy2": 6}[base]
-    wl = workloads.make_config(base, seed=workloads.configs.SEED_BASE + base_seed + seed_shift)
+    wl = workloads.make_config(base, seed=workloads.configs.SEED_BASE + base_seed + seed_shift,
+                               **WORKLOAD_OVERRIDES.get(name, {}))
     if name == "filter":
         wl.top_k = np.full(wl.B, FILTER_TOP_K, np.int32)
         wl.top_p = np.full(wl.B, FILTER_TOP_P, np.float32)
@@ -465,7 +470,7 @@ def run_gpu(args):
             # the other mode at the same shape, and config 1 as single-sequence
             # rounds, each measured the same way after the main line
             modes = {name: mode_summary(torch, sv, dev, stream, flush, name, args.steps, args.warmup, peak)
-                     for name in ("greedy2", "latency1")}
+                     for name in ("greedy2", "latency1", "long16")}
         result = {
             "metric": METRIC,
             "value": value,

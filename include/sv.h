@@ -167,11 +167,13 @@ sv_status sv_accept_from_logits(const void* target_logits, const void* draft_log
 
 /*
  * Bytes of device workspace a verification call of this size needs.  The
- * verification calls take no workspace: a sequence's per-row partials (masses,
- * maxima, argmax candidates, draw totals) are combined inside its thread-block
- * cluster through distributed shared memory, so no scratch survives in global
- * memory.  The query exists so that a caller written against a workspace
- * interface sizes nothing; it returns 0 for every argument.
+ * verification calls take no workspace: the chain plan combines a sequence's
+ * per-row partials (masses, maxima, argmax candidates, draw totals) inside its
+ * thread-block cluster through distributed shared memory, and the
+ * row-parallel plan (taken for long drafts, K >= 8) counts its per-row records
+ * into the library's own static device arrays (one slot per stream, back at
+ * zero when each launch ends).  The query exists so that a caller written
+ * against a workspace interface sizes nothing; it returns 0 for every argument.
  *   batch  B (>= 0), k  the largest K_b, vocab  V,
  *   mode   SV_MODE_GREEDY (sv_verify_greedy), SV_MODE_PROBS (sv_accept) or
  *          SV_MODE_LOGITS (sv_accept_from_logits).
