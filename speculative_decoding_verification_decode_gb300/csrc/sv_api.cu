@@ -269,22 +269,22 @@ svk::Params base_params(const void* tgt, const void* drf, int64_t stride, const 
 // The plan of a call: the row-parallel kernel (sv_rows.cuh) or the chain
 // kernel (sv_verify.cuh).  The chain walks a sequence's rows one dependent
 // link after another; the row-parallel plan decides every row at once but
-// pays a whole launch of items per wave of clusters.  So it takes long
-// drafts (K >= 8, where accepted chains can be long) whose items fit in about
-// two waves of three CTAs per SM.  Measured on GB300: sampling, K = 40 at
-// acceptance 0.995, twelve sequences of V = 3001, 35 us against 517 us;
-// K = 16, four sequences of V = 32000, 23 against 50 us; K = 8, eight
-// sequences of V = 128256 bf16, 34 against 40 us; greedy with every draft
-// accepted, K = 8, eight sequences of V = 128256, 19 against 36 us (with none
-// accepted, one sequence of V = 32000, 13 against 9 us); while B = 64, K = 5
-// at V = 128256 (six waves of items) takes 68 against 60 us.
+// pays a whole item per wave of clusters.  So it takes long drafts (K >= 8,
+// where accepted chains can be long) whose items fit in about two and a half
+// waves of three CTAs per SM (eight CTAs per SM).  Measured on GB300
+// (row-parallel against chain): sampling, K = 40 at acceptance 0.995, twelve
+// sequences of V = 3001, 28 us against 521 us; K = 16, four sequences of
+// V = 32000, 21 against 50 us; K = 16, eight sequences of V = 128256 bf16,
+// 40 against 44 us; K = 8, sixteen of them, 46 against 48 us; greedy with
+// every draft accepted, K = 40, 15 against 95 us; while B = 64, K = 5 at
+// V = 128256 (3072 CTAs) takes 66 against 60 us.
 bool choose_rows(uint32_t flags, int mode, int elem, const svk::Params& p) {
   if (flags & SV_FLAG_PLAN_CHAIN) return false;
   const int C = svh::rows_cluster_size(mode, elem, p);
   if (C == 0) return false;
   if (flags & SV_FLAG_PLAN_ROWS) return true;
   const long long ctas = static_cast<long long>(C) * p.B * (p.K + 1LL);
-  return p.K >= 8 && ctas <= 6LL * sm_count();
+  return p.K >= 8 && ctas <= 8LL * sm_count();
 }
 
 // Launches the row-parallel plan; false (error message cleared) when it

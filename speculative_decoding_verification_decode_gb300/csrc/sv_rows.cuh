@@ -898,49 +898,58 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   // memory: every thread of the cluster meets here once before any CTA of
   // the cluster exits or rank 0 reads the drawn id.
   cluster_sync_all();
-  if (rank == 0 && tid == 0) {
-    uint4 rv = make_uint4(ST_TIMEOUT | kRecTerminal, 0xFFFFFFFFu, 0u, 0u);
-    if (out == OUT_ACCEPT) {
-      rv = make_uint4(o_st, 0u, 0u, 0u);
-    } else if (out == OUT_TERM) {
-      rv = make_uint4(o_st | kRecTerminal, static_cast<uint32_t>(o_next), static_cast<uint32_t>(o_n), 0u);
-    } else if (out == OUT_DRAW && sm.out_tok != INT_MIN) {
-      rv = make_uint4(sm.out_st | kRecTerminal, static_cast<uint32_t>(sm.out_tok), static_cast<uint32_t>(o_n), 0u);
-    }
-    if (out != OUT_SKIP) R.rec[t0 + i] = rv;
-    __threadfence();
-    const int old = atomicAdd(R.seq_count + b, 1);
-    if (old == kb) {  // the last of the sequence's kb + 1 items: every record is written
+  if (rank == 0 && warp == 0) {
+    int last = 0;
+    if (lane == 0) {
+      uint4 rv = make_uint4(ST_TIMEOUT | kRecTerminal, 0xFFFFFFFFu, 0u, 0u);
+      if (out == OUT_ACCEPT) {
+        rv = make_uint4(o_st, 0u, 0u, 0u);
+      } else if (out == OUT_TERM) {
+        rv = make_uint4(o_st | kRecTerminal, static_cast<uint32_t>(o_next), static_cast<uint32_t>(o_n), 0u);
+      } else if (out == OUT_DRAW && sm.out_tok != INT_MIN) {
+        rv = make_uint4(sm.out_st | kRecTerminal, static_cast<uint32_t>(sm.out_tok), static_cast<uint32_t>(o_n), 0u);
+      }
+      if (out != OUT_SKIP) R.rec[t0 + i] = rv;
       __threadfence();
+      last = atomicAdd(R.seq_count + b, 1) == kb ? 1 : 0;
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last) {  // the last of the sequence's kb + 1 items: every record is written
+      __threadfence();
+      // the records, 32 rows per load round: the first terminal row ends the
+      // walk, and the statuses of the rows up to it are ORed
       uint32_t st = 0u;
       int n = 0, nxt = -1;
       bool term = false;
-      for (int r = 0; r <= kb; ++r) {
-        const uint4 v = __ldcg(R.rec + t0 + r);
-        if (v.x & kRecTerminal) {
-          st |= v.x & ~kRecTerminal;
-          nxt = static_cast<int>(v.y);
-          n = static_cast<int>(v.z);
+      for (int base = 0; base <= kb && !term; base += 32) {
+        const int r = base + lane;
+        const uint4 v = r <= kb ? __ldcg(R.rec + t0 + r) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t tm = __ballot_sync(0xFFFFFFFFu, r <= kb && (v.x & kRecTerminal) != 0u);
+        const int first = tm ? __ffs(tm) - 1 : 32;
+        st |= __reduce_or_sync(0xFFFFFFFFu, (lane <= first && r <= kb) ? (v.x & ~kRecTerminal) : 0u);
+        if (tm) {
+          nxt = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.y), first);
+          n = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.z), first);
           term = true;
-          break;
         }
-        st |= v.x;
       }
-      if (!term || (st & ST_TIMEOUT)) {
-        n = 0;
-        nxt = -1;
-        st = ST_TIMEOUT;
+      if (lane == 0) {
+        if (!term || (st & ST_TIMEOUT)) {
+          n = 0;
+          nxt = -1;
+          st = ST_TIMEOUT;
+        }
+        if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
+          n = 0;
+          nxt = -1;
+          st |= ST_TIMEOUT;
+        }
+        P.n_out[b] = n;
+        P.next_out[b] = nxt;
+        P.st_out[b] = st;
+        R.seq_count[b] = 0;  // ready for the next launch
+        R.seq_first[b] = 0;
       }
-      if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
-        n = 0;
-        nxt = -1;
-        st |= ST_TIMEOUT;
-      }
-      P.n_out[b] = n;
-      P.next_out[b] = nxt;
-      P.st_out[b] = st;
-      R.seq_count[b] = 0;  // ready for the next launch
-      R.seq_first[b] = 0;
     }
   }
 }
