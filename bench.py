@@ -60,15 +60,20 @@ KERNEL_NAMES = {
     "long16": "sv_rows_kernel<2, __nv_bfloat16, false>",
 }
 METRIC = "verified rows/s and achieved HBM GB/s vs GB300 peak at B=64 K=5 V=128256"
-PROFILE_FILE = os.path.join(ROOT, "profiles", "sv_verify_kernel_config2_traffic.md")
-SRC_FILES = [os.path.join(ROOT, "speculative_decoding_verification_decode_gb300", "csrc", f)
-             for f in ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh")]
+# ncu summaries that carry the dominant kernel's DRAM bytes per launch, and
+# the sources that kernel and its launch plan are built from
+_CSRC = os.path.join(ROOT, "speculative_decoding_verification_decode_gb300", "csrc")
+PROFILE_FILES = {
+    "config2": ("sv_verify_kernel_config2_traffic.md", ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh")),
+    "long16": ("sv_rows_kernel_long16_traffic.md",
+               ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh", "sv_rows.cuh", "sv_rows.cu")),
+}
 
 
-def kernel_source_sha():
+def kernel_source_sha(config="config2"):
     h = hashlib.sha256()
-    for f in SRC_FILES:
-        with open(f, "rb") as fh:
+    for f in PROFILE_FILES[config][1]:
+        with open(os.path.join(_CSRC, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -82,16 +87,18 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def profiled_traffic(config):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel source (else None)."""
+    if config not in PROFILE_FILES:
+        return None
     try:
-        text = open(PROFILE_FILE).read()
+        text = open(os.path.join(ROOT, "profiles", PROFILE_FILES[config][0])).read()
     except OSError:
         return None
     sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not sha or not val or sha.group(1) != kernel_source_sha():
+    if not sha or not val or sha.group(1) != kernel_source_sha(config):
         return None
     return int(val.group(1))
 
@@ -462,7 +469,7 @@ def run_gpu(args):
         achieved = alg / (ms_local * 1e-3) / 1e9
         if floors_ms is not None:  # the floors read every row once: the formula bytes
             achieved = formula / (floors_ms * 1e-3) / 1e9
-        traffic = profiled_traffic() if args.config == "config2" else None
+        traffic = profiled_traffic(args.config)
         value = world * rows_per_step / (ms * 1e-3)
         cpu_val, cpu_seq, cpu_dt = oracle_rows_per_s(wl, budget_s=args.cpu_budget)
         modes = None

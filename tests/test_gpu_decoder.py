@@ -66,10 +66,11 @@ def _prompts(B, L, V, seed, plen=3):
 
 
 @pytest.mark.parametrize("drafter", ["perfect", "noisy", "unrelated"])
-@pytest.mark.parametrize("graph", [False, True])
-def test_speculative_greedy_reproduces_plain_greedy(drafter, graph):
+@pytest.mark.parametrize("graph,K", [(False, 4), (True, 4), (True, 9)])
+def test_speculative_greedy_reproduces_plain_greedy(drafter, graph, K):
+    """K = 9 takes the row-parallel plan (long drafts), inside the graph."""
     from speculative_decoding_verification_decode_gb300.decoder import SpeculativeDecoder
-    V, H, B, K, R = 97, 211, 48, 4, 10
+    V, H, B, R = 97, 211, 48, 10
     target = TableModel(V, H, seed=1)
     if drafter == "perfect":
         draft = target
