@@ -9,7 +9,8 @@
 //     launched first; an item whose sequence has already posted a terminal
 //     row before i (a rejection, an error, a miss) skips its loads and work;
 //   * the cluster takes the row's decision exactly as the chain kernel does
-//     (the same defined weights, the same exact predicate and fallback), and,
+//     (one online-softmax pass with the chain's error bound, the same defined
+//     weights, the same exact predicate and fallback), and,
 //     if the row ends its sequence by a rejection or is the bonus row, its
 //     inverse-CDF draw from the resident slices (no second read of the row);
 //   * each item writes a small record of its outcome to global scratch and
@@ -26,7 +27,7 @@ namespace svk {
 
 constexpr int kRowsThreads = 256;  // 8 warps, every one reduces
 constexpr uint32_t kRecTerminal = 0x80000000u;
-constexpr int kRowsExchanges = 5;  // maxima / sums, masses, exact limbs, draw, draw from p
+constexpr int kRowsExchanges = 5;  // row statistics, (unused), exact limbs, draw, draw from p
 
 struct RowsParams {
   Params p;
@@ -40,12 +41,12 @@ struct RowsParams {
 };
 
 struct __align__(16) RowsTail {
-  uint32_t xr[4][kMaxCluster][8];  // records of exchanges 0, 1, 3, 4
+  uint32_t xr[4][kMaxCluster][8];  // records of exchanges 0, 3, 4 (slot 1 unused)
   uint32_t xe[kMaxCluster][32];    // records of exchange 2 (exact limbs)
   uint32_t my[32];                 // this CTA's outgoing record
+  float wf[kWarps][8];             // per-warp partials
   uint64_t xbar[kRowsExchanges];
   uint64_t full;
-  float wf[kWarps][4];
   int wi[kWarps][4];
   unsigned long long wu[kWarps];
   uint32_t lp[kLimbs], lq[kLimbs], infl;
@@ -54,7 +55,7 @@ struct __align__(16) RowsTail {
   float u, ud, gp, gq, lo_p, lo_q;
   int skip;
   // the cluster's view after an exchange (written by warp 0)
-  float fv[4];
+  float fv[6];
   uint32_t iv[4];
   float dpar[4];
   int bi[4];
@@ -62,62 +63,6 @@ struct __align__(16) RowsTail {
   int out_tok;
   uint32_t out_st;
 };
-
-// NaN-propagating maximum of a shared-memory slice of n elements (+-Inf
-// count as values), over the CTA's 256 threads; the thread's partial.
-template <typename T>
-__device__ __forceinline__ float slice_max_nan(const T* s, int n) {
-  constexpr int VEC = ElemTraits<T>::kVec;
-  const int nv = n / VEC;
-  float m = -kInfF;
-  if constexpr (sizeof(T) == 4) {
-    for (int vi = threadIdx.x; vi < nv; vi += kRowsThreads) {
-      const float4 v = reinterpret_cast<const float4*>(s)[vi];
-      m = fmax_nan(m, fmax_nan(fmax_nan(v.x, v.y), fmax_nan(v.z, v.w)));
-    }
-  } else {
-    constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
-    uint32_t h = kBf ? 0xFF80FF80u : 0xFC00FC00u;
-    for (int vi = threadIdx.x; vi < nv; vi += kRowsThreads) {
-      const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-      if constexpr (kBf) h = bf16x2_max_nan(h, bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w)));
-      else h = f16x2_max_nan(h, f16x2_max_nan(f16x2_max_nan(v.x, v.y), f16x2_max_nan(v.z, v.w)));
-    }
-    m = kBf ? fmax_nan(bf_lo(h), bf_hi(h)) : fmax_nan(h_lo(h), h_hi(h));
-  }
-  for (int e = nv * VEC + threadIdx.x; e < n; e += kRowsThreads) m = fmax_nan(m, ElemTraits<T>::to_f(s[e]));
-  return m;
-}
-
-// fp32 sum of the defined weights wf(l) of a shared-memory slice: a pairwise
-// tree per 16-byte vector, added into the thread's sum (one addition per
-// vector, plus one per tail element); four vectors at a time for independent
-// exponentials.
-template <typename T, typename W>
-__device__ __forceinline__ float slice_mass(const T* s, int n, const W& wf) {
-  constexpr int VEC = ElemTraits<T>::kVec;
-  constexpr int U = 4;
-  const int nv = n / VEC;
-  Acc a;
-  a.init();
-  for (int base = threadIdx.x; base < nv; base += U * kRowsThreads) {
-    float t[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = base + u * kRowsThreads;
-      float x[VEC], e[VEC];
-      if (vi < nv) unpack_vec<T>(reinterpret_cast<const uint4*>(s)[vi], x);
-#pragma unroll
-      for (int k = 0; k < VEC; ++k) e[k] = vi < nv ? wf(x[k]) : 0.f;
-      t[u] = tree_sum<VEC>(e);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (base + u * kRowsThreads < nv) a.add(t[u]);
-  }
-  for (int e = nv * VEC + threadIdx.x; e < n; e += kRowsThreads) a.add(wf(ElemTraits<T>::to_f(s[e])));
-  return a.f;
-}
 
 // Draw weights of vector vi of a resident slice pair (q may be null): VEC
 // entries, zero past the slice end; returns the number of real elements.
@@ -257,6 +202,9 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
         if (two) sq[e] = rowq[e];
       }
     }
+  }
+  cluster_sync_all();  // every peer runs and its barriers exist before the first remote arrive
+  if (!skip_mine) {
     if (tid == 32) {  // the row's decision inputs, while the slices stream in
       int t = -1;
       float gpv = 0.f, gqv = 0.f;
@@ -281,7 +229,6 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       sm.lo_q = lq;
     }
   }
-  cluster_sync_all();  // every peer runs and its barriers exist before the first remote arrive
   int bad = 0;  // this CTA's wait for its own copies gave up
   if (!skip_mine && P.use_tma) bad = mbar_wait_bounded(&sm.full, 0u) ? 0 : 1;
   __syncthreads();
@@ -515,50 +462,141 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       Bp = sum_bound(Zp.hi, R.nadd);
       Bq = sum_bound(Zq.hi, R.nadd);
     } else {
-      float xp = -kInfF, xq = -kInfF;
+      // one online-softmax pass per row (running maximum and weight sums with
+      // a tracked error bound), merged lanes -> warp -> CTA -> cluster, each
+      // merge one rescale step, as in the chain kernel
+      Online op, oq;
+      op.init();
+      oq.init();
+      float ep = -kInfF, eq = -kInfF;  // NaN-propagating maxima (validity)
       if (!skip_mine) {
-        xp = slice_max_nan<T>(sp, n_el);
-        if (two) xq = slice_max_nan<T>(sq, n_el);
+        chunk_online<T, FL>(sp, n_el, khi, sm.lo_p, op, ep);
+        if (two) chunk_online<T, FL>(sq, n_el, khi, sm.lo_q, oq, eq);
       }
       warp_converged();
-      xp = warp_max_nan_f(xp);
-      xq = warp_max_nan_f(xq);
+      const float wmp = warp_max_f(op.m), wmq = warp_max_f(oq.m);
+      float s0 = 0.f, w0 = 0.f, s1 = 0.f, w1 = 0.f;
+      if (op.m > -kInfF) {
+        const float d = __fmul_rn(__fsub_rn(wmp, op.m), khi);
+        const float f = ex2_ftz(-d);
+        s0 = __fmul_rn(op.s, f);
+        w0 = __fmul_rn(__fmaf_rn(d, op.s, op.w), f);
+      }
+      if (oq.m > -kInfF) {
+        const float d = __fmul_rn(__fsub_rn(wmq, oq.m), khi);
+        const float f = ex2_ftz(-d);
+        s1 = __fmul_rn(oq.s, f);
+        w1 = __fmul_rn(__fmaf_rn(d, oq.s, oq.w), f);
+      }
+      s0 = warp_sum_f(s0);
+      w0 = warp_sum_f(w0);
+      s1 = warp_sum_f(s1);
+      w1 = warp_sum_f(w1);
+      const float vmp = warp_max_nan_f(ep), vmq = warp_max_nan_f(eq);
+      const int rr = warp_max_i(max(op.r, oq.r));
       if (lane == 0) {
-        sm.wf[warp][0] = xp;
-        sm.wf[warp][1] = xq;
+        sm.wf[warp][0] = wmp;
+        sm.wf[warp][1] = s0;
+        sm.wf[warp][2] = w0;
+        sm.wf[warp][3] = wmq;
+        sm.wf[warp][4] = s1;
+        sm.wf[warp][5] = w1;
+        sm.wf[warp][6] = vmp;
+        sm.wf[warp][7] = vmq;
+        sm.wi[warp][0] = rr;
       }
       bad = __syncthreads_or(bad);
       if (warp == 0) {
         warp_converged();
+        static_assert(kWarps == 8 && kMaxCluster <= 16, "combine widths");
         const bool wl = lane < kWarps;
-        const float c0 = warp_max_nan_f<8>(wl ? sm.wf[lane][0] : -kInfF);
-        const float c1 = warp_max_nan_f<8>(wl ? sm.wf[lane][1] : -kInfF);
-        if (lane == 0) {
-          sm.my[0] = __float_as_uint(c0);
-          sm.my[1] = __float_as_uint(c1);
-          sm.my[2] = (bad ? 1u : 0u) | (skip_mine ? 8u : 0u);
-          sm.my[3] = 0u;
+        const float4 fa = *reinterpret_cast<const float4*>(&sm.wf[lane & 7][0]);
+        const float4 fb = *reinterpret_cast<const float4*>(&sm.wf[lane & 7][4]);
+        // warps -> CTA (one more rescale step)
+        const float xmp = wl ? fa.x : -kInfF, xmq = wl ? fa.w : -kInfF;
+        const float cmp = warp_max_f<8>(xmp), cmq = warp_max_f<8>(xmq);
+        const float c6 = warp_max_nan_f<8>(wl ? fb.z : -kInfF);
+        const float c7 = warp_max_nan_f<8>(wl ? fb.w : -kInfF);
+        const int cr = warp_max_i<8>(wl ? sm.wi[lane & 7][0] : 0);
+        float cs0 = 0.f, cw0 = 0.f, cs1 = 0.f, cw1 = 0.f;
+        if (xmp > -kInfF) {
+          const float d = __fmul_rn(__fsub_rn(cmp, xmp), khi);
+          const float f = ex2_ftz(-d);
+          cs0 = __fmul_rn(fa.y, f);
+          cw0 = __fmul_rn(__fmaf_rn(d, fa.y, fa.z), f);
         }
-        float gp = -kInfF, gq = -kInfF;
+        if (xmq > -kInfF) {
+          const float d = __fmul_rn(__fsub_rn(cmq, xmq), khi);
+          const float f = ex2_ftz(-d);
+          cs1 = __fmul_rn(fb.x, f);
+          cw1 = __fmul_rn(__fmaf_rn(d, fb.x, fb.y), f);
+        }
+        warp_converged();
+        cs0 = warp_sum_f<8>(cs0);
+        cw0 = warp_sum_f<8>(cw0);
+        cs1 = warp_sum_f<8>(cs1);
+        cw1 = warp_sum_f<8>(cw1);
+        if (lane == 0) {
+          sm.my[0] = __float_as_uint(cmp);
+          sm.my[1] = __float_as_uint(cmq);
+          sm.my[2] = __float_as_uint(cs0);
+          sm.my[3] = __float_as_uint(cw0);
+          sm.my[4] = __float_as_uint(cs1);
+          sm.my[5] = __float_as_uint(cw1);
+          sm.my[6] = static_cast<uint32_t>(cr);
+          sm.my[7] = (bad ? 1u : 0u) | (c6 < kInfF ? 0u : 2u) | (c7 < kInfF ? 0u : 4u) | (skip_mine ? 8u : 0u);
+        }
+        float gmp = -kInfF, gmq = -kInfF, zp = 0.f, zq = 0.f, gwp = 0.f, gwq = 0.f;
+        int gr = 0;
         uint32_t f = 1u;
-        if (exchange(0, 4)) {
+        if (exchange(0, 8)) {
+          // CTAs -> cluster (one more rescale step)
+          warp_converged();
           const bool cl = lane < static_cast<int>(C);
-          gp = warp_max_nan_f<16>(cl ? xrecf(0, lane, 0) : -kInfF);
-          gq = warp_max_nan_f<16>(cl ? xrecf(0, lane, 1) : -kInfF);
-          f = __reduce_or_sync(0xFFFFFFFFu, cl ? xrec(0, lane, 2) : 0u);
+          const float rmp = cl ? xrecf(0, lane, 0) : -kInfF, rmq = cl ? xrecf(0, lane, 1) : -kInfF;
+          gmp = warp_max_f<16>(rmp);
+          gmq = warp_max_f<16>(rmq);
+          gr = warp_max_i<16>(cl ? static_cast<int>(xrec(0, lane, 6)) : 0);
+          f = __reduce_or_sync(0xFFFFFFFFu, cl ? xrec(0, lane, 7) : 0u);
+          float z0 = 0.f, z1 = 0.f, v0 = 0.f, v1 = 0.f;
+          if (rmp > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(gmp, rmp), khi);
+            const float ff = ex2_ftz(-d);
+            z0 = __fmul_rn(xrecf(0, lane, 2), ff);
+            v0 = __fmul_rn(__fmaf_rn(d, xrecf(0, lane, 2), xrecf(0, lane, 3)), ff);
+          }
+          if (rmq > -kInfF) {
+            const float d = __fmul_rn(__fsub_rn(gmq, rmq), khi);
+            const float ff = ex2_ftz(-d);
+            z1 = __fmul_rn(xrecf(0, lane, 4), ff);
+            v1 = __fmul_rn(__fmaf_rn(d, xrecf(0, lane, 4), xrecf(0, lane, 5)), ff);
+          }
+          warp_converged();
+          zp = warp_sum_f<16>(z0);
+          zq = warp_sum_f<16>(z1);
+          gwp = warp_sum_f<16>(v0);
+          gwq = warp_sum_f<16>(v1);
         }
         if (lane == 0) {
-          sm.fv[0] = gp;
-          sm.fv[1] = gq;
+          sm.fv[0] = gmp;
+          sm.fv[1] = gmq;
+          sm.fv[2] = zp;
+          sm.fv[3] = zq;
+          sm.fv[4] = gwp;
+          sm.fv[5] = gwq;
           sm.iv[0] = f;
+          sm.iv[1] = static_cast<uint32_t>(gr);
         }
       }
       __syncthreads();
       mp = sm.fv[0];
       mq = sm.fv[1];
+      Zp.hi = sm.fv[2];
+      Zq.hi = sm.fv[3];
       flags = sm.iv[0];
-      if (!(mp < kInfF)) flags |= 2u;  // a NaN or +Inf logit
-      if (two && !(mq < kInfF)) flags |= 4u;
+      const int Rs = static_cast<int>(sm.iv[1]);
+      Bp = online_bound(Zp.hi, sm.fv[4], Rs + 1, R.nadd, fabsf(__fmul_rn(mp, khi))) + static_cast<float>(P.V) * 1.2e-38f;
+      Bq = online_bound(Zq.hi, sm.fv[5], Rs + 1, R.nadd, fabsf(__fmul_rn(mq, khi))) + static_cast<float>(P.V) * 1.2e-38f;
     }
 
     // ---- inverse-CDF draw over the resident slices (collective).  Returns
@@ -781,49 +819,6 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
         } else if (!bonus && q_zero) {
           o_st = ST_ZERO_MASS;
         } else {
-          if constexpr (MODE == MODE_LOGITS) {
-            // pass B: the masses of the defined weights (their exact sums
-            // are what the accept predicate compares)
-            float zp = slice_mass<T>(sp, n_el, wfp);
-            float zq = two ? slice_mass<T>(sq, n_el, wfq) : 0.f;
-            warp_converged();
-            zp = warp_sum_f(zp);
-            zq = warp_sum_f(zq);
-            if (lane == 0) {
-              sm.wf[warp][0] = zp;
-              sm.wf[warp][1] = zq;
-            }
-            __syncthreads();
-            if (warp == 0) {
-              warp_converged();
-              const bool wl = lane < kWarps;
-              const float c0 = warp_sum_f<8>(wl ? sm.wf[lane][0] : 0.f);
-              const float c1 = warp_sum_f<8>(wl ? sm.wf[lane][1] : 0.f);
-              if (lane == 0) {
-                sm.my[0] = __float_as_uint(c0);
-                sm.my[1] = __float_as_uint(c1);
-                sm.my[2] = sm.my[3] = 0u;
-              }
-              const bool ok = exchange(1, 4);
-              float z0 = 0.f, z1 = 0.f;
-              if (ok) {
-                const bool cl = lane < static_cast<int>(C);
-                z0 = warp_sum_f<16>(cl ? xrecf(1, lane, 0) : 0.f);
-                z1 = warp_sum_f<16>(cl ? xrecf(1, lane, 1) : 0.f);
-              }
-              if (lane == 0) {
-                sm.fv[2] = z0;
-                sm.fv[3] = z1;
-                sm.bi[2] = ok ? 1 : 0;
-              }
-            }
-            __syncthreads();
-            if (!sm.bi[2]) failed = true;
-            Zp.hi = sm.fv[2];
-            Zq.hi = sm.fv[3];
-            Bp = sum_bound(Zp.hi, R.nadd);
-            Bq = sum_bound(Zq.hi, R.nadd);
-          }
           if (!failed) {
             if (bonus) {
               out = OUT_DRAW;  // all K_b drafts accepted: the bonus comes from p_K
