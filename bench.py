@@ -38,7 +38,8 @@ CONFIG_TEXT = {
     "config4": "B=32 ragged K_b~U{0..8} V=129280 f32 probabilities, rejection sampling",
     "config5": "B=1024 K=3 V=32000 f16 logits, half greedy / half sampled",
     "filter": "config 2 rows (B=64 K=5 V=128256 bf16 logits, T=0.8) with top-k 50 and top-p 0.9 "
-              "on every sequence: floors kernel, then floored verification",
+              "on every sequence: one call (the fused top-k plan; floors and floored verification "
+              "only for the sequences it hands on)",
     "greedy2": "B=64 K=5 V=128256 bf16 logits, greedy (each draft token the argmax of its bf16 "
                "draft row)",
     "latency1": "B=1 K=4 V=32000 f32 probabilities, rejection sampling: one B=1 call per round "
@@ -54,7 +55,7 @@ KERNEL_NAMES = {
     "config3": "sv_verify_kernel<0, float, false>",
     "config4": "sv_verify_kernel<1, float, false>",
     "config5": "sv_verify_kernel<2, __half, false>",
-    "filter": "floors_kernel<__nv_bfloat16>",
+    "filter": "sv_rows_kernel<2, __nv_bfloat16, true, true>",
     "greedy2": "sv_verify_kernel<0, __nv_bfloat16, false>",
     "latency1": "sv_verify_kernel<1, float, false>",
     "long16": "sv_rows_kernel<2, __nv_bfloat16, false>",
@@ -243,11 +244,7 @@ def call(sv, wl, x):
         return sv.verify_greedy(x["target"], x["tokens"], x["cu_k"], k)
     if wl.mode in ("accept", "both"):
         return sv.accept(x["target"], x["draft"], x["tokens"], x["uniforms"], x["cu_k"], k)
-    if x.get("top_k") is not None:
-        if "floors" in x:  # device inputs: the floors kernel, then the floored verification
-            floors(sv, wl, x)
-            return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
-                                         x["uniforms"], x["cu_k"], k, floors=x["floors"])
+    if x.get("top_k") is not None:  # one call: the fused plan or the two steps, by shape
         return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
                                      x["uniforms"], x["cu_k"], k, top_k=x["top_k"], top_p=x["top_p"])
     return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"],
@@ -257,6 +254,14 @@ def call(sv, wl, x):
 def floors(sv, wl, x):
     return sv.sampler_floors(x["target"], x["draft"], x["temperature"], x["top_k"], x["top_p"], x["cu_k"],
                              wl.K, int(wl.tokens.size), out=x["floors"])
+
+
+def two_steps(sv, wl, x):
+    """The filtered verification as two steps (every row's floors, then the
+    floored verification), for comparison with the call's own plan."""
+    k = wl.K if wl.cu_k is not None else None
+    return sv.accept_from_logits(x["target"], x["draft"], x["temperature"], x["tokens"], x["uniforms"],
+                                 x["cu_k"], k, top_k=x["top_k"], top_p=x["top_p"], flags=sv.FLAG_PLAN_CHAIN)
 
 
 def make_workload(name, seed_shift=0):
@@ -431,9 +436,10 @@ def run_gpu(args):
     barrier(dist, dev)
     ms_local = float(np.mean(per_step_ms))
     ms = max_over_ranks(ms_local, dist, dev)
-    floors_ms = None
-    if args.config == "filter":  # the floors kernel alone (the roofline's kernel)
+    floors_ms = two_ms = None
+    if args.config == "filter":  # the two steps and their floors kernel, for comparison
         floors_ms = float(np.mean(timed_steps(torch, stream, args.steps, flush, lambda i: floors(sv, wl, x))))
+        two_ms = float(np.mean(timed_steps(torch, stream, args.steps, flush, lambda i: two_steps(sv, wl, x))))
 
     # end to end through the public API with pinned host buffers
     hx = host_inputs(wl, torch)
@@ -467,8 +473,6 @@ def run_gpu(args):
             alg = algorithmic_bytes(wl, n_acc)
             formula = wl.formula_bytes()
         achieved = alg / (ms_local * 1e-3) / 1e9
-        if floors_ms is not None:  # the floors read every row once: the formula bytes
-            achieved = formula / (floors_ms * 1e-3) / 1e9
         traffic = profiled_traffic(args.config)
         value = world * rows_per_step / (ms * 1e-3)
         cpu_val, cpu_seq, cpu_dt = oracle_rows_per_s(wl, budget_s=args.cpu_budget)
@@ -503,7 +507,8 @@ def run_gpu(args):
                 "algorithmic_bytes_per_step": alg,
                 "l2": "flushed between timed steps (512 MB write, then a 512 MB read)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                **({"floors_us": floors_ms * 1e3, "verify_us": (ms_local - floors_ms) * 1e3,
+                **({"two_steps_us": two_ms * 1e3, "two_steps_floors_us": floors_ms * 1e3,
+                    "two_steps_floors_gbs": formula / (floors_ms * 1e-3) / 1e9,
                     "top_k": FILTER_TOP_K, "top_p": FILTER_TOP_P} if floors_ms is not None else {}),
             },
             "roofline": {
@@ -531,7 +536,7 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
             },
-            "gpu_launches": args.steps * (2 if args.config == "filter" else 1),
+            "gpu_launches": args.steps * (3 if args.config == "filter" else 1),
             "clocks": clocks.summary(),
         }
         if modes is not None:

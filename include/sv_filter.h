@@ -92,6 +92,29 @@ sv_status sv_accept_from_logits_floored(const void* target_logits, const void* d
                                         float* warped_target_out, float* warped_draft_out,
                                         uint32_t flags, void* stream);
 
+/* The filtered verification in one call: sv_sampler_floors and then
+ * sv_accept_from_logits_floored on the same arguments, with the floors held
+ * in the library's own scratch (results identical to those two calls, up to
+ * the draws' boundary band and the SV_SEQ_EXACT_PATH / SV_SEQ_NEAR_BOUNDARY
+ * bits).  top_k / top_p as sv_sampler_floors (both NULL: sv_accept_from_logits).
+ * For 16-bit logits with top_k set, a fused plan decides every sequence
+ * whose top-k is in [1, 64] and whose kept tokens its per-CTA candidate lists
+ * hold (the keys at or above each row slice's k-th largest contain every key
+ * the filters keep), without a floors pass over the rows; the floors kernel
+ * and the floored verification then run for the remaining sequences only.
+ * The library takes it when the rows to filter (2 sum_k + batch) exceed two
+ * per SM or stay under half the SM count (else the two steps);
+ * SV_FLAG_PLAN_ROWS requests it and SV_FLAG_PLAN_CHAIN refuses it.  Up to
+ * three kernel launches on `stream`; the scratch is one slot per stream (a
+ * stream beyond the library's four slots gets SV_ERR_UNSUPPORTED), so calls
+ * on one stream are ordered and calls on different streams do not share it. */
+sv_status sv_accept_from_logits_filtered(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                                         int64_t row_stride, const float* temperature, const int32_t* top_k,
+                                         const float* top_p, const int32_t* draft_tokens, const float* uniforms,
+                                         const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
+                                         int32_t vocab, int32_t* n_accepted, int32_t* next_token,
+                                         uint32_t* status, uint32_t flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

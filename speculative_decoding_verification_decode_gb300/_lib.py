@@ -44,6 +44,10 @@ SIGNATURES = {
     "sv_accept_from_logits_floored": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _i32, _i32,
                                              _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u32,
                                              _vp]),
+    # target, draft, dtype, stride, temperature, top_k, top_p, tokens, uniforms, cu_k, B, K, sum_k, V,
+    # n, next, status, flags, stream
+    "sv_accept_from_logits_filtered": (_i32, [_vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                              _i32, _i32, _vp, _vp, _vp, _u32, _vp]),
     "sv_gate_draft_lengths": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      ctypes.POINTER(GateParams), _vp, _vp, _vp]),
     "sv_gate_update": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _f64, _vp]),

@@ -156,10 +156,12 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     kernel reached (a testing aid).
 
     ``top_k`` (int32 ``[B]``) / ``top_p`` (f32 ``[B]``): the sampler filters of
-    include/sv_filter.h, applied alike to target and draft rows (two launches:
-    the floors, then the floored verification).  ``floors``: a pair of f32
-    device tensors ``[target_rows]``, ``[draft_rows]`` of precomputed floors
-    (used instead of top_k / top_p; either may be None)."""
+    include/sv_filter.h, applied alike to target and draft rows, in one call of
+    ``sv_accept_from_logits_filtered`` (the fused top-k plan where it applies,
+    the floors and the floored verification for the rest; with ``warped_out``
+    the two calls instead).  ``floors``: a pair of f32 device tensors
+    ``[target_rows]``, ``[draft_rows]`` of precomputed floors (used instead of
+    top_k / top_p; either may be None)."""
     m = _Marshal(target_logits)
     tg = _rows(m.dev(target_logits))
     dr = _rows(m.dev(draft_logits, tg.dtype))
@@ -175,8 +177,14 @@ def accept_from_logits(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     n, nxt, st = m.outputs(B)
     lib = _lib.load()
     if floors is None and (top_k is not None or top_p is not None):
-        floors = _floors(lib, m, tg, dr, T, m.dev(top_k, torch.int32), m.dev(top_p, torch.float32),
-                         cu, B, K, sum_k)
+        tk, tp = m.dev(top_k, torch.int32), m.dev(top_p, torch.float32)
+        if warped_out is None:
+            with torch.cuda.device(m.device):
+                _check(lib.sv_accept_from_logits_filtered(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T),
+                                                          _p(tk), _p(tp), _p(tok), _p(u), _p(cu), B, K, sum_k,
+                                                          tg.shape[1], _p(n), _p(nxt), _p(st), flags, m.stream()))
+            return m.finish(VerifyResult(n, nxt, st))
+        floors = _floors(lib, m, tg, dr, T, tk, tp, cu, B, K, sum_k)
     with torch.cuda.device(m.device):
         if floors is None:
             _check(lib.sv_accept_from_logits(_p(tg), _p(dr), _DTYPES[tg.dtype], tg.stride(0), _p(T),

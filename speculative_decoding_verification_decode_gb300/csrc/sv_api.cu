@@ -358,7 +358,7 @@ sv_status svh::accept_logits(const void* target_logits, const void* draft_logits
                              int32_t sum_k, int32_t vocab, const float* floor_target,
                              const float* floor_draft, int32_t* n_accepted, int32_t* next_token,
                              uint32_t* status, float* warped_target_out, float* warped_draft_out,
-                             const uint32_t* ext_err, uint32_t flags, void* stream) {
+                             const uint32_t* ext_err, uint32_t flags, void* stream, const int* gate) {
   sv_status s = check_common(target_logits, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab,
                              n_accepted, next_token, status, flags);
   if (s != SV_OK || batch == 0) return s;
@@ -379,6 +379,7 @@ sv_status svh::accept_logits(const void* target_logits, const void* draft_logits
   p.flo_t = floor_target;
   p.flo_d = floor_draft;
   p.ext_err = ext_err;
+  p.gate = gate;
   p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
               (row_stride * elem) % 16 == 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -421,6 +422,60 @@ sv_status sv_accept_from_logits_floored(const void* target_logits, const void* d
                             uniforms, cu_k, batch, k, sum_k, vocab, floor_target, floor_draft, n_accepted,
                             next_token, status, warped_target_out, warped_draft_out, nullptr, flags,
                             stream);
+}
+
+sv_status sv_accept_from_logits_filtered(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                                         int64_t row_stride, const float* temperature, const int32_t* top_k,
+                                         const float* top_p, const int32_t* draft_tokens, const float* uniforms,
+                                         const int32_t* cu_k, int32_t batch, int32_t k, int32_t sum_k,
+                                         int32_t vocab, int32_t* n_accepted, int32_t* next_token,
+                                         uint32_t* status, uint32_t flags, void* stream) {
+  if (!top_k && !top_p)
+    return svh::accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens, uniforms,
+                              cu_k, batch, k, sum_k, vocab, nullptr, nullptr, n_accepted, next_token, status,
+                              nullptr, nullptr, nullptr, flags, stream);
+  // every host check of the verification and of the floors before anything is enqueued
+  sv_status s = check_common(target_logits, row_stride, draft_tokens, cu_k, batch, k, sum_k, vocab, n_accepted,
+                             next_token, status, flags);
+  if (s != SV_OK || batch == 0) return s;
+  if (dtype != SV_F32 && dtype != SV_BF16 && dtype != SV_F16)
+    return fail(SV_ERR_ARG, "unknown dtype %d", static_cast<int>(dtype));
+  if (sum_k > 0 && !draft_logits) return fail(SV_ERR_ARG, "draft_logits is NULL");
+  if (!uniforms) return fail(SV_ERR_ARG, "uniforms is NULL");
+  if (!temperature) return fail(SV_ERR_ARG, "temperature is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* gate = nullptr;
+  float *ft = nullptr, *fd = nullptr;
+  if (!svh::rows_filter_scratch(st, batch, sum_k + batch, &gate, &ft, &fd))
+    return fail(SV_ERR_UNSUPPORTED, "no scratch slot for the floors on this stream (or a call beyond one)");
+  const int elem = dtype == SV_F32 ? 4 : 2;
+  bool fused = false;
+  // The fused plan decides the sequences its candidate lists can decide; the
+  // floors and the floored verification then run for the rest only.  It pays
+  // a wave of row-parallel items per accepted row, the two steps one floors
+  // CTA per row: measured on GB300 at V = 128256 bf16, top-k 50 / top-p 0.9,
+  // B = 64 K = 5 146 against 191 us, B = 256 K = 3 (V = 32000) 135 against
+  // 212 us, B = 4 K = 5 58 against 74 us, but B = 16 K = 5 91 against 84 us
+  // and B = 8 K = 16 109 against 86 us.  So it takes batches whose rows to
+  // filter exceed two per SM, or stay under half an SM count.
+  const long long filt_rows = 2LL * sum_k + batch;
+  const bool fused_shape = filt_rows > 2LL * sm_count() || 2 * filt_rows < sm_count();
+  if (dtype != SV_F32 && top_k && !(flags & SV_FLAG_PLAN_CHAIN) && (fused_shape || (flags & SV_FLAG_PLAN_ROWS))) {
+    svk::Params p = base_params(target_logits, draft_logits, row_stride, draft_tokens, uniforms, cu_k,
+                                temperature, batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
+    p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
+                (row_stride * elem) % 16 == 0;
+    s = svh::launch_rows_topk(dtype, p, top_k, top_p, st);
+    if (s == SV_OK) fused = true;
+    else if (s != SV_ERR_UNSUPPORTED) return s;
+    else g_err[0] = '\0';
+  }
+  s = svh::sampler_floors_gated(target_logits, draft_logits, dtype, row_stride, temperature, top_k, top_p, cu_k,
+                                batch, k, sum_k, vocab, ft, fd, fused ? gate : nullptr, stream);
+  if (s != SV_OK) return s;
+  return svh::accept_logits(target_logits, draft_logits, dtype, row_stride, temperature, draft_tokens, uniforms, cu_k,
+                            batch, k, sum_k, vocab, ft, fd, n_accepted, next_token, status, nullptr, nullptr,
+                            nullptr, flags, stream, fused ? gate : nullptr);
 }
 
 size_t sv_workspace_size(int32_t batch, int32_t k, int32_t vocab, int32_t mode) {

@@ -63,6 +63,7 @@ struct Args {
   int B, K, V, sum_k;
   float* ft;
   float* fd;
+  const int* gate;  // per sequence: 0 = skip (NULL: every sequence)
 };
 
 // Order-preserving keys and the radix levels over them (widths 11 + 11 + 10
@@ -385,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 2) floors_kernel(const __grid_consta
 
   const long long b = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
   if (b >= a.B) return;
+  if (a.gate && !a.gate[b]) return;
   int kb = a.K;
   long long t0 = b * (a.K + 1LL), d0 = b * static_cast<long long>(a.K);
   if (a.cu_k) {
@@ -685,6 +687,15 @@ extern "C" sv_status sv_sampler_floors(const void* target_logits, const void* dr
                                        int32_t sum_k, int32_t vocab, float* floor_target, float* floor_draft,
                                        void* stream) {
   svh::clear_error();
+  return svh::sampler_floors_gated(target_logits, draft_logits, dtype, row_stride, temperature, top_k, top_p, cu_k,
+                                   batch, k, sum_k, vocab, floor_target, floor_draft, nullptr, stream);
+}
+
+sv_status svh::sampler_floors_gated(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                                    int64_t row_stride, const float* temperature, const int32_t* top_k,
+                                    const float* top_p, const int32_t* cu_k, int32_t batch, int32_t k,
+                                    int32_t sum_k, int32_t vocab, float* floor_target, float* floor_draft,
+                                    const int* gate, void* stream) {
   if (batch < 0) return svh::fail(SV_ERR_ARG, "batch must be >= 0 (got %d)", batch);
   if (k < 0) return svh::fail(SV_ERR_ARG, "k must be >= 0 (got %d)", k);
   if (vocab < 1) return svh::fail(SV_ERR_ARG, "vocab must be >= 1 (got %d)", vocab);
@@ -718,6 +729,7 @@ extern "C" sv_status sv_sampler_floors(const void* target_logits, const void* dr
   a.sum_k = sum_k;
   a.ft = floor_target;
   a.fd = floor_draft;
+  a.gate = gate;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dtype) {
     case SV_F32: return svf::launch<float>(a, st);

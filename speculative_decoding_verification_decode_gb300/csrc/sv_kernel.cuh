@@ -83,6 +83,7 @@ struct Params {
   const float* flo_t;  // per-row floors of the sampler filters (NULL: none)
   const float* flo_d;
   const unsigned* ext_err;  // nonzero word: the kernel that wrote the rows gave up (NULL: none)
+  const int* gate;          // per sequence: 0 = leave the sequence to another launch (NULL: every one)
   unsigned flags;
   int slice;       // elements per CTA slice (multiple of the vector width)
   int slot_bytes;  // bytes per ring slot (multiple of 16)

@@ -137,6 +137,10 @@ __device__ __forceinline__ void dsmem_st_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

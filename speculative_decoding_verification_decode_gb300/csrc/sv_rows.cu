@@ -27,6 +27,9 @@ constexpr int kMaxRows = 1 << 18;  // target rows per launch (sum_k + B)
 static __device__ int g_count[kSlots][kMaxSeq];
 static __device__ int g_first[kSlots][kMaxSeq];
 static __device__ uint4 g_rec[kSlots][kMaxRows];
+// the filtered verification: per sequence the fallback flag, per row the floor
+static __device__ int g_flag[kSlots][kMaxSeq];
+static __device__ float g_floor[kSlots][2][kMaxRows];
 
 struct Slot {
   bool used;
@@ -34,6 +37,9 @@ struct Slot {
   int* count;
   int* first;
   uint4* rec;
+  int* flag;
+  float* floor_t;
+  float* floor_d;
 };
 
 std::mutex g_slot_mutex;
@@ -59,9 +65,10 @@ bool slot_for(cudaStream_t stream, Slot& out) {
     }
   }
   if (!free_slot) return false;
-  void *pc = nullptr, *pf = nullptr, *pr = nullptr;
+  void *pc = nullptr, *pf = nullptr, *pr = nullptr, *pg = nullptr, *pl = nullptr;
   if (cudaGetSymbolAddress(&pc, g_count) != cudaSuccess || cudaGetSymbolAddress(&pf, g_first) != cudaSuccess ||
-      cudaGetSymbolAddress(&pr, g_rec) != cudaSuccess) {
+      cudaGetSymbolAddress(&pr, g_rec) != cudaSuccess || cudaGetSymbolAddress(&pg, g_flag) != cudaSuccess ||
+      cudaGetSymbolAddress(&pl, g_floor) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
@@ -70,6 +77,9 @@ bool slot_for(cudaStream_t stream, Slot& out) {
   free_slot->count = static_cast<int*>(pc) + static_cast<size_t>(free_idx) * kMaxSeq;
   free_slot->first = static_cast<int*>(pf) + static_cast<size_t>(free_idx) * kMaxSeq;
   free_slot->rec = static_cast<uint4*>(pr) + static_cast<size_t>(free_idx) * kMaxRows;
+  free_slot->flag = static_cast<int*>(pg) + static_cast<size_t>(free_idx) * kMaxSeq;
+  free_slot->floor_t = static_cast<float*>(pl) + static_cast<size_t>(free_idx) * 2 * kMaxRows;
+  free_slot->floor_d = free_slot->floor_t + kMaxRows;
   out = *free_slot;
   return true;
 }
@@ -87,7 +97,10 @@ struct RowsPlan {
   size_t smem;
 };
 
-bool rows_plan(bool sampling, int V, int elem, RowsPlan& p) {
+// topk: the fused filters' plan (16-bit rows): room for the candidate lists
+// and the radix histogram beside the draw sums, and for rank 0's receive area
+// and work space inside the row slices.
+bool rows_plan(bool sampling, int V, int elem, RowsPlan& p, bool topk = false) {
   const int vec = 16 / elem;
   const long long row_bytes = static_cast<long long>(V) * elem;
   const long long cap = sampling ? kSampleSliceBytes : kGreedySliceBytes;
@@ -104,6 +117,11 @@ bool rows_plan(bool sampling, int V, int elem, RowsPlan& p) {
   const long long nvt = (slice + vec - 1) / vec;
   size_t vs = static_cast<size_t>((nvt + svk::kGroupVecs - 1) / svk::kGroupVecs) * 8;
   if (vs < 2 * svk::kBuckets * 8) vs = 2 * svk::kBuckets * 8;
+  if (topk) {
+    if (vs < static_cast<size_t>(2 * svk::kListCap * 8 + 1024 + 64)) vs = 2 * svk::kListCap * 8 + 1024 + 64;
+    const size_t recv = 256 + static_cast<size_t>(p.C) * 2 * svk::kListCap * 8 + svk::kTopkScratch;
+    if (!sampling || recv > rows) return false;
+  }
   p.vsum_off = static_cast<int>(rows);
   p.tail_off = static_cast<int>(round_up(rows + vs, 128));
   p.smem = p.tail_off + sizeof(svk::RowsTail);
@@ -122,18 +140,18 @@ struct Cache {
   size_t smem_fit[svk::kMaxCluster + 1];
 };
 
-template <int MODE, typename T, bool FL>
+template <int MODE, typename T, bool FL, bool TOPK = false>
 Cache& cache_of(int dev) {
   static Cache c[64] = {};
   return c[dev >= 0 && dev < 64 ? dev : 0];
 }
 
-template <int MODE, typename T, bool FL>
+template <int MODE, typename T, bool FL, bool TOPK = false>
 sv_status launch_t(svk::RowsParams rp, const RowsPlan& pl, long long blocks, cudaStream_t stream) {
-  auto kern = svk::sv_rows_kernel<MODE, T, FL>;
+  auto kern = svk::sv_rows_kernel<MODE, T, FL, TOPK>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  Cache& kc = cache_of<MODE, T, FL>(dev);
+  Cache& kc = cache_of<MODE, T, FL, TOPK>(dev);
   cudaError_t e;
   if (kc.smem_set < pl.smem) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
@@ -209,6 +227,9 @@ sv_status svh::launch_rows(int mode, sv_dtype dtype, const svk::Params& p, bool 
   rp.seq_count = sl.count;
   rp.seq_first = sl.first;
   rp.rec = sl.rec;
+  rp.seq_flag = nullptr;
+  rp.top_k = nullptr;
+  rp.top_p = nullptr;
   rp.nadd = pl.nadd;
   rp.x_off = pl.x_off;
   rp.vsum_off = pl.vsum_off;
@@ -226,4 +247,43 @@ sv_status svh::launch_rows(int mode, sv_dtype dtype, const svk::Params& p, bool 
       if (dtype == SV_BF16) return launch_m<svk::MODE_LOGITS, __nv_bfloat16>(rp, pl, blocks, filtered, stream);
       return launch_m<svk::MODE_LOGITS, __half>(rp, pl, blocks, filtered, stream);
   }
+}
+
+bool svh::rows_filter_scratch(cudaStream_t stream, int batch, int t_rows, int** flag, float** floor_t,
+                              float** floor_d) {
+  if (batch < 0 || batch > kMaxSeq || t_rows < 0 || t_rows > kMaxRows) return false;
+  Slot sl;
+  if (!slot_for(stream, sl)) return false;
+  *flag = sl.flag;
+  *floor_t = sl.floor_t;
+  *floor_d = sl.floor_d;
+  return true;
+}
+
+sv_status svh::launch_rows_topk(sv_dtype dtype, const svk::Params& p, const int32_t* top_k, const float* top_p,
+                                cudaStream_t stream) {
+  if (dtype == SV_F32 || !top_k) return fail(SV_ERR_UNSUPPORTED, "fused filters: 16-bit logits with top-k only");
+  if (p.B < 1 || p.B > kMaxSeq || static_cast<long long>(p.sum_k) + p.B > kMaxRows || p.wt_out || p.wd_out)
+    return fail(SV_ERR_UNSUPPORTED, "fused filters: shape beyond the scratch");
+  RowsPlan pl;
+  if (!rows_plan(true, p.V, 2, pl, true)) return fail(SV_ERR_UNSUPPORTED, "fused filters: vocab %d", p.V);
+  const long long blocks = static_cast<long long>(pl.C) * p.B * (p.K + 1LL);
+  if (blocks > 0x7FFFFFFFLL) return fail(SV_ERR_UNSUPPORTED, "fused filters: too many rows");
+  Slot sl;
+  if (!slot_for(stream, sl)) return fail(SV_ERR_UNSUPPORTED, "fused filters: no scratch slot for this stream");
+  svk::RowsParams rp;
+  rp.p = p;
+  rp.p.slice = pl.slice;
+  rp.seq_count = sl.count;
+  rp.seq_first = sl.first;
+  rp.rec = sl.rec;
+  rp.seq_flag = sl.flag;
+  rp.top_k = top_k;
+  rp.top_p = top_p;
+  rp.nadd = pl.nadd;
+  rp.x_off = pl.x_off;
+  rp.vsum_off = pl.vsum_off;
+  rp.tail_off = pl.tail_off;
+  if (dtype == SV_BF16) return launch_t<svk::MODE_LOGITS, __nv_bfloat16, true, true>(rp, pl, blocks, stream);
+  return launch_t<svk::MODE_LOGITS, __half, true, true>(rp, pl, blocks, stream);
 }

@@ -21,12 +21,14 @@
 // Nothing waits on another cluster: the only waits are on the CTA's own bulk
 // copies and on the cluster's exchanges, all bounded.
 #pragma once
+#include "sv_topk.cuh"
 #include "sv_verify.cuh"
 
 namespace svk {
 
 constexpr int kRowsThreads = 256;  // 8 warps, every one reduces
 constexpr uint32_t kRecTerminal = 0x80000000u;
+constexpr uint32_t kRecFallback = 0x40000000u;  // fused filters: this row needs the general path
 constexpr int kRowsExchanges = 5;  // row statistics, (unused), exact limbs, draw, draw from p
 
 struct RowsParams {
@@ -34,6 +36,9 @@ struct RowsParams {
   int* seq_count;  // per sequence: items arrived (0 between launches)
   int* seq_first;  // per sequence: INT_MAX - (first terminal row posted), 0 when none
   uint4* rec;      // per target row: {status | kRecTerminal, next, n, 0}
+  int* seq_flag;   // fused filters: per sequence 1 = handed to the fallback (NULL otherwise)
+  const int* top_k;    // fused filters: per sequence top-k (NULL otherwise)
+  const float* top_p;  // fused filters: per sequence top-p (NULL: none)
   int nadd;        // fp32 additions of any element inside its thread (mass bounds)
   int x_off;       // byte offset of the draft slice
   int vsum_off;    // byte offset of the draw's group sums / the exact buckets
@@ -54,6 +59,8 @@ struct __align__(16) RowsTail {
   int t;
   float u, ud, gp, gq, lo_p, lo_q;
   int skip;
+  int kk;    // fused filters: the sequence's top-k and top-p
+  float pp;
   // the cluster's view after an exchange (written by warp 0)
   float fv[6];
   uint32_t iv[4];
@@ -92,9 +99,73 @@ __device__ __forceinline__ int smem_draw_weights(const T* p, const T* q, int n, 
 
 namespace svk {
 
-enum : int { OUT_ACCEPT = 0, OUT_TERM = 1, OUT_SKIP = 2, OUT_TIMEOUT = 3, OUT_DRAW = 4 };
+enum : int { OUT_ACCEPT = 0, OUT_TERM = 1, OUT_SKIP = 2, OUT_TIMEOUT = 3, OUT_DRAW = 4, OUT_FALLBACK = 5 };
 
-template <int MODE, typename T, bool FL = false>
+// Warp 0 of an item's rank-0 CTA, after the item is decided: writes the
+// item's record (unless it skipped), counts the item in, and, when it is the
+// last of the sequence's kb + 1 items, combines the records into the
+// sequence's outputs and returns the counter and the posted row to zero.
+// Records are read 32 rows per load round; the first terminal record ends
+// the walk and the statuses of the rows up to it are ORed.  A record marked
+// kRecFallback ends the walk as well but hands the sequence to the general
+// path (seq_flag[b] = 1, outputs left to it).
+__device__ __forceinline__ void rows_record_combine(const RowsParams& R, int b, int i, int kb, long long t0,
+                                                    bool write, uint4 rv) {
+  const Params& P = R.p;
+  const int lane = threadIdx.x & 31;
+  int last = 0;
+  if (lane == 0) {
+    if (write) R.rec[t0 + i] = rv;
+    __threadfence();
+    last = atomicAdd(R.seq_count + b, 1) == kb ? 1 : 0;
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (!last) return;  // every record of the sequence is written once the count is complete
+  __threadfence();
+  uint32_t st = 0u;
+  int n = 0, nxt = -1;
+  bool term = false, fb = false;
+  for (int base = 0; base <= kb && !term; base += 32) {
+    const int r = base + lane;
+    const uint4 v = r <= kb ? __ldcg(R.rec + t0 + r) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t tm = __ballot_sync(0xFFFFFFFFu, r <= kb && (v.x & (kRecTerminal | kRecFallback)) != 0u);
+    const int first = tm ? __ffs(tm) - 1 : 32;
+    st |= __reduce_or_sync(0xFFFFFFFFu,
+                           (lane <= first && r <= kb) ? (v.x & ~(kRecTerminal | kRecFallback)) : 0u);
+    if (tm) {
+      nxt = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.y), first);
+      n = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.z), first);
+      fb = (__shfl_sync(0xFFFFFFFFu, v.x, first) & kRecFallback) != 0u;
+      term = true;
+    }
+  }
+  if (lane == 0) {
+    if (fb) {
+      R.seq_flag[b] = 1;
+    } else {
+      if (!term || (st & ST_TIMEOUT)) {
+        n = 0;
+        nxt = -1;
+        st = ST_TIMEOUT;
+      }
+      if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
+        n = 0;
+        nxt = -1;
+        st |= ST_TIMEOUT;
+      }
+      P.n_out[b] = n;
+      P.next_out[b] = nxt;
+      P.st_out[b] = st;
+      if (R.seq_flag) R.seq_flag[b] = 0;
+    }
+    R.seq_count[b] = 0;  // ready for the next launch
+    R.seq_first[b] = 0;
+  }
+}
+
+// TOPK: the sequences' top-k / top-p floors are computed here (16-bit logits,
+// 1 <= top-k <= kTopKMax) instead of coming from the floors kernel.
+template <int MODE, typename T, bool FL = false, bool TOPK = false>
 __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_constant__ RowsParams R) {
   static_assert(kRowsThreads == kConsumers, "the chunk passes stride by kConsumers threads");
   const Params& P = R.p;
@@ -117,6 +188,7 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   const long long item = blockIdx.x / C;
   const int b = static_cast<int>(item % P.B);
   const int i = static_cast<int>(item / P.B);
+  if (P.gate && !P.gate[b]) return;  // the whole cluster shares b
 
   // ---------------------------------------------------------------- sequence layout
   int kb = P.K;
@@ -145,6 +217,7 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       P.n_out[b] = 0;
       P.next_out[b] = -1;
       P.st_out[b] = (layout_ok ? ST_BAD_VALUE : ST_BAD_LAYOUT) | (P.ext_err && *P.ext_err ? ST_TIMEOUT : 0u);
+      if (R.seq_flag) R.seq_flag[b] = 0;
     }
     return;
   }
@@ -165,6 +238,15 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       const int s = *reinterpret_cast<const volatile int*>(R.seq_first + b);
       skip = (s != 0 && INT_MAX - s < i) ? 1 : 0;
     }
+    if constexpr (TOPK) {
+      // a fused-filter row the candidate lists cannot decide (top-k outside
+      // [1, kTopKMax]) or an invalid top-p needs no rows: load nothing
+      if (sampling) {
+        const int kk0 = R.top_k ? R.top_k[b] : 0;
+        const float pp0 = R.top_p ? R.top_p[b] : 1.f;
+        if (!(kk0 >= 1 && kk0 <= kTopKMax && kk0 < P.V) || !(pp0 > 0.f)) skip |= 2;
+      }
+    }
     sm.skip = skip;
     for (int x = 0; x < kRowsExchanges; ++x) mbar_init(&sm.xbar[x], C);
     mbar_init(&sm.full, 1);
@@ -173,10 +255,29 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
     fence_mbar_init_cluster();
   }
   __syncthreads();
-  const bool skip_mine = sm.skip != 0;
+  const bool skip_mine = (sm.skip & 1) != 0;
+  const bool no_rows = (sm.skip & 2) != 0;  // fused filters: this item decides without its rows
+  if (TOPK && sampling && no_rows) {
+    // the same for every CTA of the cluster (read from the same words): rank 0
+    // records the row's outcome without rows, barriers or exchanges: a bad
+    // draft id, else a NaN floor (invalid top-p), else the general path
+    if (rank != 0) return;
+    if (warp == 0) {
+      uint32_t rs = ST_BAD_VALUE | kRecTerminal;
+      if (!bonus) {
+        const int t = P.tok[d0 + i];
+        if (t < 0 || t >= P.V) rs = ST_BAD_TOKEN | kRecTerminal;
+      }
+      const float pp0 = R.top_p ? R.top_p[b] : 1.f;
+      if (rs == (ST_BAD_VALUE | kRecTerminal) && pp0 > 0.f) rs = kRecFallback;
+      if (lane == 0) atomicMax(R.seq_first + b, INT_MAX - i);
+      rows_record_combine(R, b, i, kb, t0, true, make_uint4(rs, 0xFFFFFFFFu, static_cast<uint32_t>(i), 0u));
+    }
+    return;
+  }
 
   // ---------------------------------------------------------------- loads
-  if (!skip_mine) {
+  if (!skip_mine && !no_rows) {
     if (P.use_tma) {
       if (warp == 0) {
         const uint32_t bytes = static_cast<uint32_t>(n_el) * static_cast<uint32_t>(sizeof(T));
@@ -227,10 +328,14 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       }
       sm.lo_p = lp;
       sm.lo_q = lq;
+      if constexpr (TOPK) {
+        sm.kk = R.top_k ? R.top_k[b] : 0;
+        sm.pp = R.top_p ? R.top_p[b] : 1.f;
+      }
     }
   }
   int bad = 0;  // this CTA's wait for its own copies gave up
-  if (!skip_mine && P.use_tma) bad = mbar_wait_bounded(&sm.full, 0u) ? 0 : 1;
+  if (!skip_mine && !no_rows && P.use_tma) bad = mbar_wait_bounded(&sm.full, 0u) ? 0 : 1;
   __syncthreads();
 
   // Exchange of sm.my with every CTA of the cluster through exchange slot x
@@ -325,6 +430,426 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
         else if (t == a) out = OUT_ACCEPT;
       }
       if (out == OUT_TERM) post_terminal();
+    }
+  } else if constexpr (TOPK) {
+    // ============================================================== sampling, fused top-k / top-p
+    // Every CTA takes, per row, the keys of its slice at or above the
+    // slice's k-th largest key: the row's k-th largest key is at least every
+    // slice's, so the union of these lists holds every key the filters keep.
+    // Rank 0 gathers the lists and finds the floors, the masses of the kept
+    // tokens, the decision and the draw on them alone (a logit below the
+    // floor weighs 0 everywhere).  A row outside what the lists can decide
+    // (top-k outside [1, kTopKMax], a list or kept set over its capacity)
+    // is recorded for the general path.
+    static_assert(sizeof(T) == 2 && MODE == MODE_LOGITS && FL, "fused filters: 16-bit logits rows");
+    using KY = Key16x<T>;
+    using WT = typename WarpOf<T>::type;
+    float khi = 0.f, klo = 0.f;
+    log2e_over(temp, khi, klo);
+    const int kk = sm.kk;
+    const float pp = sm.pp;
+    const bool p_ok = pp > 0.f;  // NaN or <= 0: invalid top-p, the floors are NaN
+    const bool use_p = pp < 1.f;
+    const bool fast = kk >= 1 && kk <= kTopKMax && kk < P.V;
+    unsigned char* vsa = smem + R.vsum_off;
+    uint2* lst = reinterpret_cast<uint2*>(vsa);                               // [2][kListCap]
+    unsigned* hist = reinterpret_cast<unsigned*>(vsa + 2 * kListCap * 8);     // [256]
+    int* misc = reinterpret_cast<int*>(vsa + 2 * kListCap * 8 + 1024);        // [16]
+    bad = __syncthreads_or(bad);
+    uint32_t fl = (bad ? 16u : 0u) | (skip_mine ? 8u : 0u);  // 1 / 2 row invalid, 4 list overflow
+    int nl0 = 0, nl1 = 0;
+    if (!bad && !skip_mine && fast && p_ok) {
+      for (int x = 0; x < (two ? 2 : 1); ++x) {
+        const T* s = x ? sq : sp;
+        float mxn = warp_max_nan_f(slice_max_nan16<T>(s, n_el));
+        if (lane == 0) sm.wf[warp][0] = mxn;
+        __syncthreads();
+        float cm = -kInfF;
+        for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w][0]);
+        __syncthreads();
+        if (!(cm < kInfF)) {  // a NaN or +Inf logit: the row is invalid, its list stays empty
+          fl |= x ? 2u : 1u;
+          continue;
+        }
+        // the slice's kk-th largest key: when it lies within 255 keys of the
+        // slice maximum, one histogram of the distance to it over the few
+        // logits in that window (the rest fail one float comparison); else
+        // two radix levels over every key
+        uint32_t kmx;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) KY::key(__float_as_uint(cm) >> 16, kmx);
+        else KY::key(__half_as_ushort(__float2half_rn(cm)), kmx);
+        const float vlo = kmx > 256u ? KY::value(kmx - 255u) : -kInfF;
+        hist[tid] = 0u;
+        __syncthreads();
+        for_values_at_least<T>(s, n_el, vlo, [&](uint32_t raw, int) {
+          uint32_t k;
+          KY::key(raw, k);
+          const uint32_t d = kmx - k;
+          if (d < 256u) atomicAdd(&hist[255u - d], 1u);
+        });
+        __syncthreads();
+        if (warp == 0) {
+          unsigned tot = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) tot += hist[lane * 8 + j];
+          tot = __reduce_add_sync(0xFFFFFFFFu, tot);
+          unsigned ab = 0;
+          const int bin = tot >= static_cast<unsigned>(kk) ? pick_bin_count(hist, 0u, static_cast<unsigned>(kk), ab) : -1;
+          if (lane == 0) misc[0] = bin;
+        }
+        __syncthreads();
+        uint32_t kth = misc[0] < 0 ? 0u : kmx - (255u - static_cast<uint32_t>(misc[0]));
+        if (kth == 0u)
+          kth = kth_largest16([&](auto f) { for_keys16<T>(s, n_el, [&](uint32_t k, int) { f(k); }); },
+                              static_cast<unsigned>(kk), hist, misc);
+        if (tid == 0) misc[2] = 0;
+        __syncthreads();
+        for_values_at_least<T>(s, n_el, KY::value(kth), [&](uint32_t raw, int e) {
+          uint32_t k;
+          KY::key(raw, k);
+          const int at = atomicAdd(&misc[2], 1);
+          if (at < kListCap) lst[x * kListCap + at] = make_uint2(k, static_cast<uint32_t>(v_lo + e));
+        });
+        __syncthreads();
+        const int c = misc[2];
+        if (c > kListCap) fl |= 4u;
+        if (x) nl1 = min(c, kListCap);
+        else nl0 = min(c, kListCap);
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+    cluster_sync_all();  // rank 0 no longer reads its slices: they become its receive area
+    {
+      // rank 0's receive area: [C] headers {n_0, n_1, flags, 0}, then [C][2][kListCap] entries
+      const uint32_t base = dsmem_addr(smem, 0u);
+      if (tid == 0)
+        dsmem_st_v4(base + rank * 16u, make_uint4(static_cast<uint32_t>(nl0), static_cast<uint32_t>(nl1), fl, 0u));
+      const uint32_t lbase = base + 256u + rank * (2u * kListCap * 8u);
+      for (int j = tid; j < nl0 + nl1; j += kRowsThreads) {
+        const int x = j < nl0 ? 0 : 1;
+        const int q = x ? j - nl0 : j;
+        dsmem_st_v2(lbase + static_cast<uint32_t>(x * kListCap + q) * 8u, lst[x * kListCap + q]);
+      }
+    }
+    __syncthreads();
+    cluster_sync_all();  // every list has reached rank 0
+    // Nothing reaches another CTA's shared memory after this point: the
+    // other CTAs leave now (their SM slots take later items) and rank 0
+    // finishes the item alone, without the final cluster barrier.
+    if (rank != 0) {
+      if (bad && tid == 0) mbar_wait_bounded(&sm.full, 0u);  // no copy may land after exit
+      return;
+    }
+    {
+      const uint4* rh = reinterpret_cast<const uint4*>(smem);
+      const uint2* rl = reinterpret_cast<const uint2*>(smem + 256);
+      unsigned char* w0 = smem + 256 + static_cast<size_t>(C) * 2 * kListCap * 8;
+      // rank 0's work space after the lists (kTopkScratch bytes)
+      uint2* kept = reinterpret_cast<uint2*>(w0);                          // [2][kKeptCap]
+      int* ord = reinterpret_cast<int*>(kept + 2 * kKeptCap);             // [kKeptCap] p's kept, by index
+      int* ordq = ord + kKeptCap;                                          // [kKeptCap] q's kept, by index
+      unsigned* hist2 = reinterpret_cast<unsigned*>(ordq + kKeptCap);      // [2][256]
+      uint32_t* tk = hist2 + 2 * 256;                                      // [2][kTopKMax]
+      uint32_t* tko = tk + 2 * kTopKMax;                                   // [2][kTopKMax]
+      unsigned long long* tkw = reinterpret_cast<unsigned long long*>(tko + 2 * kTopKMax);  // [2][kTopKMax]
+      int* rs = reinterpret_cast<int*>(tkw + 2 * kTopKMax);               // [32]
+      float* rsf = reinterpret_cast<float*>(rs + 24);                      // [4] inside rs
+      unsigned long long* bk = reinterpret_cast<unsigned long long*>(vsa);  // exact buckets (over the lists)
+      if (tid == 0) {
+        uint32_t Fa = 0u;
+        for (uint32_t c = 0; c < C; ++c) Fa |= rh[c].z;
+        rs[0] = static_cast<int>(Fa);
+      }
+      __syncthreads();
+      const uint32_t F = static_cast<uint32_t>(rs[0]);
+      const int t = sm.t;
+      const float u = sm.u;
+      uint32_t st = 0u;
+      out = OUT_TERM;
+      o_n = i;
+      o_next = -1;
+      if (F & 16u) {
+        out = OUT_TIMEOUT;
+      } else if (F & 8u) {
+        out = OUT_SKIP;
+      } else {
+        // input errors in the general path's order (a NaN floor is an invalid row)
+        uint32_t err = 0u;
+        if (!bonus && (t < 0 || t >= P.V)) err = ST_BAD_TOKEN;
+        if (!err && !p_ok) err = ST_BAD_VALUE;
+        if (!err && !fast) {
+          out = OUT_FALLBACK;
+        } else {
+          if (!err && (F & 1u)) err = ST_BAD_VALUE;
+          if (!err && two && (F & 2u)) err = ST_BAD_VALUE;
+          if (!err && !(u >= 0.f && u < 1.f)) err = ST_BAD_VALUE;
+          if (err) {
+            o_st = err;
+          } else if (F & 4u) {
+            out = OUT_FALLBACK;
+          } else {
+            // ---- per row, one warp each (warp 0 the target row, warp 1 the
+            // draft row): the maximum, the top-k floor key, the top-p floor key
+            // among the top-k set, and the kept tokens (keys at or above it)
+            if (warp < (two ? 2 : 1)) {
+              const int x = warp;
+              unsigned* hx = hist2 + x * 256;
+              uint32_t* tkx = tk + x * kTopKMax;
+              // every lane runs the same trips; `ok` marks the lanes holding an entry
+              auto each = [&](auto f) {
+                for (uint32_t c = 0; c < C; ++c) {
+                  const int cnt = static_cast<int>(x ? rh[c].y : rh[c].x);
+                  for (int q0 = 0; q0 < cnt; q0 += 32) {
+                    const int q = q0 + lane;
+                    const bool ok = q < cnt;
+                    f(ok ? rl[(c * 2 + x) * kListCap + q] : make_uint2(0u, 0u), ok);
+                  }
+                }
+              };
+              uint32_t km = 0u;
+              each([&](uint2 e, bool ok) { if (ok) km = max(km, e.x); });
+              km = __reduce_max_sync(0xFFFFFFFFu, km);
+              int fbx = km == 0u ? 1 : 0;  // no key listed: cannot happen for a valid row
+              float mrow = -kInfF, flox = -kInfF;
+              int nkx = 0;
+              if (!fbx) mrow = KY::value(km);
+              if (!fbx && mrow > -kInfF) {  // (every logit -Inf: zero mass, no floor)
+                for (int j = lane; j < 256; j += 32) hx[j] = 0u;
+                __syncwarp();
+                each([&](uint2 e, bool ok) {
+                  const uint32_t d = km - e.x;
+                  if (ok && d < 256u) atomicAdd(&hx[255u - d], 1u);
+                });
+                __syncwarp();
+                unsigned tot = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tot += hx[lane * 8 + j];
+                tot = __reduce_add_sync(0xFFFFFFFFu, tot);
+                unsigned ab = 0;
+                const int bin = tot >= static_cast<unsigned>(kk) ? pick_bin_count(hx, 0u, static_cast<unsigned>(kk), ab)
+                                                                 : -1;
+                if (bin < 0) {
+                  fbx = 1;  // the k-th largest lies more than 255 keys below the maximum
+                } else {
+                  const uint32_t key_k = km - (255u - static_cast<uint32_t>(bin));
+                  uint32_t key_f = key_k;
+                  if (use_p && key_k < km) {
+                    int n = 0;
+                    each([&](uint2 e, bool ok) { warp_compact(ok && e.x >= key_k, e.x, tkx, kTopKMax, n); });
+                    if (n > kTopKMax) {
+                      fbx = 1;
+                    } else {
+                      WT wf;
+                      wf.m = mrow;
+                      wf.k = khi;
+                      wf.lo = -kInfF;
+                      auto weight = [&](uint32_t k) -> unsigned long long {
+                        return floor_u64(__fmul_rn(wf(KY::value(k)), 0x1p40f));
+                      };
+                      __syncwarp();
+                      unsigned long long z = 0ull;
+                      for (int j = lane; j < n; j += 32) z += weight(tkx[j]);
+                      z = warp_sum_u64(z);
+                      key_f = top_p_walk(tkx, n, weight, static_cast<double>(pp) * static_cast<double>(z),
+                                         tko + x * kTopKMax, tkw + x * kTopKMax);
+                    }
+                  }
+                  if (!fbx) {
+                    flox = KY::value(key_f);
+                    int n2 = 0;
+                    each([&](uint2 e, bool ok) { warp_compact(ok && e.x >= key_f, e, kept + x * kKeptCap, kKeptCap, n2); });
+                    nkx = n2;
+                    if (n2 > kKeptCap) fbx = 1;
+                  }
+                }
+              }
+              if (lane == 0) {
+                rs[16 + x] = fbx;
+                rs[18 + x] = nkx;
+                rsf[x] = mrow;
+                rsf[2 + x] = flox;
+              }
+            }
+            __syncthreads();
+            const bool fb = rs[16] != 0 || (two && rs[17] != 0);
+            const float m_row[2] = {rsf[0], two ? rsf[1] : -kInfF};
+            const float flo[2] = {rsf[2], two ? rsf[3] : -kInfF};
+            const int nk[2] = {rs[18], two ? rs[19] : 0};
+            if (fb) {
+              out = OUT_FALLBACK;
+            } else if (!(m_row[0] > -kInfF) || (!bonus && !(m_row[1] > -kInfF))) {
+              o_st = ST_ZERO_MASS;
+            } else {
+              WT wfp, wfq;
+              wfp.m = m_row[0];
+              wfp.k = khi;
+              wfp.lo = flo[0];
+              wfq.m = m_row[1];
+              wfq.k = khi;
+              wfq.lo = flo[1];
+              // fp32 masses of the kept tokens (each lane adds at most 8, then a tree)
+              if (warp == 0) {
+                float zp = 0.f, zq = 0.f;
+                for (int j = lane; j < nk[0]; j += 32) zp = __fadd_rn(zp, wfp(KY::value(kept[j].x)));
+                for (int j = lane; j < nk[1]; j += 32) zq = __fadd_rn(zq, wfq(KY::value(kept[kKeptCap + j].x)));
+                zp = warp_sum_f(zp);
+                zq = warp_sum_f(zq);
+                if (lane == 0) {
+                  sm.fv[0] = zp;
+                  sm.fv[1] = zq;
+                }
+              }
+              __syncthreads();
+              const DF Zp = {sm.fv[0], 0.f}, Zq = {sm.fv[1], 0.f};
+              bool have_exact = false;
+              double Zp_ex = 0.0, Zq_ex = 0.0;
+              int dec = 0;
+              if (!bonus) {
+                const float pt = wfp(sm.gp), qt = wfq(sm.gq);
+                dec = filter_decide(u, pt, qt, Zp, sum_bound(Zp.hi, (nk[0] + 31) / 32), Zq,
+                                    sum_bound(Zq.hi, (nk[1] + 31) / 32));
+                if ((P.flags & FLAG_FORCE_EXACT) || dec < 0) {
+                  // the exact masses of the kept tokens (every other weight is 0)
+                  for (int q = tid; q < 2 * kBuckets; q += kRowsThreads) bk[q] = 0ull;
+                  __syncthreads();
+                  for (int j = tid; j < nk[0]; j += kRowsThreads) bucket_add(bk, wfp(KY::value(kept[j].x)));
+                  for (int j = tid; j < nk[1]; j += kRowsThreads)
+                    bucket_add(bk + kBuckets, wfq(KY::value(kept[kKeptCap + j].x)));
+                  __syncthreads();
+                  if (tid == 0) {
+                    buckets_to_limbs(bk, sm.lp);
+                    buckets_to_limbs(bk + kBuckets, sm.lq);
+                    sm.bi[3] = exact_accept(u, pt, qt, sm.lp, sm.lq) ? 1 : 0;
+                  }
+                  __syncthreads();
+                  dec = sm.bi[3];
+                  have_exact = true;
+                  Zp_ex = limbs_to_double(sm.lp);
+                  Zq_ex = limbs_to_double(sm.lq);
+                  st |= ST_EXACT;
+                }
+              }
+              if (!bonus && dec) {
+                out = OUT_ACCEPT;
+                o_st = st;
+              } else {
+                // ---- the bonus from p_K, or the residual after the rejection, with u_K
+                const float ud = sm.ud;
+                o_n = bonus ? kb : i;
+                if (!bonus && !(ud >= 0.f && ud < 1.f)) {
+                  o_st = st | ST_BAD_VALUE;
+                } else {
+                  DrawLogits<true> dw;
+                  dw.scale = __uint_as_float(static_cast<uint32_t>(127 + P.fixed_shift) << 23);
+                  dw.resid = bonus ? 0 : 1;
+                  const float zp = have_exact ? static_cast<float>(Zp_ex) : Zp.hi;
+                  const float zq = bonus ? 1.f : (have_exact ? static_cast<float>(Zq_ex) : Zq.hi);
+                  dw.k = khi;
+                  const DF mk = two_prod(m_row[0], khi), qk = two_prod(m_row[1], khi);
+                  dw.cp = -__fadd_rn(mk.hi, __fadd_rn(mk.lo, log2f(zp)));
+                  dw.cq = bonus ? 0.f : -__fadd_rn(qk.hi, __fadd_rn(qk.lo, log2f(zq)));
+                  dw.lo_p = flo[0];
+                  dw.lo_q = bonus ? -kInfF : flo[1];
+                  // warp 0: the kept tokens of p in index order, their fixed-point
+                  // draw weights, the inverse CDF (0 found, 1 empty residual,
+                  // 2 p has no draw mass)
+                  auto draw_kept = [&](bool resid, uint32_t st_in) -> int {
+                    const int n = nk[0], nq = resid ? nk[1] : 0;
+                    for (int j = lane; j < n; j += 32) {  // p's kept tokens in index order
+                      const uint32_t vj = kept[j].y;
+                      int r = 0;
+                      for (int m = 0; m < n; ++m) r += kept[m].y < vj ? 1 : 0;
+                      ord[r] = j;
+                    }
+                    for (int j = lane; j < nq; j += 32) {  // q's, for a binary search by index
+                      const uint32_t vj = kept[kKeptCap + j].y;
+                      int r = 0;
+                      for (int m = 0; m < nq; ++m) r += kept[kKeptCap + m].y < vj ? 1 : 0;
+                      ordq[r] = j;
+                    }
+                    __syncwarp();
+                    unsigned long long f[8];
+                    unsigned long long tot = 0ull;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                      const int pos = lane * 8 + q;
+                      f[q] = 0ull;
+                      if (pos < n) {
+                        const uint2 e = kept[ord[pos]];
+                        float lq = -kInfF;
+                        if (nq > 0) {  // the draft logit at this token when q keeps it
+                          int lo = 0, hi = nq;
+                          while (lo < hi) {
+                            const int mid = (lo + hi) >> 1;
+                            if (kept[kKeptCap + ordq[mid]].y < e.y) lo = mid + 1;
+                            else hi = mid;
+                          }
+                          if (lo < nq && kept[kKeptCap + ordq[lo]].y == e.y) lq = KY::value(kept[kKeptCap + ordq[lo]].x);
+                        }
+                        f[q] = dw.fix(dw(KY::value(e.x), lq));
+                        tot += f[q];
+                      }
+                    }
+                    unsigned long long inc = tot;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                      const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                      if (lane >= o) inc += v;
+                    }
+                    const unsigned long long Rt = __shfl_sync(0xFFFFFFFFu, inc, 31);
+                    if (Rt == 0ull) return resid ? 1 : 2;
+                    const unsigned long long tau = tau_of(ud, Rt);
+                    const unsigned long long ex = inc - tot;
+                    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, tau >= ex && tau < inc);
+                    int found = -1, near_b = 0;
+                    if (hit) {
+                      const int L = __ffs(hit) - 1;
+                      if (lane == L) {
+                        unsigned long long c = ex;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                          const int pos = lane * 8 + q;
+                          const unsigned long long cur = c + f[q];
+                          if (found < 0 && pos < n && tau < cur) {
+                            const unsigned long long dlo = tau - c, dhi = cur - tau;
+                            found = static_cast<int>(kept[ord[pos]].y);
+                            near_b = static_cast<double>(dlo < dhi ? dlo : dhi) <= 1e-5 * static_cast<double>(Rt) ? 1 : 0;
+                          }
+                          c = cur;
+                        }
+                      }
+                      found = __shfl_sync(0xFFFFFFFFu, found, L);
+                      near_b = __shfl_sync(0xFFFFFFFFu, near_b, L);
+                    }
+                    if (lane == 0) {
+                      sm.out_tok = found;
+                      sm.out_st = found >= 0 ? (st_in | (near_b ? ST_NEAR : 0u)) : ST_TIMEOUT;
+                    }
+                    return 0;
+                  };
+                  if (warp == 0) {
+                    int code = draw_kept(!bonus, st);
+                    if (code == 1) {  // an empty residual: the draw falls back to p
+                      dw.resid = 0;
+                      code = draw_kept(false, st | ST_ZERO_MASS);
+                    }
+                    if (lane == 0) sm.bi[2] = code;
+                  }
+                  __syncthreads();
+                  const int code = sm.bi[2];
+                  if (code == 2) {
+                    o_st = st | ST_ZERO_MASS;
+                  } else {
+                    out = OUT_DRAW;
+                  }
+                }
+              }
+            }
+          }
+        }
+        if (out == OUT_TERM || out == OUT_DRAW || out == OUT_FALLBACK) post_terminal();
+      }
     }
   } else {
     // ============================================================== sampling
@@ -891,61 +1416,21 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   __syncthreads();
   // Peers push records (and the draw's owner its id) into this CTA's shared
   // memory: every thread of the cluster meets here once before any CTA of
-  // the cluster exits or rank 0 reads the drawn id.
-  cluster_sync_all();
+  // the cluster exits or rank 0 reads the drawn id.  (A fused-filter
+  // sampling item has only rank 0 left here, with no exchange pending.)
+  if (!(TOPK && sampling)) cluster_sync_all();
   if (rank == 0 && warp == 0) {
-    int last = 0;
-    if (lane == 0) {
-      uint4 rv = make_uint4(ST_TIMEOUT | kRecTerminal, 0xFFFFFFFFu, 0u, 0u);
-      if (out == OUT_ACCEPT) {
-        rv = make_uint4(o_st, 0u, 0u, 0u);
-      } else if (out == OUT_TERM) {
-        rv = make_uint4(o_st | kRecTerminal, static_cast<uint32_t>(o_next), static_cast<uint32_t>(o_n), 0u);
-      } else if (out == OUT_DRAW && sm.out_tok != INT_MIN) {
-        rv = make_uint4(sm.out_st | kRecTerminal, static_cast<uint32_t>(sm.out_tok), static_cast<uint32_t>(o_n), 0u);
-      }
-      if (out != OUT_SKIP) R.rec[t0 + i] = rv;
-      __threadfence();
-      last = atomicAdd(R.seq_count + b, 1) == kb ? 1 : 0;
+    uint4 rv = make_uint4(ST_TIMEOUT | kRecTerminal, 0xFFFFFFFFu, 0u, 0u);
+    if (out == OUT_ACCEPT) {
+      rv = make_uint4(o_st, 0u, 0u, 0u);
+    } else if (out == OUT_TERM) {
+      rv = make_uint4(o_st | kRecTerminal, static_cast<uint32_t>(o_next), static_cast<uint32_t>(o_n), 0u);
+    } else if (out == OUT_DRAW && sm.out_tok != INT_MIN) {
+      rv = make_uint4(sm.out_st | kRecTerminal, static_cast<uint32_t>(sm.out_tok), static_cast<uint32_t>(o_n), 0u);
+    } else if (out == OUT_FALLBACK) {
+      rv = make_uint4(kRecFallback, 0xFFFFFFFFu, 0u, 0u);
     }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (last) {  // the last of the sequence's kb + 1 items: every record is written
-      __threadfence();
-      // the records, 32 rows per load round: the first terminal row ends the
-      // walk, and the statuses of the rows up to it are ORed
-      uint32_t st = 0u;
-      int n = 0, nxt = -1;
-      bool term = false;
-      for (int base = 0; base <= kb && !term; base += 32) {
-        const int r = base + lane;
-        const uint4 v = r <= kb ? __ldcg(R.rec + t0 + r) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t tm = __ballot_sync(0xFFFFFFFFu, r <= kb && (v.x & kRecTerminal) != 0u);
-        const int first = tm ? __ffs(tm) - 1 : 32;
-        st |= __reduce_or_sync(0xFFFFFFFFu, (lane <= first && r <= kb) ? (v.x & ~kRecTerminal) : 0u);
-        if (tm) {
-          nxt = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.y), first);
-          n = __shfl_sync(0xFFFFFFFFu, static_cast<int>(v.z), first);
-          term = true;
-        }
-      }
-      if (lane == 0) {
-        if (!term || (st & ST_TIMEOUT)) {
-          n = 0;
-          nxt = -1;
-          st = ST_TIMEOUT;
-        }
-        if (P.ext_err && *P.ext_err) {  // the producer of the rows gave up: they are invalid
-          n = 0;
-          nxt = -1;
-          st |= ST_TIMEOUT;
-        }
-        P.n_out[b] = n;
-        P.next_out[b] = nxt;
-        P.st_out[b] = st;
-        R.seq_count[b] = 0;  // ready for the next launch
-        R.seq_first[b] = 0;
-      }
-    }
+    rows_record_combine(R, b, i, kb, t0, out != OUT_SKIP, rv);
   }
 }
 

@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(threads_of(MODE), 2) sv_verify_kernel(const __
 
   const long long b = blockIdx.y + static_cast<long long>(blockIdx.z) * gridDim.y;
   if (b >= P.B) return;  // the whole cluster shares b
+  if (P.gate && !P.gate[b]) return;
   const uint32_t C = cluster_size();
   const uint32_t rank = cluster_rank();
 
