@@ -68,6 +68,9 @@ PROFILE_FILES = {
     "config2": ("sv_verify_kernel_config2_traffic.md", ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh")),
     "long16": ("sv_rows_kernel_long16_traffic.md",
                ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh", "sv_rows.cuh", "sv_rows.cu")),
+    "filter": ("sv_rows_kernel_filter_config2_traffic.md",
+               ("sv_api.cu", "sv_kernel.cuh", "sv_verify.cuh", "sv_ptx.cuh", "sv_rows.cuh", "sv_rows.cu",
+                "sv_topk.cuh")),
 }
 
 

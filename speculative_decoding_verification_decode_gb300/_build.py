@@ -9,7 +9,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 LIB_DIR = os.path.join(PKG_DIR, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsv.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("sv_api.cu", "sv_gate.cu", "sv_filter.cu", "sv_lm_head.cu", "sv_static.cu", "sv_penalties.cu", "sv_rows.cu")]
-HEADERS = [os.path.join(CSRC, f) for f in ("sv_kernel.cuh", "sv_verify.cuh", "sv_rows.cuh", "sv_ptx.cuh", "sv_host.h")] + [
+HEADERS = [os.path.join(CSRC, f) for f in ("sv_kernel.cuh", "sv_verify.cuh", "sv_rows.cuh", "sv_topk.cuh", "sv_ptx.cuh", "sv_host.h")] + [
     os.path.join(os.path.dirname(PKG_DIR), "include", h) for h in ("sv.h", "sv_gate.h", "sv_filter.h", "sv_lm_head.h", "sv_penalties.h")]
 
 NVCC_FLAGS = [

@@ -118,7 +118,8 @@ bool rows_plan(bool sampling, int V, int elem, RowsPlan& p, bool topk = false) {
   size_t vs = static_cast<size_t>((nvt + svk::kGroupVecs - 1) / svk::kGroupVecs) * 8;
   if (vs < 2 * svk::kBuckets * 8) vs = 2 * svk::kBuckets * 8;
   if (topk) {
-    if (vs < static_cast<size_t>(2 * svk::kListCap * 8 + 1024 + 64)) vs = 2 * svk::kListCap * 8 + 1024 + 64;
+    // lists [2][kListCap], histograms [2][256], 16 scalars
+    if (vs < static_cast<size_t>(2 * svk::kListCap * 8 + 2048 + 64)) vs = 2 * svk::kListCap * 8 + 2048 + 64;
     const size_t recv = 256 + static_cast<size_t>(p.C) * 2 * svk::kListCap * 8 + svk::kTopkScratch;
     if (!sampling || recv > rows) return false;
   }

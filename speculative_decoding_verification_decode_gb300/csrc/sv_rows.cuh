@@ -434,8 +434,9 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   } else if constexpr (TOPK) {
     // ============================================================== sampling, fused top-k / top-p
     // Every CTA takes, per row, the keys of its slice at or above the
-    // slice's k-th largest key: the row's k-th largest key is at least every
-    // slice's, so the union of these lists holds every key the filters keep.
+    // slice's k-th largest key (and possibly a few below it): the row's k-th
+    // largest key is at least every slice's, so the union of these lists
+    // holds every key the filters keep.
     // Rank 0 gathers the lists and finds the floors, the masses of the kept
     // tokens, the decision and the draw on them alone (a logit below the
     // floor weighs 0 everywhere).  A row outside what the lists can decide
@@ -453,78 +454,104 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
     const bool fast = kk >= 1 && kk <= kTopKMax && kk < P.V;
     unsigned char* vsa = smem + R.vsum_off;
     uint2* lst = reinterpret_cast<uint2*>(vsa);                               // [2][kListCap]
-    unsigned* hist = reinterpret_cast<unsigned*>(vsa + 2 * kListCap * 8);     // [256]
-    int* misc = reinterpret_cast<int*>(vsa + 2 * kListCap * 8 + 1024);        // [16]
+    unsigned* hist = reinterpret_cast<unsigned*>(vsa + 2 * kListCap * 8);     // [2][256]
+    int* misc = reinterpret_cast<int*>(vsa + 2 * kListCap * 8 + 2048);        // [16]
     bad = __syncthreads_or(bad);
     uint32_t fl = (bad ? 16u : 0u) | (skip_mine ? 8u : 0u);  // 1 / 2 row invalid, 4 list overflow
     int nl0 = 0, nl1 = 0;
+    uint32_t smax = 0u;  // the slice maximum keys of the two rows (16 bits each; 0: none)
     if (!bad && !skip_mine && fast && p_ok) {
-      for (int x = 0; x < (two ? 2 : 1); ++x) {
-        const T* s = x ? sq : sp;
-        float mxn = warp_max_nan_f(slice_max_nan16<T>(s, n_el));
-        if (lane == 0) sm.wf[warp][0] = mxn;
-        __syncthreads();
+      // Both rows go through each pass before the pass's barrier.  (1) The
+      // slice maxima, keeping each thread's own maximum key.  (2) Per row,
+      // one warp takes the kk-th largest of the 256 per-thread maxima: they
+      // are kk distinct logits of the slice, so it is at most the slice's
+      // kk-th largest key.  (3) Every logit at or above it goes to the list
+      // (a packed compare per pair, per-element work only in the rare
+      // vectors that hold one): the keys at or above the slice's kk-th
+      // largest and a few more, which is all rank 0 needs.
+      const int nx = two ? 2 : 1;
+      unsigned* tkey = hist;  // [2][kRowsThreads] per-thread maximum keys
+      for (int x = 0; x < nx; ++x) {
+        const float tm = slice_max_nan16<T>(x ? sq : sp, n_el);  // -Inf for a thread without elements
+        uint32_t k = 0u;  // (a NaN makes the row invalid below)
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) KY::key(__float_as_uint(tm) >> 16, k);
+        else KY::key(__half_as_ushort(__float2half_rn(tm)), k);
+        tkey[x * kRowsThreads + tid] = k;
+        const float mxn = warp_max_nan_f(tm);
+        if (lane == 0) sm.wf[warp][x] = mxn;
+      }
+      __syncthreads();
+      bool live[2] = {false, false};
+      for (int x = 0; x < nx; ++x) {
         float cm = -kInfF;
-        for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w][0]);
-        __syncthreads();
+        for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w][x]);
         if (!(cm < kInfF)) {  // a NaN or +Inf logit: the row is invalid, its list stays empty
           fl |= x ? 2u : 1u;
           continue;
         }
-        // the slice's kk-th largest key: when it lies within 255 keys of the
-        // slice maximum, one histogram of the distance to it over the few
-        // logits in that window (the rest fail one float comparison); else
-        // two radix levels over every key
-        uint32_t kmx;
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) KY::key(__float_as_uint(cm) >> 16, kmx);
-        else KY::key(__half_as_ushort(__float2half_rn(cm)), kmx);
-        const float vlo = kmx > 256u ? KY::value(kmx - 255u) : -kInfF;
-        hist[tid] = 0u;
-        __syncthreads();
-        for_values_at_least<T>(s, n_el, vlo, [&](uint32_t raw, int) {
-          uint32_t k;
-          KY::key(raw, k);
-          const uint32_t d = kmx - k;
-          if (d < 256u) atomicAdd(&hist[255u - d], 1u);
-        });
-        __syncthreads();
-        if (warp == 0) {
-          unsigned tot = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) tot += hist[lane * 8 + j];
-          tot = __reduce_add_sync(0xFFFFFFFFu, tot);
-          unsigned ab = 0;
-          const int bin = tot >= static_cast<unsigned>(kk) ? pick_bin_count(hist, 0u, static_cast<unsigned>(kk), ab) : -1;
-          if (lane == 0) misc[0] = bin;
-        }
-        __syncthreads();
-        uint32_t kth = misc[0] < 0 ? 0u : kmx - (255u - static_cast<uint32_t>(misc[0]));
-        if (kth == 0u)
-          kth = kth_largest16([&](auto f) { for_keys16<T>(s, n_el, [&](uint32_t k, int) { f(k); }); },
-                              static_cast<unsigned>(kk), hist, misc);
-        if (tid == 0) misc[2] = 0;
-        __syncthreads();
-        for_values_at_least<T>(s, n_el, KY::value(kth), [&](uint32_t raw, int e) {
-          uint32_t k;
-          KY::key(raw, k);
-          const int at = atomicAdd(&misc[2], 1);
-          if (at < kListCap) lst[x * kListCap + at] = make_uint2(k, static_cast<uint32_t>(v_lo + e));
-        });
-        __syncthreads();
-        const int c = misc[2];
-        if (c > kListCap) fl |= 4u;
-        if (x) nl1 = min(c, kListCap);
-        else nl0 = min(c, kListCap);
-        __syncthreads();
+        live[x] = true;
+        uint32_t k = 0u;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) KY::key(__float_as_uint(cm) >> 16, k);
+        else KY::key(__half_as_ushort(__float2half_rn(cm)), k);
+        smax |= k << (16 * x);
       }
+      if (warp < nx && live[warp]) {
+        const uint32_t L = kth_of_256(tkey + warp * kRowsThreads, static_cast<unsigned>(kk));
+        if (lane == 0) misc[warp] = static_cast<int>(L);
+      }
+      __syncthreads();
+      // this thread's count of list entries, an exclusive scan of the counts
+      // over the CTA, then the entries at those offsets (no atomics)
+      KeysAtLeast16<T> sel[2] = {KeysAtLeast16<T>(sp, n_el, static_cast<uint32_t>(misc[0])),
+                                 KeysAtLeast16<T>(sq, n_el, static_cast<uint32_t>(misc[1]))};
+      unsigned mine[2] = {0u, 0u};
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+        if (x < nx && live[x]) mine[x] = sel[x].count();
+      unsigned* wt = hist;  // [2][kWarps] (the per-thread maxima are no longer read)
+      unsigned incl[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        unsigned v = mine[x];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+          if (lane >= o) v += t;
+        }
+        incl[x] = v;
+        if (lane == 31) wt[x * kWarps + warp] = v;
+      }
+      __syncthreads();
+      unsigned cnt[2] = {0u, 0u};
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (x >= nx) continue;
+        unsigned base = 0u;
+        for (int w = 0; w < kWarps; ++w) {
+          const unsigned t = wt[x * kWarps + w];
+          if (w < warp) base += t;
+          cnt[x] += t;
+        }
+        if (!live[x]) continue;
+        uint2* lx = lst + x * kListCap;
+        unsigned at = base + incl[x] - mine[x];
+        sel[x].visit([&](uint32_t k, int e) {
+          if (at < static_cast<unsigned>(kListCap)) lx[at] = make_uint2(k, static_cast<uint32_t>(v_lo + e));
+          ++at;
+        });
+      }
+      if (cnt[0] > static_cast<unsigned>(kListCap) || cnt[1] > static_cast<unsigned>(kListCap)) fl |= 4u;
+      nl0 = static_cast<int>(min(cnt[0], static_cast<unsigned>(kListCap)));
+      nl1 = static_cast<int>(min(cnt[1], static_cast<unsigned>(kListCap)));
     }
     __syncthreads();
     cluster_sync_all();  // rank 0 no longer reads its slices: they become its receive area
     {
-      // rank 0's receive area: [C] headers {n_0, n_1, flags, 0}, then [C][2][kListCap] entries
+      // rank 0's receive area: [C] headers {n_0, n_1, flags, slice maximum keys},
+      // then [C][2][kListCap] entries
       const uint32_t base = dsmem_addr(smem, 0u);
       if (tid == 0)
-        dsmem_st_v4(base + rank * 16u, make_uint4(static_cast<uint32_t>(nl0), static_cast<uint32_t>(nl1), fl, 0u));
+        dsmem_st_v4(base + rank * 16u, make_uint4(static_cast<uint32_t>(nl0), static_cast<uint32_t>(nl1), fl, smax));
       const uint32_t lbase = base + 256u + rank * (2u * kListCap * 8u);
       for (int j = tid; j < nl0 + nl1; j += kRowsThreads) {
         const int x = j < nl0 ? 0 : 1;
@@ -548,12 +575,13 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       // rank 0's work space after the lists (kTopkScratch bytes)
       uint2* kept = reinterpret_cast<uint2*>(w0);                          // [2][kKeptCap]
       int* ord = reinterpret_cast<int*>(kept + 2 * kKeptCap);             // [kKeptCap] p's kept, by index
-      int* ordq = ord + kKeptCap;                                          // [kKeptCap] q's kept, by index
-      unsigned* hist2 = reinterpret_cast<unsigned*>(ordq + kKeptCap);      // [2][256]
+      float* lqa = reinterpret_cast<float*>(ord + kKeptCap);               // [kKeptCap] q's logit there
+      unsigned* hist2 = reinterpret_cast<unsigned*>(lqa + kKeptCap);       // [2][256]
       uint32_t* tk = hist2 + 2 * 256;                                      // [2][kTopKMax]
       uint32_t* tko = tk + 2 * kTopKMax;                                   // [2][kTopKMax]
       unsigned long long* tkw = reinterpret_cast<unsigned long long*>(tko + 2 * kTopKMax);  // [2][kTopKMax]
-      int* rs = reinterpret_cast<int*>(tkw + 2 * kTopKMax);               // [32]
+      uint2* tke = reinterpret_cast<uint2*>(tkw + 2 * kTopKMax);          // [2][kTopKMax] top-k entries
+      int* rs = reinterpret_cast<int*>(tke + 2 * kTopKMax);               // [32]
       float* rsf = reinterpret_cast<float*>(rs + 24);                      // [4] inside rs
       unsigned long long* bk = reinterpret_cast<unsigned long long*>(vsa);  // exact buckets (over the lists)
       if (tid == 0) {
@@ -607,8 +635,8 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
                   }
                 }
               };
-              uint32_t km = 0u;
-              each([&](uint2 e, bool ok) { if (ok) km = max(km, e.x); });
+              // the row maximum: the largest slice maximum in the headers
+              uint32_t km = lane < static_cast<int>(C) ? (rh[lane].w >> (16 * x)) & 0xFFFFu : 0u;
               km = __reduce_max_sync(0xFFFFFFFFu, km);
               int fbx = km == 0u ? 1 : 0;  // no key listed: cannot happen for a valid row
               float mrow = -kInfF, flox = -kInfF;
@@ -634,9 +662,19 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
                 } else {
                   const uint32_t key_k = km - (255u - static_cast<uint32_t>(bin));
                   uint32_t key_f = key_k;
+                  int n = -1;  // the top-k set's size, once gathered into tkx / tke
                   if (use_p && key_k < km) {
-                    int n = 0;
-                    each([&](uint2 e, bool ok) { warp_compact(ok && e.x >= key_k, e.x, tkx, kTopKMax, n); });
+                    n = 0;
+                    each([&](uint2 e, bool ok) {  // keys and entries of the top-k set
+                      const bool pr = ok && e.x >= key_k;
+                      const unsigned bl = __ballot_sync(0xFFFFFFFFu, pr);
+                      const int at = n + __popc(bl & ((1u << lane) - 1u));
+                      if (pr && at < kTopKMax) {
+                        tkx[at] = e.x;
+                        tke[x * kTopKMax + at] = e;
+                      }
+                      n += __popc(bl);
+                    });
                     if (n > kTopKMax) {
                       fbx = 1;
                     } else {
@@ -658,7 +696,16 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
                   if (!fbx) {
                     flox = KY::value(key_f);
                     int n2 = 0;
-                    each([&](uint2 e, bool ok) { warp_compact(ok && e.x >= key_f, e, kept + x * kKeptCap, kKeptCap, n2); });
+                    if (n >= 0) {  // the kept set lies within the gathered top-k set
+                      __syncwarp();
+                      for (int q0 = 0; q0 < n; q0 += 32) {
+                        const int q = q0 + lane;
+                        const uint2 e = q < n ? tke[x * kTopKMax + q] : make_uint2(0u, 0u);
+                        warp_compact(q < n && e.x >= key_f, e, kept + x * kKeptCap, kKeptCap, n2);
+                      }
+                    } else {
+                      each([&](uint2 e, bool ok) { warp_compact(ok && e.x >= key_f, e, kept + x * kKeptCap, kKeptCap, n2); });
+                    }
                     nkx = n2;
                     if (n2 > kKeptCap) fbx = 1;
                   }
@@ -754,21 +801,30 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
                   // warp 0: the kept tokens of p in index order, their fixed-point
                   // draw weights, the inverse CDF (0 found, 1 empty residual,
                   // 2 p has no draw mass)
-                  auto draw_kept = [&](bool resid, uint32_t st_in) -> int {
-                    const int n = nk[0], nq = resid ? nk[1] : 0;
-                    for (int j = lane; j < n; j += 32) {  // p's kept tokens in index order
-                      const uint32_t vj = kept[j].y;
+                  // p's kept tokens ranked by vocab index, one thread each (the
+                  // indices are distinct), with the draft logit at each token
+                  // when q keeps it (-Inf otherwise)
+                  static_assert(kKeptCap <= kRowsThreads, "one thread per kept token");
+                  {
+                    const int n = nk[0], nq = bonus ? 0 : nk[1];
+                    if (tid < n) {
+                      const uint32_t vj = kept[tid].y;
                       int r = 0;
+#pragma unroll 4
                       for (int m = 0; m < n; ++m) r += kept[m].y < vj ? 1 : 0;
-                      ord[r] = j;
+                      float lq = -kInfF;
+#pragma unroll 4
+                      for (int m = 0; m < nq; ++m) {
+                        const uint2 e = kept[kKeptCap + m];
+                        if (e.y == vj) lq = KY::value(e.x);
+                      }
+                      ord[r] = tid;
+                      lqa[r] = lq;
                     }
-                    for (int j = lane; j < nq; j += 32) {  // q's, for a binary search by index
-                      const uint32_t vj = kept[kKeptCap + j].y;
-                      int r = 0;
-                      for (int m = 0; m < nq; ++m) r += kept[kKeptCap + m].y < vj ? 1 : 0;
-                      ordq[r] = j;
-                    }
-                    __syncwarp();
+                    __syncthreads();
+                  }
+                  auto draw_kept = [&](bool resid, uint32_t st_in) -> int {
+                    const int n = nk[0];
                     unsigned long long f[8];
                     unsigned long long tot = 0ull;
 #pragma unroll
@@ -777,17 +833,7 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
                       f[q] = 0ull;
                       if (pos < n) {
                         const uint2 e = kept[ord[pos]];
-                        float lq = -kInfF;
-                        if (nq > 0) {  // the draft logit at this token when q keeps it
-                          int lo = 0, hi = nq;
-                          while (lo < hi) {
-                            const int mid = (lo + hi) >> 1;
-                            if (kept[kKeptCap + ordq[mid]].y < e.y) lo = mid + 1;
-                            else hi = mid;
-                          }
-                          if (lo < nq && kept[kKeptCap + ordq[lo]].y == e.y) lq = KY::value(kept[kKeptCap + ordq[lo]].x);
-                        }
-                        f[q] = dw.fix(dw(KY::value(e.x), lq));
+                        f[q] = dw.fix(dw(KY::value(e.x), resid ? lqa[pos] : -kInfF));
                         tot += f[q];
                       }
                     }

@@ -1,7 +1,7 @@
 // Helpers of the row-parallel kernel's fused top-k / top-p path (16-bit
-// logits): order-preserving keys, radix selects over shared-memory key sets,
-// and the top-p walk.  The definitions are those of include/sv_filter.h and
-// the floors kernel (sv_filter.cu): the top-k floor is the k-th largest
+// logits): order-preserving keys, selects over small key sets, packed scans
+// of shared-memory slices, and the top-p walk.  The definitions are those of
+// include/sv_filter.h and the floors kernel (sv_filter.cu): the top-k floor is the k-th largest
 // logit (ties kept); the top-p floor is, among the top-k tokens, the lowest
 // logit whose higher-ranked weight (fp32 weights truncated to multiples of
 // 2^-40, summed exactly as integers) is still below p times the set's total,
@@ -16,8 +16,8 @@ constexpr int kListCap = 256;   // candidates a CTA may contribute per row
 constexpr int kKeptCap = 256;   // kept tokens per row the fused decision and draw take
 // rank 0's work space beyond its receive area: kept sets [2][kKeptCap] (8 B),
 // two index orders [kKeptCap] (4 B), two 256-bin histograms, the top-k sets,
-// their orders and weights [2][kTopKMax] (4 + 4 + 8 B), 32 scalars
-constexpr int kTopkScratch = 2 * kKeptCap * 8 + 2 * kKeptCap * 4 + 2 * 256 * 4 + 2 * kTopKMax * 16 + 32 * 4;
+// their orders, weights and entries [2][kTopKMax] (4 + 4 + 8 + 8 B), 32 scalars
+constexpr int kTopkScratch = 2 * kKeptCap * 8 + 2 * kKeptCap * 4 + 2 * 256 * 4 + 2 * kTopKMax * 24 + 32 * 4;
 
 // Order-preserving 16-bit keys of bf16 / f16 bits: negative values flipped,
 // positive ones with the sign bit set, -0 keyed as +0.  NaN has no key.
@@ -29,6 +29,9 @@ struct Key16x {
     if ((raw & 0x7FFFu) == 0u) raw = 0u;
     k = (raw & 0x8000u) ? (~raw & 0xFFFFu) : (raw | 0x8000u);
     return true;
+  }
+  __device__ __forceinline__ static uint32_t raw(uint32_t k) {  // the bits of a key's value
+    return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
   }
   __device__ __forceinline__ static float value(uint32_t k) {
     const uint32_t raw = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
@@ -76,103 +79,13 @@ __device__ __forceinline__ int pick_bin_count(const unsigned* hist, unsigned abo
   return __shfl_sync(0xFFFFFFFFu, mine, L);
 }
 
-// One count into hist[bin], aggregated over the lanes of the warp that add
-// to the same bin at this point (keys of a row crowd into few bins).
-__device__ __forceinline__ void hist_add(unsigned* hist, uint32_t bin) {
-  const unsigned act = __activemask();
-  const unsigned same = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(same) - 1)) atomicAdd(&hist[bin], __popc(same));
-}
-
-// A slot in a shared-memory list for every lane whose `pred` holds (one
-// atomic per warp); -1 for the other lanes.
-__device__ __forceinline__ int warp_append(int* counter, bool pred) {
-  const unsigned act = __activemask();
-  const unsigned b = __ballot_sync(act, pred);
-  if (!b) return -1;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(b) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(b));
-  base = __shfl_sync(act, base, leader);
-  return pred ? base + __popc(b & ((1u << lane) - 1u)) : -1;
-}
-
-// The lim-th largest key of a source when it lies within 255 keys of the
-// largest key kmax: one histogram of kmax - k over the keys in that window
-// (the rest of the row passes without an atomic).  Returns 0 when fewer than
-// lim keys lie in the window (the caller then takes kth_largest16).
-template <typename Src>
-__device__ __forceinline__ uint32_t kth_near_max16(const Src& src, uint32_t kmax, unsigned lim, unsigned* hist,
-                                                   int* pick) {
-  const int tid = threadIdx.x;
-  __syncthreads();  // earlier readers of hist and pick are done
-  hist[tid] = 0u;
-  __syncthreads();
-  src([&](uint32_t k) {
-    const uint32_t d = kmax - k;
-    if (d < 256u) hist_add(hist, 255u - d);  // bin 255: kmax itself
-  });
-  __syncthreads();
-  if (tid < 32) {
-    unsigned tot = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) tot += hist[tid * 8 + j];
-#pragma unroll
-    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
-    unsigned ab = 0;
-    const int bin = tot >= lim ? pick_bin_count(hist, 0u, lim, ab) : -1;
-    if (tid == 0) pick[0] = bin;
-  }
-  __syncthreads();
-  const int bin = pick[0];
-  return bin < 0 ? 0u : kmax - (255u - static_cast<uint32_t>(bin));
-}
-
-// The lim-th largest 16-bit key of a key source (CTA collective, 256
-// threads): two radix levels of 8 bits over shared-memory histograms.
-// src(f) calls f(key) for every key of the set (each thread its share).
-// Returns 0 for an empty set.  `hist` holds 256 counters; `pick` two ints.
-template <typename Src>
-__device__ __forceinline__ uint32_t kth_largest16(const Src& src, unsigned lim, unsigned* hist, int* pick) {
-  const int tid = threadIdx.x;
-  uint32_t hi = 0;
-  unsigned above = 0;
-  for (int level = 0; level < 2; ++level) {
-    __syncthreads();  // earlier readers of hist and pick are done
-    hist[tid] = 0u;
-    __syncthreads();
-    src([&](uint32_t k) {
-      if (level == 0) hist_add(hist, k >> 8);
-      else if ((k >> 8) == hi) hist_add(hist, k & 0xFFu);
-    });
-    __syncthreads();
-    if (tid < 32) {
-      unsigned ab = 0;
-      const int bin = pick_bin_count(hist, above, lim, ab);
-      if (tid == 0) {
-        pick[0] = bin;
-        pick[1] = static_cast<int>(ab);
-      }
-    }
-    __syncthreads();
-    const int bin = pick[0];
-    if (bin < 0) return 0u;
-    if (level == 0) {
-      hi = static_cast<uint32_t>(bin);
-      above = static_cast<unsigned>(pick[1]);
-    } else {
-      return (hi << 8) | static_cast<uint32_t>(bin);
-    }
-  }
-  return 0u;
-}
-
-// Warp: the top-p floor key of a set of n <= kTopKMax keys tk[0..n): walking
-// the distinct keys from the largest, the lowest key whose higher-ranked
-// weight (keys strictly above it) is below m_lim.  `ord` holds kTopKMax
-// words and `ordw` kTopKMax weights.  Returns the key on every lane (0 when
-// n = 0).
+// Warp: the top-p floor key of a set of n <= kTopKMax keys tk[0..n): among
+// the distinct keys, the lowest whose higher-ranked weight (the keys strictly
+// above it) is below m_lim.  The keys are ranked into descending order
+// (`ord`, with their weights in `ordw`), their weights prefix-summed, and the
+// test taken at every group's first position at once: the weight above grows
+// down the ranking, so the passing groups are a prefix of it and the answer
+// is the last of them.  Returns the key on every lane (0 when n = 0).
 template <typename WFn>
 __device__ __forceinline__ uint32_t top_p_walk(const uint32_t* tk, int n, const WFn& weight, double m_lim,
                                                uint32_t* ord, unsigned long long* ordw) {
@@ -182,6 +95,7 @@ __device__ __forceinline__ uint32_t top_p_walk(const uint32_t* tk, int n, const 
     if (j >= n) continue;
     const uint32_t kj = tk[j];
     int rank = 0;
+#pragma unroll 8
     for (int m = 0; m < n; ++m) {
       const uint32_t km = tk[m];
       rank += (km > kj || (km == kj && m < j)) ? 1 : 0;
@@ -190,24 +104,31 @@ __device__ __forceinline__ uint32_t top_p_walk(const uint32_t* tk, int n, const 
     ordw[rank] = weight(kj);
   }
   __syncwarp();
-  uint32_t ans = 0u;
-  if (lane == 0) {
-    unsigned long long above = 0ull;  // weight of the keys strictly above the current group
-    int j = 0;
-    while (j < n) {
-      const uint32_t g = ord[j];
-      if (!(static_cast<double>(above) < m_lim)) break;
-      ans = g;
-      unsigned long long w = 0ull;
-      while (j < n && ord[j] == g) {
-        w += ordw[j];
-        ++j;
-      }
-      above += w;
-    }
+  // lane l holds ranks 2l and 2l + 1: their exclusive prefix of weight
+  static_assert(kTopKMax == 64, "two ranks per lane");
+  const int r0 = 2 * lane, r1 = r0 + 1;
+  const unsigned long long w0 = r0 < n ? ordw[r0] : 0ull, w1 = r1 < n ? ordw[r1] : 0ull;
+  unsigned long long inc = w0 + w1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  const unsigned long long ex0 = inc - w0 - w1, ex1 = ex0 + w0;
+  // a group starts at rank r when r is 0 or its key differs from rank r - 1's
+  const bool g0 = r0 < n && (r0 == 0 || ord[r0] != ord[r0 - 1]);
+  const bool g1 = r1 < n && ord[r1] != ord[r0];
+  const bool p0 = g0 && static_cast<double>(ex0) < m_lim;
+  const bool p1 = g1 && static_cast<double>(ex1) < m_lim;
+  const unsigned b0 = __ballot_sync(0xFFFFFFFFu, p0), b1 = __ballot_sync(0xFFFFFFFFu, p1);
+  // the last passing group start in rank order
+  int best = -1;
+  if (b0 | b1) {
+    const int l0 = b0 ? 31 - __clz(b0) : -1, l1 = b1 ? 31 - __clz(b1) : -1;
+    best = max(l0 >= 0 ? 2 * l0 : -1, l1 >= 0 ? 2 * l1 + 1 : -1);
   }
   __syncwarp();
-  return __shfl_sync(0xFFFFFFFFu, ans, 0);
+  return best >= 0 ? ord[best] : 0u;
 }
 
 // NaN-propagating maximum of a 16-bit shared-memory slice (+-Inf count as
@@ -227,56 +148,124 @@ __device__ __forceinline__ float slice_max_nan16(const T* s, int n) {
   return m;
 }
 
-// f(key, e) for every non-NaN element e of a 16-bit shared-memory slice
-// (each of the CTA's 256 threads its share; 16-byte vectors, then the tail).
-template <typename T, typename F>
-__device__ __forceinline__ void for_keys16(const T* s, int n, F&& f) {
-  using KY = Key16x<T>;
-  const int nv = n / 8;
-  for (int vi = threadIdx.x; vi < nv; vi += 256) {
-    const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t k;
-      if (KY::key(w[q] & 0xFFFFu, k)) f(k, vi * 8 + 2 * q);
-      if (KY::key(w[q] >> 16, k)) f(k, vi * 8 + 2 * q + 1);
-    }
-  }
-  for (int e = nv * 8 + static_cast<int>(threadIdx.x); e < n; e += 256) {
-    uint32_t k;
-    if (KY::key(reinterpret_cast<const unsigned short*>(s)[e], k)) f(k, e);
-  }
+// 0xFFFF in each 16-bit half of a packed pair a that is >= the same half of
+// t (an ordered compare: NaN gives 0).
+template <typename T>
+__device__ __forceinline__ uint32_t ge_mask2(uint32_t a, uint32_t t) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value)
+    return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&t));
+  else
+    return __hge2_mask(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&t));
 }
 
-// f(value, e) for every element e of a 16-bit shared-memory slice whose value
-// is at least `lo` (a value of the row's type; the row holds no NaN): the
-// comparison runs on the unpacked floats, the caller's work only on the few
-// elements that pass.
-template <typename T, typename F>
-__device__ __forceinline__ void for_values_at_least(const T* s, int n, float lo, F&& f) {
-  const int nv = n / 8;
-  for (int vi = threadIdx.x; vi < nv; vi += 256) {
+// The elements of a 16-bit shared-memory slice (no NaN) whose value is at
+// least that of key `lo_key`, as seen by one thread of 256.  count() counts
+// this thread's share with one packed compare per pair of elements and
+// remembers up to kMarks of the 16-byte vectors that hold one; visit(f) then
+// calls f(key, e) for each of those elements, in vector order, looking only
+// into the remembered vectors (into all of them when there were more).
+template <typename T>
+struct KeysAtLeast16 {
+  static constexpr int kMarks = 4;
+  const T* s;
+  int n;
+  uint32_t t2;  // the floor's bits in both halves
+  int nm = 0;   // vectors of this thread that hold an element
+  int vm[kMarks] = {0, 0, 0, 0};
+  __device__ __forceinline__ KeysAtLeast16(const T* s_, int n_, uint32_t lo_key) : s(s_), n(n_) {
+    const uint32_t r = Key16x<T>::raw(lo_key);
+    t2 = r | (r << 16);
+  }
+  __device__ __forceinline__ unsigned count() {
+    const int nv = n / 8;
+    unsigned c = 0u;
+    for (int vi = threadIdx.x; vi < nv; vi += 256) {
+      const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+      const unsigned cv = __popc(ge_mask2<T>(v.x, t2)) + __popc(ge_mask2<T>(v.y, t2)) +
+                          __popc(ge_mask2<T>(v.z, t2)) + __popc(ge_mask2<T>(v.w, t2));
+      if (cv) {
+#pragma unroll
+        for (int j = 0; j < kMarks; ++j)
+          if (nm == j) vm[j] = vi;
+        ++nm;
+      }
+      c += cv;
+    }
+    c >>= 4;  // 16 mask bits per element
+    for (int e = nv * 8 + static_cast<int>(threadIdx.x); e < n; e += 256)
+      c += ge_mask2<T>(reinterpret_cast<const unsigned short*>(s)[e], t2) & 1u;
+    return c;
+  }
+  template <typename F>
+  __device__ __forceinline__ void emit(int vi, F& f) const {
+    using KY = Key16x<T>;
     const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float a, c;
-      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        a = bf_lo(w[q]);
-        c = bf_hi(w[q]);
-      } else {
-        a = h_lo(w[q]);
-        c = h_hi(w[q]);
+      const uint32_t m = ge_mask2<T>(w[q], t2);
+      uint32_t k = 0u;
+      if (m & 0xFFFFu) {
+        KY::key(w[q] & 0xFFFFu, k);
+        f(k, vi * 8 + 2 * q);
       }
-      if (a >= lo) f(w[q] & 0xFFFFu, vi * 8 + 2 * q);
-      if (c >= lo) f(w[q] >> 16, vi * 8 + 2 * q + 1);
+      if (m >> 16) {
+        KY::key(w[q] >> 16, k);
+        f(k, vi * 8 + 2 * q + 1);
+      }
     }
   }
-  for (int e = nv * 8 + static_cast<int>(threadIdx.x); e < n; e += 256) {
-    const unsigned short raw = reinterpret_cast<const unsigned short*>(s)[e];
-    if (ElemTraits<T>::to_f(s[e]) >= lo) f(static_cast<uint32_t>(raw), e);
+  template <typename F>
+  __device__ __forceinline__ void visit(F&& f) const {
+    const int nv = n / 8;
+    if (nm <= kMarks) {
+#pragma unroll
+      for (int j = 0; j < kMarks; ++j)
+        if (j < nm) emit(vm[j], f);
+    } else {
+      for (int vi = threadIdx.x; vi < nv; vi += 256) {
+        const uint4 v = reinterpret_cast<const uint4*>(s)[vi];
+        if ((ge_mask2<T>(v.x, t2) | ge_mask2<T>(v.y, t2) | ge_mask2<T>(v.z, t2) | ge_mask2<T>(v.w, t2)) != 0u)
+          emit(vi, f);
+      }
+    }
+    for (int e = nv * 8 + static_cast<int>(threadIdx.x); e < n; e += 256) {
+      const uint32_t raw = reinterpret_cast<const unsigned short*>(s)[e];
+      if (ge_mask2<T>(raw, t2) & 1u) {
+        uint32_t k = 0u;
+        Key16x<T>::key(raw, k);
+        f(k, e);
+      }
+    }
   }
+};
+
+// Warp: the lim-th largest of 256 keys keys[0..256) (lim in [1, 256]): the
+// largest L with at least lim keys >= L, by bisection between the smallest
+// and the largest key.
+__device__ __forceinline__ uint32_t kth_of_256(const uint32_t* keys, unsigned lim) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = keys[q * 32 + lane];
+  uint32_t lo = v[0], hi = v[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) {
+    lo = min(lo, v[q]);
+    hi = max(hi, v[q]);
+  }
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);  // every key is >= lo: the answer is in [lo, hi]
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+#pragma unroll 1
+  while (lo < hi) {
+    const uint32_t c = lo + (hi - lo + 1u) / 2u;
+    unsigned cnt = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) cnt += v[q] >= c ? 1u : 0u;
+    if (__reduce_add_sync(0xFFFFFFFFu, cnt) >= lim) lo = c;
+    else hi = c - 1u;
+  }
+  return lo;
 }
 
 // Warp: appends the lanes whose `pred` holds to list[*n..] in lane order
