@@ -190,6 +190,19 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   const int i = static_cast<int>(item / P.B);
   if (P.gate && !P.gate[b]) return;  // the whole cluster shares b
 
+  // the item's scalar inputs, issued together (b < B indexes every
+  // per-sequence array)
+  const float temp_in = MODE == MODE_LOGITS ? P.temp[b] : 0.f;
+  int first_in = 0, kk_in = 0;
+  float pp_in = 1.f;
+  if (tid == 0) {
+    if (i > 0) first_in = *reinterpret_cast<const volatile int*>(R.seq_first + b);
+    if constexpr (TOPK) {
+      kk_in = R.top_k ? R.top_k[b] : 0;
+      pp_in = R.top_p ? R.top_p[b] : 1.f;
+    }
+  }
+
   // ---------------------------------------------------------------- sequence layout
   int kb = P.K;
   long long t0 = static_cast<long long>(b) * (P.K + 1LL), d0 = static_cast<long long>(b) * P.K;
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   float temp = 0.f;
   bool temp_ok = true;
   if (MODE == MODE_LOGITS && layout_ok) {
-    temp = P.temp[b];
+    temp = temp_in;
     temp_ok = temp >= 0.f && temp <= FLT_MAX;
     sampling = temp > 0.f;
   }
@@ -233,19 +246,14 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
   const T* rowq = two ? drf + (d0 + i) * P.stride + v_lo : nullptr;
 
   if (tid == 0) {
-    int skip = 0;
-    if (i > 0) {  // an earlier row of b already ended the sequence
-      const int s = *reinterpret_cast<const volatile int*>(R.seq_first + b);
-      skip = (s != 0 && INT_MAX - s < i) ? 1 : 0;
-    }
+    // an earlier row of b already ended the sequence
+    int skip = (first_in != 0 && INT_MAX - first_in < i) ? 1 : 0;
     if constexpr (TOPK) {
       // a fused-filter row the candidate lists cannot decide (top-k outside
       // [1, kTopKMax]) or an invalid top-p needs no rows: load nothing
-      if (sampling) {
-        const int kk0 = R.top_k ? R.top_k[b] : 0;
-        const float pp0 = R.top_p ? R.top_p[b] : 1.f;
-        if (!(kk0 >= 1 && kk0 <= kTopKMax && kk0 < P.V) || !(pp0 > 0.f)) skip |= 2;
-      }
+      if (sampling && (!(kk_in >= 1 && kk_in <= kTopKMax && kk_in < P.V) || !(pp_in > 0.f))) skip |= 2;
+      sm.kk = kk_in;
+      sm.pp = pp_in;
     }
     sm.skip = skip;
     for (int x = 0; x < kRowsExchanges; ++x) mbar_init(&sm.xbar[x], C);
@@ -268,8 +276,7 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
         const int t = P.tok[d0 + i];
         if (t < 0 || t >= P.V) rs = ST_BAD_TOKEN | kRecTerminal;
       }
-      const float pp0 = R.top_p ? R.top_p[b] : 1.f;
-      if (rs == (ST_BAD_VALUE | kRecTerminal) && pp0 > 0.f) rs = kRecFallback;
+      if (rs == (ST_BAD_VALUE | kRecTerminal) && sm.pp > 0.f) rs = kRecFallback;
       if (lane == 0) atomicMax(R.seq_first + b, INT_MAX - i);
       rows_record_combine(R, b, i, kb, t0, true, make_uint4(rs, 0xFFFFFFFFu, static_cast<uint32_t>(i), 0u));
     }
@@ -328,10 +335,6 @@ __global__ void __launch_bounds__(kRowsThreads, 3) sv_rows_kernel(const __grid_c
       }
       sm.lo_p = lp;
       sm.lo_q = lq;
-      if constexpr (TOPK) {
-        sm.kk = R.top_k ? R.top_k[b] : 0;
-        sm.pp = R.top_p ? R.top_p[b] : 1.f;
-      }
     }
   }
   int bad = 0;  // this CTA's wait for its own copies gave up
