@@ -161,3 +161,34 @@ def test_repeated_calls_and_force_exact():
     assert np.array_equal(one.n_accepted, first.n_accepted)
     ok = (one.status & np.uint32(sv().SEQ_BAD_TOKEN | sv().SEQ_BAD_VALUE | sv().SEQ_ZERO_MASS)) == 0
     assert ((one.status[ok] & np.uint32(sv().SEQ_EXACT_PATH)) > 0).all()
+
+
+@pytest.mark.parametrize("V", [200, 257])
+def test_small_vocab_threads_without_logits(V):
+    """A slice shorter than the CTA's 256 threads: the threads that hold no
+    logit enter the per-thread-maxima bound as -Inf, which can only lower the
+    list floor; top-k up to 64 and 1, top-p on and off."""
+    wl = workloads.make_config("config2", B=12, K=3, V=V)
+    top_k = np.array([64, 1, 2, 50, 63, 10] * 2, np.int32)
+    top_p = np.array([0.5, 1.0, 0.9, 0.95, 0.3, 1.0] * 2, F32)
+    _check(wl, top_k, top_p, f"small vocab {V}")
+    _check(wl, top_k, None, f"small vocab {V}, top-k alone")
+
+
+def test_f16_full_vocab_and_ties_across_slices():
+    """Eight slices per row: f16 rows, and bf16 rows whose largest logits are
+    tied across every slice (600 ties: a top-k set over 64 and a kept set over
+    256, handed to the general path; 2100 ties: a slice's list over its
+    capacity) beside ordinary rows."""
+    f16 = workloads.make_config("config5", B=8, K=3, V=128256)
+    _check(f16, np.full(f16.B, 50, np.int32), np.full(f16.B, 0.9, F32), "f16 V=128256", False)
+    rng = np.random.default_rng(23)
+    wl = workloads.make_config("config2", B=4, K=3, V=128256)
+    from workloads.configs import _bf16_bits_to_f32, f32_to_bf16_bits
+    vals = _bf16_bits_to_f32(wl.target.copy())
+    vals[0, rng.choice(128256, 600, replace=False)] = vals[0].max() + 1.0
+    vals[4, rng.choice(128256, 2100, replace=False)] = vals[4].max() + 1.0
+    wl.target = f32_to_bf16_bits(vals)
+    B = wl.B
+    _check(wl, np.full(B, 50, np.int32), np.full(B, 0.9, F32), "ties across slices", False)
+    _check(wl, np.full(B, 50, np.int32), None, "ties across slices, top-k alone", False)
