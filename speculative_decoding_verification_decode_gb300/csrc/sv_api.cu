@@ -451,16 +451,13 @@ sv_status sv_accept_from_logits_filtered(const void* target_logits, const void* 
   const int elem = dtype == SV_F32 ? 4 : 2;
   bool fused = false;
   // The fused plan decides the sequences its candidate lists can decide; the
-  // floors and the floored verification then run for the rest only.  It pays
-  // a wave of row-parallel items per accepted row, the two steps one floors
-  // CTA per row: measured on GB300 at V = 128256 bf16, top-k 50 / top-p 0.9,
-  // B = 64 K = 5 146 against 191 us, B = 256 K = 3 (V = 32000) 135 against
-  // 212 us, B = 4 K = 5 58 against 74 us, but B = 16 K = 5 91 against 84 us
-  // and B = 8 K = 16 109 against 86 us.  So it takes batches whose rows to
-  // filter exceed two per SM, or stay under half an SM count.
-  const long long filt_rows = 2LL * sum_k + batch;
-  const bool fused_shape = filt_rows > 2LL * sm_count() || 2 * filt_rows < sm_count();
-  if (dtype != SV_F32 && top_k && !(flags & SV_FLAG_PLAN_CHAIN) && (fused_shape || (flags & SV_FLAG_PLAN_ROWS))) {
+  // floors and the floored verification then run for the rest only.  It is
+  // taken for every 16-bit batch with top-k: measured on GB300 at V = 128256
+  // bf16, top-k 50 / top-p 0.9, B = 256 K = 5 197 against 527 us, B = 64
+  // K = 5 95 against 189 us, B = 16 K = 5 62 against 83 us, B = 8 K = 5 47
+  // against 71 us, B = 8 K = 16 72 against 85 us, B = 1 K = 5 46 against 76
+  // us (one A/B call).
+  if (dtype != SV_F32 && top_k && !(flags & SV_FLAG_PLAN_CHAIN)) {
     svk::Params p = base_params(target_logits, draft_logits, row_stride, draft_tokens, uniforms, cu_k,
                                 temperature, batch, k, vocab, sum_k, n_accepted, next_token, status, flags);
     p.use_tma = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) &&
