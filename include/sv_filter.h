@@ -102,8 +102,10 @@ sv_status sv_accept_from_logits_floored(const void* target_logits, const void* d
  * hold (the keys at or above each row slice's k-th largest contain every key
  * the filters keep), without a floors pass over the rows; the floors kernel
  * and the floored verification then run for the remaining sequences only.
- * The library takes it for every such batch; SV_FLAG_PLAN_CHAIN refuses it
- * (the two steps on every sequence) and SV_FLAG_PLAN_ROWS is accepted.  Up to
+ * The library takes it for every such batch whose rows are long enough to
+ * hold its candidate lists in their slices' shared memory (about 3700
+ * logits); SV_FLAG_PLAN_CHAIN refuses it (the two steps on every sequence)
+ * and SV_FLAG_PLAN_ROWS is accepted.  Up to
  * three kernel launches on `stream`; the scratch is one slot per stream (a
  * stream beyond the library's four slots gets SV_ERR_UNSUPPORTED), so calls
  * on one stream are ordered and calls on different streams do not share it. */

@@ -164,10 +164,11 @@ def test_repeated_calls_and_force_exact():
 
 
 @pytest.mark.parametrize("V", [200, 257])
-def test_small_vocab_threads_without_logits(V):
-    """A slice shorter than the CTA's 256 threads: the threads that hold no
-    logit enter the per-thread-maxima bound as -Inf, which can only lower the
-    list floor; top-k up to 64 and 1, top-p on and off."""
+def test_small_vocab_takes_the_two_steps(V):
+    """Vocabularies too short for the fused plan (rank 0's receive area, the
+    gathered lists and its work space, must fit where its two slices were:
+    about 3700 16-bit logits per row): the one call falls back to the two
+    steps and must match them; top-k up to 64 and 1, top-p on and off."""
     wl = workloads.make_config("config2", B=12, K=3, V=V)
     top_k = np.array([64, 1, 2, 50, 63, 10] * 2, np.int32)
     top_p = np.array([0.5, 1.0, 0.9, 0.95, 0.3, 1.0] * 2, F32)
